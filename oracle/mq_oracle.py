@@ -1,0 +1,241 @@
+"""CPU oracle for the block-quantized matmul hot path.
+
+TEST INFRASTRUCTURE ONLY. Only tests/, __graft_entry__.smoke() and the
+cpu_baseline / reference leg of bench.py may import this module. The product
+path (the CUDA library and its Python binding) never calls it, and this module
+shares no code, table or constant generator with the CUDA path.
+
+Plain, slow, obviously correct numpy. Floating-point steps that decide an
+integer (the q8 quantization) run in f32, the precision the pages' kernels use;
+dot products run in f64 on dequantized values.
+
+Sources (engineering write-ups of the "minfer" inference engine):
+  [r60]  "64 · r60 — the coronation: flipping the verified gate set to default-on"
+  [r52]  "55 · r52 — skip-write mode 2: skipping the f32 intermediate write-out"
+  [D3-7] "72 · D3-7 — attn_v-q6K MMVQ routing (2b) + rms wide-block / positions memo (2c)"
+
+Readings taken where the pages are silent (each also listed in the design doc):
+  R1  q4_K super-block byte order (the pages only name the type).
+  R2  q6_K super-block byte order.
+  R3  an all-zero activation block has d = 0, q = 0, s = 0.
+  R4  q = rint(v / d) with an IEEE f32 division (not v * (1/d)).
+  R5  rint rounds ties to even.
+  R6  q is clamped to [-127, 127].
+  R7  d is stored as f32 and s as int32.
+  R8  RMSNorm sum-of-squares order: 32 lane partials, lane l serially adding
+      float4 number l, l+32, ...; each float4 contributes
+      ((x0*x0 + x1*x1) + x2*x2) + x3*x3 with separately rounded f32 ops; the 32
+      partials are combined by an xor butterfly at offsets 16, 8, 4, 2, 1.
+  R9  scale = 1 / sqrt(ss / K + eps) with correctly rounded f32 sqrt and divide
+      (the pages use rsqrtf, an approximation with no exact CPU counterpart).
+  R10 SwiGLU uses the platform's f32 exp; planes are compared within +-1 quant
+      level on at most 1e-4 of elements.
+  R11 the GEMM/GEMV error bound is per output element:
+      |gpu - oracle| <= 1e-3 * sum_k |a[m,k]| * |w[n,k]|, a the dequantized q8
+      activation.
+
+Parity pins live in tests/test_oracle.py (closed forms, hand-built blocks,
+invariants, brute force). Parity unpinned: whether R1/R2 match the byte order
+of real GGUF files (no such file is available).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+QK = 32            # activation block length (q8)
+QK_K = 256         # weight super-block length
+Q4K_BYTES = 144    # d (f16), dmin (f16), 12 bytes of packed 6-bit scales/mins, 128 bytes of nibbles
+Q6K_BYTES = 210    # 128 bytes low nibbles, 64 bytes high 2-bit pairs, 16 int8 scales, d (f16)
+
+
+# --------------------------------------------------------------------------- f16
+
+def f16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Decode IEEE binary16 bit patterns to float64 (exact, subnormals included)."""
+    b = np.asarray(bits).astype(np.int64)
+    sign = np.where((b >> 15) & 1, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    m = (b & 0x3FF).astype(np.float64)
+    normal = (1.0 + m / 1024.0) * np.exp2(e.astype(np.float64) - 15.0)
+    sub = m * 2.0 ** -24
+    val = np.where(e == 0, sub, normal)
+    val = np.where(e == 31, np.where(m == 0, np.inf, np.nan), val)
+    return sign * val
+
+
+def _u16_le(lo: np.ndarray, hi: np.ndarray) -> np.ndarray:
+    return lo.astype(np.int64) | (hi.astype(np.int64) << 8)
+
+
+# --------------------------------------------------------------------------- q4_K (R1)
+
+def q4k_scales_mins(packed: np.ndarray):
+    """Unpack the 12-byte scale field of q4_K into 8 six-bit scales and 8 six-bit mins.
+
+    Sub-blocks 0..3 take the low 6 bits of bytes j (scale) and j+4 (min).
+    Sub-blocks 4..7 take a nibble of byte j+4 (low: scale, high: min) and the
+    top two bits of byte j-4 (scale) or byte j (min) as bits 4..5.
+    """
+    q = packed.astype(np.int64)
+    sc = np.zeros(q.shape[:-1] + (8,), np.int64)
+    mn = np.zeros(q.shape[:-1] + (8,), np.int64)
+    for j in range(4):
+        sc[..., j] = q[..., j] & 63
+        mn[..., j] = q[..., j + 4] & 63
+    for j in range(4, 8):
+        sc[..., j] = (q[..., j + 4] & 15) | ((q[..., j - 4] >> 6) << 4)
+        mn[..., j] = (q[..., j + 4] >> 4) | ((q[..., j] >> 6) << 4)
+    return sc, mn
+
+
+def q4k_fields(w: np.ndarray, N: int, K: int):
+    """Split raw q4_K bytes [N, K/256*144] into d, dmin [N,S], sc, mn [N,S,8], q [N,S,256]."""
+    S = K // QK_K
+    blk = np.asarray(w, np.uint8).reshape(N, S, Q4K_BYTES)
+    d = f16_bits_to_f64(_u16_le(blk[..., 0], blk[..., 1]))
+    dmin = f16_bits_to_f64(_u16_le(blk[..., 2], blk[..., 3]))
+    sc, mn = q4k_scales_mins(blk[..., 4:16])
+    qs = blk[..., 16:144].astype(np.int64)
+    q = np.zeros((N, S, QK_K), np.int64)
+    for p in range(4):                       # 32 bytes hold sub-blocks 2p (low) and 2p+1 (high)
+        chunk = qs[..., 32 * p:32 * p + 32]
+        q[..., 64 * p:64 * p + 32] = chunk & 15
+        q[..., 64 * p + 32:64 * p + 64] = chunk >> 4
+    return d, dmin, sc, mn, q
+
+
+def dequant_q4k(w: np.ndarray, N: int, K: int) -> np.ndarray:
+    """w[n,k] = d * sc[j] * q - dmin * m[j], j = (k mod 256) / 32. Returns f64 [N, K]."""
+    d, dmin, sc, mn, q = q4k_fields(w, N, K)
+    j = np.arange(QK_K) // QK
+    out = d[..., None] * sc[..., j] * q - dmin[..., None] * mn[..., j]
+    return out.reshape(N, K)
+
+
+# --------------------------------------------------------------------------- q6_K (R2)
+
+def q6k_fields(w: np.ndarray, N: int, K: int):
+    """Split raw q6_K bytes into d [N,S], int8 scales [N,S,16], 6-bit q [N,S,256]."""
+    S = K // QK_K
+    blk = np.asarray(w, np.uint8).reshape(N, S, Q6K_BYTES)
+    ql = blk[..., 0:128].astype(np.int64)
+    qh = blk[..., 128:192].astype(np.int64)
+    sc = blk[..., 192:208].view(np.int8).astype(np.int64)
+    d = f16_bits_to_f64(_u16_le(blk[..., 208], blk[..., 209]))
+    e = np.arange(QK_K)
+    h, r = e // 128, e % 128          # half of the super-block
+    t, l = r // 32, r % 32            # quarter within the half, position in the quarter
+    low_byte = ql[..., 64 * h + l + 32 * (t & 1)]
+    low = np.where(t < 2, low_byte & 15, low_byte >> 4)
+    high = (qh[..., 32 * h + l] >> (2 * t)) & 3
+    q = low | (high << 4)
+    return d, sc, q
+
+
+def dequant_q6k(w: np.ndarray, N: int, K: int) -> np.ndarray:
+    """w[n,k] = d * sc[g] * (q - 32), g = (k mod 256) / 16. Returns f64 [N, K]."""
+    d, sc, q = q6k_fields(w, N, K)
+    g = np.arange(QK_K) // 16
+    out = d[..., None] * sc[..., g] * (q - 32)
+    return out.reshape(N, K)
+
+
+def dequant(kind: str, w: np.ndarray, N: int, K: int) -> np.ndarray:
+    return {"q4k": dequant_q4k, "q6k": dequant_q6k}[kind](w, N, K)
+
+
+# --------------------------------------------------------------------------- q8 activations
+
+def quantize_q8(v: np.ndarray):
+    """Quantize f32 rows to blocks of 32 ([r52] §2.2; [D3-7] Excerpt C's per-block epilogue).
+
+    Per block: amax = max |v| (exact), d = amax / 127 (f32), q = rint(v / d)
+    clamped to [-127, 127] (R4-R6), s = sum q (int32). d == 0 gives q = 0 (R3).
+    Returns qs int8 [M, K], d f32 [M, K/32], s int32 [M, K/32].
+    """
+    v = np.asarray(v, np.float32)
+    M, K = v.shape
+    blocks = v.reshape(M, K // QK, QK)
+    amax = np.max(np.abs(blocks), axis=-1)
+    d = (amax / np.float32(127.0)).astype(np.float32)
+    nz = d != 0
+    safe = np.where(nz, d, np.float32(1.0)).astype(np.float32)
+    q = np.rint(blocks / safe[..., None])
+    q = np.clip(q, -127, 127)
+    q = np.where(nz[..., None], q, 0).astype(np.int8)
+    s = q.astype(np.int32).sum(axis=-1, dtype=np.int32)
+    return q.reshape(M, K), d, s
+
+
+def dequant_plane(qs: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """a[m,k] = d[m, k/32] * q[m,k] in f64."""
+    M, K = qs.shape
+    return (qs.astype(np.float64).reshape(M, K // QK, QK) * d.astype(np.float64)[..., None]).reshape(M, K)
+
+
+# --------------------------------------------------------------------------- fused producers
+
+def rms_scale(x: np.ndarray, eps: float) -> np.ndarray:
+    """Per-row 1/sqrt(mean(x^2) + eps) in f32, in the R8 order ([r52] §3.2; [D3-7] §2c(i))."""
+    x = np.asarray(x, np.float32)
+    M, K = x.shape
+    f4 = x.reshape(M, K // 128, 32, 4)          # float4 number 32*j + lane
+    lane = np.zeros((M, 32), np.float32)
+    for j in range(K // 128):                   # each lane's serial chain
+        v = f4[:, j]
+        term = ((v[..., 0] * v[..., 0] + v[..., 1] * v[..., 1]) + v[..., 2] * v[..., 2]) + v[..., 3] * v[..., 3]
+        lane = lane + term
+    idx = np.arange(32)
+    for off in (16, 8, 4, 2, 1):                # xor butterfly
+        lane = lane + lane[:, idx ^ off]
+    ss = lane[:, 0]
+    return (np.float32(1.0) / np.sqrt(ss / np.float32(K) + np.float32(eps))).astype(np.float32)
+
+
+def rms_values(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """The f32 RMSNorm output v = (x * scale) * w that the fused producer quantizes."""
+    x = np.asarray(x, np.float32)
+    scale = rms_scale(x, eps)
+    return ((x * scale[:, None]) * np.asarray(w, np.float32)[None, :]).astype(np.float32)
+
+
+def rms_quant(x: np.ndarray, w: np.ndarray, eps: float):
+    """Fused RMSNorm -> q8 plane ([r52] §3.2 mode-2 rms kernel): quantize_q8(rms_values)."""
+    return quantize_q8(rms_values(x, w, eps))
+
+
+def swiglu_values(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """v = (g / (1 + exp(-g))) * u in f32 ([r52] §3.2 mode-2 swiglu kernel; R10)."""
+    g = np.asarray(g, np.float32)
+    u = np.asarray(u, np.float32)
+    with np.errstate(over="ignore"):
+        e = np.exp(-g)
+    return ((g / (np.float32(1.0) + e)) * u).astype(np.float32)
+
+
+def swiglu_quant(g: np.ndarray, u: np.ndarray):
+    """Fused SwiGLU -> q8 plane: quantize_q8(swiglu_values)."""
+    return quantize_q8(swiglu_values(g, u))
+
+
+# --------------------------------------------------------------------------- matmul
+
+def gemm(qs: np.ndarray, d: np.ndarray, w_deq: np.ndarray) -> np.ndarray:
+    """out[m,n] = sum_k (d_a[m,k/32] q_a[m,k]) * w[n,k] in f64 ([r60] §3.2 MMQ dispatch)."""
+    return dequant_plane(qs, d) @ np.asarray(w_deq, np.float64).T
+
+
+def gemm_bound(qs: np.ndarray, d: np.ndarray, w_deq: np.ndarray, rel: float = 1e-3) -> np.ndarray:
+    """Per-element tolerance rel * sum_k |a[m,k]| |w[n,k]| (R11)."""
+    return rel * (np.abs(dequant_plane(qs, d)) @ np.abs(np.asarray(w_deq, np.float64)).T)
+
+
+def gemm_rows(qs, d, w_raw, kind: str, N: int, K: int, rows=None, cols=None):
+    """Oracle GEMM on a subset of output rows / columns (dequantizes only what it needs)."""
+    rows = np.arange(qs.shape[0]) if rows is None else np.asarray(rows)
+    cols = np.arange(N) if cols is None else np.asarray(cols)
+    row_bytes = w_raw.shape[1]
+    wsub = np.asarray(w_raw, np.uint8).reshape(N, row_bytes)[cols]
+    wdeq = dequant(kind, wsub, len(cols), K)
+    a_q, a_d = np.asarray(qs)[rows], np.asarray(d)[rows]
+    return gemm(a_q, a_d, wdeq), gemm_bound(a_q, a_d, wdeq)
