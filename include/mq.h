@@ -1,0 +1,160 @@
+/*
+ * mq.h — C ABI of the GB300 (sm_103a) block-quantized matmul library (libmq.so).
+ *
+ * The library computes the hot path of GGML-style quantized LLM inference:
+ * activations quantized to int8 blocks of 32 (a "q8 plane"), produced either
+ * standalone or fused into RMSNorm / SwiGLU, multiplied against q4_K / q6_K
+ * weight super-blocks (prefill GEMM, decode GEMV).
+ *
+ * Sources (engineering write-ups of the "minfer" inference engine):
+ *   [r60]  "64 · r60 — the coronation: flipping the verified gate set to default-on"
+ *   [r52]  "55 · r52 — skip-write mode 2: skipping the f32 intermediate write-out"
+ *   [D3-7] "72 · D3-7 — attn_v-q6K MMVQ routing (2b) + rms wide-block / positions memo (2c)"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Dimensions: M = tokens (activation rows), K = input features (the
+ *    reduction axis, "id" on the pages), N = output features ("od").
+ *  - Every pointer argument that names tensor data is a DEVICE pointer on the
+ *    current CUDA device. The caller allocates and owns every buffer. The
+ *    library never allocates, frees or synchronizes; it only launches kernels
+ *    asynchronously on `stream` (0 = legacy default stream).
+ *  - Inputs are read only. Outputs (planes, out) are overwritten, never
+ *    accumulated into.
+ *  - K must be a positive multiple of 256 (one weight super-block; it also
+ *    gives the producers whole 8-lane groups, [r52] §3.2). M == 0 or N == 0 is
+ *    a no-op returning MQ_OK.
+ *  - Alignment: every device pointer must be 16-byte aligned.
+ *  - Return value: MQ_OK, or an MQ_ERR_* code from host-side validation,
+ *    returned before anything is launched, or MQ_ERR_LAUNCH when the launch
+ *    itself failed. There is no fallback path. Kernel faults surface, as with
+ *    any CUDA work, at the next synchronizing call.
+ */
+#ifndef MQ_H
+#define MQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    MQ_OK = 0,
+    MQ_ERR_NULL = 1,    /* a required pointer is NULL */
+    MQ_ERR_SHAPE = 2,   /* K not a positive multiple of 256, negative M/N, plane dims mismatch, M != 1 for a GEMV */
+    MQ_ERR_ALIGN = 3,   /* a pointer is not 16-byte aligned */
+    MQ_ERR_ARCH = 4,    /* the current device is not a compute capability 10.3 (GB300) GPU */
+    MQ_ERR_LAUNCH = 5,  /* the CUDA launch (or tensor-map encoding) failed */
+    MQ_ERR_DEVICE = 6   /* a kernel gave up on a bounded wait (reported by mq_device_status) */
+};
+
+/*
+ * q8 activation plane ([r52] §2.2; [D3-7] Excerpt C): for each row m and each
+ * block b of 32 consecutive elements, int8 quants qs, an f32 scale d and the
+ * int32 sum of the block's quants s:
+ *     qs : int8    [M][K]      row-major, row stride K bytes
+ *     d  : float   [M][K/32]   row-major
+ *     s  : int32_t [M][K/32]   row-major
+ * The plane is a pure function of the f32 values it quantizes, so one plane
+ * may feed several GEMMs (Q/K/V, gate/up). The library reads only rows < M;
+ * the GEMM supplies the zero rows of a partial 128-row tile itself.
+ * The struct lives in host memory; only its three pointers are device pointers.
+ */
+typedef struct mq_q8_plane {
+    int8_t*  qs;
+    float*   d;
+    int32_t* s;
+    int M;
+    int K;
+} mq_q8_plane;
+
+/* Bytes of each plane array for an M x K activation. Returns the total. Pure host helper. */
+size_t mq_plane_bytes(int M, int K, size_t* qs_bytes, size_t* d_bytes, size_t* s_bytes);
+
+/*
+ * Bytes of one weight row (K/256 super-blocks):
+ *   q4_K super-block, 144 B: f16 d, f16 dmin, 12 B of packed 6-bit scales and
+ *     mins for eight 32-element sub-blocks, 128 B of 4-bit quants;
+ *   q6_K super-block, 210 B: 128 B low 4 bits, 64 B high 2 bits, 16 int8
+ *     scales (one per 16 elements), f16 d.
+ * ([r60] §3.2 names the types; the byte order is the library's documented
+ * reading, the public GGUF order.) Weights are N rows x K/256 super-blocks, row-major,
+ * rows packed back to back (row stride = the value returned here).
+ */
+size_t mq_q4k_row_bytes(int K);
+size_t mq_q6k_row_bytes(int K);
+
+/*
+ * mq_quantize_q8 — standalone activation quantization ([r52] §2.2; [D3-7]
+ * Excerpt C, the per-32-block epilogue; [D3-7] Excerpt A2, the decode
+ * quantize). x: f32 [M][K] row-major. For every block of 32:
+ *     amax = max|v|; d = amax / 127 (f32); q = rint(v / d) (IEEE f32 divide,
+ *     ties to even) clamped to [-127, 127]; s = sum q; an all-zero block gives
+ *     d = 0, q = 0, s = 0.
+ * out->M, out->K must equal M, K. Input values must be finite.
+ */
+int mq_quantize_q8(const float* x, int M, int K, const mq_q8_plane* out, cudaStream_t stream);
+
+/*
+ * mq_rms_quant — fused RMSNorm -> q8 plane that never writes the f32
+ * normalized rows ([r52] §3.2, the mode-2 rms kernel; [D3-7] §2c(i) and
+ * Excerpt C for the single-row decode shape). x: f32 [M][K], w: f32 [K].
+ *     ss = sum x^2 in a fixed order (32 lane partials over float4 l, l+32, ...;
+ *          each float4 adds ((x0*x0 + x1*x1) + x2*x2) + x3*x3; xor butterfly),
+ *     scale = 1 / sqrt(ss / K + eps) (correctly rounded f32 ops),
+ *     v = (x * scale) * w, then the mq_quantize_q8 block rule on v.
+ * The result is bit-identical to quantizing the f32 RMSNorm output computed in
+ * that order.
+ */
+int mq_rms_quant(const float* x, const float* w, int M, int K, float eps,
+                 const mq_q8_plane* out, cudaStream_t stream);
+
+/*
+ * mq_swiglu_quant — fused SwiGLU -> q8 plane that never writes the f32
+ * product ([r52] §3.2, the mode-2 swiglu kernel). g, u: f32 [M][K].
+ *     v = (g / (1 + expf(-g))) * u, then the mq_quantize_q8 block rule on v.
+ */
+int mq_swiglu_quant(const float* g, const float* u, int M, int K,
+                    const mq_q8_plane* out, cudaStream_t stream);
+
+/*
+ * mq_gemm_q4k / mq_gemm_q6k — prefill matmul of a q8 plane by super-block
+ * weights ([r60] §3.1 and §3.2, the MMQ dispatch for nt >= 16; q6_K "runs as
+ * k32 chunks with dual 16-sub rescale"):
+ *     out[m][n] = sum_k (d_a[m][k/32] * q_a[m][k]) * w[n][k]
+ * with w the dequantized weight (q4_K: d*sc*q - dmin*m per 32; q6_K:
+ * d*sc*(q-32) per 16). a: plane with a->M >= 1 rows and a->K = K; w: N rows of
+ * super-blocks; out: f32 [a->M][N] row-major, overwritten. Any M >= 1 is
+ * accepted (the kernel is built for M >= 16). Accuracy: within
+ * 1e-3 * sum_k |a||w| per element.
+ */
+int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+
+/*
+ * mq_gemv_q4k / mq_gemv_q6k — decode matrix-vector product (M == 1)
+ * ([D3-7] §2 (2b) and Excerpt A/A2, the MMVQ decode path): the same result as
+ * the GEMM with a->M == 1. out: f32 [N]. Returns MQ_ERR_SHAPE if a->M != 1.
+ */
+int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+
+/*
+ * mq_device_status — synchronizes `stream`, then returns MQ_OK if no kernel of
+ * this library launched so far on the current device has given up on a
+ * bounded wait, else MQ_ERR_DEVICE, and clears the record. Returns
+ * MQ_ERR_LAUNCH if the synchronization itself reports a CUDA error.
+ */
+int mq_device_status(cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mq_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MQ_H */

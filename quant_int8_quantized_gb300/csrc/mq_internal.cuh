@@ -1,0 +1,84 @@
+// Internal helpers shared by the libmq CUDA translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "mq.h"
+
+namespace mq {
+
+constexpr int QK = 32;          // activation block
+constexpr int QK_K = 256;       // weight super-block
+constexpr int Q4K_BYTES = 144;
+constexpr int Q6K_BYTES = 210;
+
+// Host-side validation helpers ------------------------------------------------
+
+int check_arch();   // MQ_OK if the current device is compute capability 10.3
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int check_plane(const mq_q8_plane* p, int M, int K) {
+    if (!p) return MQ_ERR_NULL;
+    if (p->M != M || p->K != K) return MQ_ERR_SHAPE;
+    if (M == 0) return MQ_OK;
+    if (!p->qs || !p->d || !p->s) return MQ_ERR_NULL;
+    if (!aligned16(p->qs) || !aligned16(p->d) || !aligned16(p->s)) return MQ_ERR_ALIGN;
+    return MQ_OK;
+}
+
+inline bool valid_k(int K) { return K > 0 && (K % QK_K) == 0; }
+
+inline int launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MQ_OK : MQ_ERR_LAUNCH;
+}
+
+int num_sms();      // SM count of the current device (cached)
+
+// Device-side failure record (bounded waits) -----------------------------------
+// Each translation unit with bounded waits owns one word; these read and clear it.
+int take_gemm_device_error(cudaStream_t stream, unsigned* code);
+
+}  // namespace mq
+
+// Device helpers -----------------------------------------------------------------
+
+__device__ __forceinline__ float mq_f16_to_f32(uint16_t h) {
+    float f;
+    asm("{ .reg .f16 t; mov.b16 t, %1; cvt.f32.f16 %0, t; }" : "=f"(f) : "h"(h));
+    return f;
+}
+
+// Quantize four f32 values that belong to one 32-block whose 8 owners are the
+// lanes of one aligned 8-lane group. amax and the int sum are combined with xor
+// shuffles at offsets 4, 2, 1 (max and integer sums are exact in any order).
+// Returns the packed int8 quants; d and s are valid in every lane of the group.
+__device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v2, float v3,
+                                                     float& d_out, int& s_out) {
+    float am = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    const float d = __fdiv_rn(am, 127.0f);
+    int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+    if (d != 0.0f) {
+        q0 = __float2int_rn(__fdiv_rn(v0, d));
+        q1 = __float2int_rn(__fdiv_rn(v1, d));
+        q2 = __float2int_rn(__fdiv_rn(v2, d));
+        q3 = __float2int_rn(__fdiv_rn(v3, d));
+        q0 = max(-127, min(127, q0));
+        q1 = max(-127, min(127, q1));
+        q2 = max(-127, min(127, q2));
+        q3 = max(-127, min(127, q3));
+    }
+    int s = (q0 + q1) + (q2 + q3);
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    d_out = d;
+    s_out = s;
+    return (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) | ((uint32_t)(q2 & 0xff) << 16) |
+           ((uint32_t)(q3 & 0xff) << 24);
+}

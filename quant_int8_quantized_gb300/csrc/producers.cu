@@ -1,0 +1,229 @@
+// q8 plane producers: standalone quantize, fused RMSNorm -> q8, fused SwiGLU -> q8.
+//
+// All three share the lane mapping of the pages' mode-2 kernels ("55 · r52 —
+// skip-write mode 2", §3.2): a warp sweeps 128 consecutive floats per round,
+// lane l owns float4 number l, so the 8 lanes of group l>>3 own one 32-block
+// (block index 4*round + (l>>3)). amax and the int sum of a block are reduced
+// with xor shuffles at 4, 2, 1 — exact in any order ("55 · r52", §2.2). Loads
+// and the qs store of a round are 512 B / 128 B coalesced warp accesses
+// ("55 · r52", §3.3 pitfall 2). No f32 intermediate is ever written.
+//
+// HBM roofline: quantize reads 4 B and writes 1.25 B per element; rms reads
+// 4 B (x) and writes 1.25 B; swiglu reads 8 B (g, u) and writes 1.25 B.
+
+#include "mq_internal.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRoundsPerIter = 4;   // float4 loads in flight per lane
+
+__device__ __forceinline__ void store_round(uint32_t* __restrict__ qs, float* __restrict__ d,
+                                            int32_t* __restrict__ s, long long round, int lane,
+                                            uint32_t q, float dd, int ss) {
+    qs[round * 32 + lane] = q;
+    if ((lane & 7) == 0) {
+        const long long b = round * 4 + (lane >> 3);
+        d[b] = dd;
+        s[b] = ss;
+    }
+}
+
+// x is viewed as a flat array of M*K floats (rows are contiguous, K % 128 == 0),
+// so every round lies inside one row and the plane arrays are flat too.
+__global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __restrict__ x,
+                                                               uint32_t* __restrict__ qs,
+                                                               float* __restrict__ d,
+                                                               int32_t* __restrict__ s,
+                                                               long long rounds) {
+    const int lane = threadIdx.x & 31;
+    const long long warp = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * kThreads) >> 5;
+    for (long long r0 = warp * kRoundsPerIter; r0 < rounds; r0 += nwarps * kRoundsPerIter) {
+        float4 v[kRoundsPerIter];
+#pragma unroll
+        for (int u = 0; u < kRoundsPerIter; ++u)
+            if (r0 + u < rounds) v[u] = __ldcs(x + (r0 + u) * 32 + lane);
+#pragma unroll
+        for (int u = 0; u < kRoundsPerIter; ++u) {
+            if (r0 + u < rounds) {   // warp-uniform
+                float dd;
+                int ss;
+                const uint32_t q = mq_quant4_group8(v[u].x, v[u].y, v[u].z, v[u].w, dd, ss);
+                store_round(qs, d, s, r0 + u, lane, q, dd, ss);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    // (g / (1 + expf(-g))) * u, each step a correctly rounded f32 op except expf.
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+__global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __restrict__ g,
+                                                                const float4* __restrict__ u,
+                                                                uint32_t* __restrict__ qs,
+                                                                float* __restrict__ d,
+                                                                int32_t* __restrict__ s,
+                                                                long long rounds) {
+    const int lane = threadIdx.x & 31;
+    const long long warp = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
+    const long long nwarps = ((long long)gridDim.x * kThreads) >> 5;
+    for (long long r0 = warp * kRoundsPerIter; r0 < rounds; r0 += nwarps * kRoundsPerIter) {
+        float4 gv[kRoundsPerIter], uv[kRoundsPerIter];
+#pragma unroll
+        for (int k = 0; k < kRoundsPerIter; ++k) {
+            if (r0 + k < rounds) {
+                gv[k] = __ldcs(g + (r0 + k) * 32 + lane);
+                uv[k] = __ldcs(u + (r0 + k) * 32 + lane);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kRoundsPerIter; ++k) {
+            if (r0 + k < rounds) {
+                float dd;
+                int ss;
+                const uint32_t q = mq_quant4_group8(silu_mul(gv[k].x, uv[k].x), silu_mul(gv[k].y, uv[k].y),
+                                                    silu_mul(gv[k].z, uv[k].z), silu_mul(gv[k].w, uv[k].w),
+                                                    dd, ss);
+                store_round(qs, d, s, r0 + k, lane, q, dd, ss);
+            }
+        }
+    }
+}
+
+// RMSNorm scale of one row, computed by one full warp in the fixed order:
+// lane l serially adds float4 l, l+32, ... (each as ((x0*x0 + x1*x1) + x2*x2) +
+// x3*x3, every op separately rounded), then an xor butterfly 16, 8, 4, 2, 1.
+// ("55 · r52", §3.2 phase 1; "72 · D3-7", §2c(i) and Excerpt C.)
+__device__ __forceinline__ float rms_scale_warp(const float4* __restrict__ xr, int K, float eps, int lane) {
+    const int K4 = K >> 2;
+    float ss = 0.0f;
+#pragma unroll 8
+    for (int i = lane; i < K4; i += 32) {
+        const float4 v = __ldg(xr + i);
+        float t = __fadd_rn(__fmul_rn(v.x, v.x), __fmul_rn(v.y, v.y));
+        t = __fadd_rn(t, __fmul_rn(v.z, v.z));
+        t = __fadd_rn(t, __fmul_rn(v.w, v.w));
+        ss = __fadd_rn(ss, t);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+}
+
+__device__ __forceinline__ void rms_quant_rounds(const float4* __restrict__ xr, const float4* __restrict__ w4,
+                                                 uint32_t* __restrict__ qs, float* __restrict__ d,
+                                                 int32_t* __restrict__ s, long long row_round0, int k0,
+                                                 int kstep, int nrounds, float scale, int lane) {
+#pragma unroll 4
+    for (int k = k0; k < nrounds; k += kstep) {
+        const float4 xv = __ldg(xr + k * 32 + lane);
+        const float4 wv = __ldg(w4 + k * 32 + lane);
+        float dd;
+        int ss;
+        const uint32_t q = mq_quant4_group8(__fmul_rn(__fmul_rn(xv.x, scale), wv.x),
+                                            __fmul_rn(__fmul_rn(xv.y, scale), wv.y),
+                                            __fmul_rn(__fmul_rn(xv.z, scale), wv.z),
+                                            __fmul_rn(__fmul_rn(xv.w, scale), wv.w), dd, ss);
+        store_round(qs, d, s, row_round0 + k, lane, q, dd, ss);
+    }
+}
+
+// Many rows: one warp per row (8 rows per block).
+__global__ void __launch_bounds__(kThreads) rms_quant_rows_kernel(const float4* __restrict__ x,
+                                                                  const float4* __restrict__ w4,
+                                                                  uint32_t* __restrict__ qs,
+                                                                  float* __restrict__ d,
+                                                                  int32_t* __restrict__ s, int M, int K,
+                                                                  float eps) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (row >= M) return;   // warp-uniform
+    const int nrounds = K >> 7;
+    const float4* xr = x + (long long)row * (K >> 2);
+    const float scale = rms_scale_warp(xr, K, eps, lane);
+    rms_quant_rounds(xr, w4, qs, d, s, (long long)row * nrounds, 0, 1, nrounds, scale, lane);
+}
+
+// Few rows (decode): one 128-thread block per row. Warp 0 computes the scale in
+// the same order as above and broadcasts it through shared memory; all four
+// warps then quantize interleaved rounds ("72 · D3-7", §2c(i), Excerpt C).
+__global__ void __launch_bounds__(128) rms_quant_wide_kernel(const float4* __restrict__ x,
+                                                             const float4* __restrict__ w4,
+                                                             uint32_t* __restrict__ qs,
+                                                             float* __restrict__ d,
+                                                             int32_t* __restrict__ s, int M, int K,
+                                                             float eps) {
+    __shared__ float s_scale;
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5;
+    const int row = blockIdx.x;
+    const float4* xr = x + (long long)row * (K >> 2);
+    if (wid == 0) {
+        const float sc = rms_scale_warp(xr, K, eps, lane);
+        if (lane == 0) s_scale = sc;
+    }
+    __syncthreads();
+    const int nrounds = K >> 7;
+    rms_quant_rounds(xr, w4, qs, d, s, (long long)row * nrounds, wid, 4, nrounds, s_scale, lane);
+}
+
+int flat_grid(long long rounds) {
+    const long long per_block = (kThreads / 32) * kRoundsPerIter;
+    long long blocks = (rounds + per_block - 1) / per_block;
+    const long long cap = (long long)mq::num_sms() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    return (int)blocks;
+}
+
+int check_producer(const void* a, const void* b, int M, int K, const mq_q8_plane* out) {
+    if (M < 0 || !mq::valid_k(K)) return MQ_ERR_SHAPE;
+    int rc = mq::check_plane(out, M, K);
+    if (rc != MQ_OK || M == 0) return rc;
+    if (!a || !b) return MQ_ERR_NULL;
+    if (!mq::aligned16(a) || !mq::aligned16(b)) return MQ_ERR_ALIGN;
+    return mq::check_arch();
+}
+
+}  // namespace
+
+extern "C" int mq_quantize_q8(const float* x, int M, int K, const mq_q8_plane* out, cudaStream_t stream) {
+    int rc = check_producer(x, x, M, K, out);
+    if (rc != MQ_OK || M == 0) return rc;
+    const long long rounds = (long long)M * K / 128;
+    quantize_q8_kernel<<<flat_grid(rounds), kThreads, 0, stream>>>(
+        reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(out->qs), out->d, out->s, rounds);
+    return mq::launch_status();
+}
+
+extern "C" int mq_swiglu_quant(const float* g, const float* u, int M, int K, const mq_q8_plane* out,
+                               cudaStream_t stream) {
+    int rc = check_producer(g, u, M, K, out);
+    if (rc != MQ_OK || M == 0) return rc;
+    const long long rounds = (long long)M * K / 128;
+    swiglu_quant_kernel<<<flat_grid(rounds), kThreads, 0, stream>>>(
+        reinterpret_cast<const float4*>(g), reinterpret_cast<const float4*>(u),
+        reinterpret_cast<uint32_t*>(out->qs), out->d, out->s, rounds);
+    return mq::launch_status();
+}
+
+extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float eps, const mq_q8_plane* out,
+                            cudaStream_t stream) {
+    int rc = check_producer(x, w, M, K, out);
+    if (rc != MQ_OK || M == 0) return rc;
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    const float4* w4 = reinterpret_cast<const float4*>(w);
+    uint32_t* qs = reinterpret_cast<uint32_t*>(out->qs);
+    // One warp per row fills the machine once there are a few warps per SM.
+    if (M >= 4 * mq::num_sms()) {
+        const int rows_per_block = kThreads / 32;
+        rms_quant_rows_kernel<<<(M + rows_per_block - 1) / rows_per_block, kThreads, 0, stream>>>(
+            x4, w4, qs, out->d, out->s, M, K, eps);
+    } else {
+        rms_quant_wide_kernel<<<M, 128, 0, stream>>>(x4, w4, qs, out->d, out->s, M, K, eps);
+    }
+    return mq::launch_status();
+}

@@ -1,0 +1,198 @@
+"""Thin ctypes binding of libmq.so (include/mq.h), with the same entry-point names.
+
+Argument marshalling only: torch tensors are checked for device, dtype and
+contiguity, their data pointers and the current CUDA stream are passed to the
+C ABI, and a non-zero status raises MQError. Every step of the computation
+runs in the library's CUDA kernels; there is no other code path. If the
+library has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libmq.so")
+
+MQ_OK, MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_ARCH, MQ_ERR_LAUNCH, MQ_ERR_DEVICE = range(7)
+
+EXPORTED = ["mq_plane_bytes", "mq_q4k_row_bytes", "mq_q6k_row_bytes", "mq_quantize_q8", "mq_rms_quant",
+            "mq_swiglu_quant", "mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k",
+            "mq_device_status", "mq_status_str"]
+
+
+class MQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_str(status)} (status {status})")
+
+
+class CPlane(ctypes.Structure):
+    _fields_ = [("qs", ctypes.c_void_p), ("d", ctypes.c_void_p), ("s", ctypes.c_void_p),
+                ("M", ctypes.c_int), ("K", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        pp = ctypes.POINTER(CPlane)
+        psz = ctypes.POINTER(ctypes.c_size_t)
+        sig = {
+            "mq_plane_bytes": (sz, [i, i, psz, psz, psz]),
+            "mq_q4k_row_bytes": (sz, [i]),
+            "mq_q6k_row_bytes": (sz, [i]),
+            "mq_quantize_q8": (i, [vp, i, i, pp, vp]),
+            "mq_rms_quant": (i, [vp, vp, i, i, f, pp, vp]),
+            "mq_swiglu_quant": (i, [vp, vp, i, i, pp, vp]),
+            "mq_gemm_q4k": (i, [pp, vp, i, vp, vp]),
+            "mq_gemm_q6k": (i, [pp, vp, i, vp, vp]),
+            "mq_gemv_q4k": (i, [pp, vp, i, vp, vp]),
+            "mq_gemv_q6k": (i, [pp, vp, i, vp, vp]),
+            "mq_device_status": (i, [vp]),
+            "mq_status_str": (ctypes.c_char_p, [i]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().mq_status_str(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(status: int, where: str):
+    if status != MQ_OK:
+        raise MQError(status, where)
+
+
+def _dev_tensor(t, dtype, name):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class Plane:
+    """Device q8 plane: qs int8 [M, K], d f32 [M, K/32], s int32 [M, K/32]."""
+
+    def __init__(self, qs: torch.Tensor, d: torch.Tensor, s: torch.Tensor):
+        self.qs, self.d, self.s = qs, d, s
+        self.M, self.K = int(qs.shape[0]), int(qs.shape[1])
+        _dev_tensor(qs, torch.int8, "plane.qs")
+        _dev_tensor(d, torch.float32, "plane.d")
+        _dev_tensor(s, torch.int32, "plane.s")
+
+    @classmethod
+    def empty(cls, M: int, K: int, device="cuda") -> "Plane":
+        return cls(torch.empty((M, K), dtype=torch.int8, device=device),
+                   torch.empty((M, K // 32), dtype=torch.float32, device=device),
+                   torch.empty((M, K // 32), dtype=torch.int32, device=device))
+
+    def c(self) -> CPlane:
+        return CPlane(self.qs.data_ptr(), self.d.data_ptr(), self.s.data_ptr(), self.M, self.K)
+
+
+def mq_plane_bytes(M: int, K: int):
+    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    tot = lib().mq_plane_bytes(M, K, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+    return int(tot), int(a.value), int(b.value), int(c.value)
+
+
+def mq_q4k_row_bytes(K: int) -> int:
+    return int(lib().mq_q4k_row_bytes(K))
+
+
+def mq_q6k_row_bytes(K: int) -> int:
+    return int(lib().mq_q6k_row_bytes(K))
+
+
+def mq_quantize_q8(x: torch.Tensor, out: Plane, stream=None) -> Plane:
+    _dev_tensor(x, torch.float32, "x")
+    cp = out.c()
+    _check(lib().mq_quantize_q8(_ptr(x), x.shape[0], x.shape[1], ctypes.byref(cp), _stream(stream)),
+           "mq_quantize_q8")
+    return out
+
+
+def mq_rms_quant(x: torch.Tensor, w: torch.Tensor, eps: float, out: Plane, stream=None) -> Plane:
+    _dev_tensor(x, torch.float32, "x")
+    _dev_tensor(w, torch.float32, "w")
+    cp = out.c()
+    _check(lib().mq_rms_quant(_ptr(x), _ptr(w), x.shape[0], x.shape[1], float(eps), ctypes.byref(cp),
+                              _stream(stream)), "mq_rms_quant")
+    return out
+
+
+def mq_swiglu_quant(g: torch.Tensor, u: torch.Tensor, out: Plane, stream=None) -> Plane:
+    _dev_tensor(g, torch.float32, "g")
+    _dev_tensor(u, torch.float32, "u")
+    if g.shape != u.shape:
+        raise ValueError("g and u must have the same shape")
+    cp = out.c()
+    _check(lib().mq_swiglu_quant(_ptr(g), _ptr(u), g.shape[0], g.shape[1], ctypes.byref(cp), _stream(stream)),
+           "mq_swiglu_quant")
+    return out
+
+
+def _matmul(fn_name: str, a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream):
+    _dev_tensor(w, torch.uint8, "w")
+    _dev_tensor(out, torch.float32, "out")
+    cp = a.c()
+    _check(getattr(lib(), fn_name)(ctypes.byref(cp), _ptr(w), int(N), _ptr(out), _stream(stream)), fn_name)
+    return out
+
+
+def mq_gemm_q4k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return _matmul("mq_gemm_q4k", a, w, N, out, stream)
+
+
+def mq_gemm_q6k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return _matmul("mq_gemm_q6k", a, w, N, out, stream)
+
+
+def mq_gemv_q4k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return _matmul("mq_gemv_q4k", a, w, N, out, stream)
+
+
+def mq_gemv_q6k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return _matmul("mq_gemv_q6k", a, w, N, out, stream)
+
+
+def mq_device_status(stream=None) -> int:
+    return int(lib().mq_device_status(_stream(stream)))
+
+
+def gemm(kind: str, a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k}[kind](a, w, N, out, stream)
+
+
+def gemv(kind: str, a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return {"q4k": mq_gemv_q4k, "q6k": mq_gemv_q6k}[kind](a, w, N, out, stream)

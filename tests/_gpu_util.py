@@ -1,0 +1,75 @@
+"""Helpers for the GPU parity tests: guarded, poisoned device buffers and
+plane comparisons against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+from quant_int8_quantized_gb300 import mq
+
+POISON = 0xCD
+GUARD = 256   # bytes of guard band on each side of a buffer
+
+
+def require_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from quant_int8_quantized_gb300 import build as B
+    B.build()
+    mq.lib()
+
+
+class Guarded:
+    """A device tensor carved out of a larger poisoned byte buffer.
+
+    Every byte of the buffer starts as 0xCD; `check()` asserts that the guard
+    bands before and after the tensor are untouched (no out-of-bounds write),
+    and `untouched()` counts tensor bytes still equal to the poison (no write).
+    """
+
+    def __init__(self, shape, dtype, device="cuda"):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        self.nbytes = n
+        self.raw = torch.full((n + 2 * GUARD,), POISON, dtype=torch.uint8, device=device)
+        self.t = self.raw[GUARD:GUARD + n].view(dtype).view(shape) if n else torch.empty(shape, dtype=dtype, device=device)
+
+    def check(self):
+        raw = self.raw.cpu().numpy()
+        assert np.all(raw[:GUARD] == POISON), "write before the buffer"
+        assert np.all(raw[GUARD + self.nbytes:] == POISON), "write after the buffer"
+
+
+class GuardedPlane:
+    def __init__(self, M, K):
+        self.g = [Guarded((M, K), torch.int8), Guarded((M, K // 32), torch.float32),
+                  Guarded((M, K // 32), torch.int32)]
+        self.plane = mq.Plane(self.g[0].t, self.g[1].t, self.g[2].t)
+
+    def check(self):
+        for g in self.g:
+            g.check()
+
+    def numpy(self):
+        return (self.plane.qs.cpu().numpy(), self.plane.d.cpu().numpy(), self.plane.s.cpu().numpy())
+
+
+def assert_plane_equal(got, ref, what=""):
+    qs, d, s = got
+    rq, rd, rs = ref
+    assert qs.shape == rq.shape and d.shape == rd.shape
+    bad = np.argwhere(qs != rq)
+    assert bad.size == 0, f"{what}: {len(bad)} qs mismatches, first at {bad[:5].tolist()}"
+    assert np.array_equal(d.view(np.uint32), rd.view(np.uint32)), f"{what}: d differs"
+    assert np.array_equal(s, rs), f"{what}: s differs"
+
+
+def assert_plane_close(got, ref, max_frac=1e-4, what=""):
+    """+-1 quant level on at most max_frac of elements; d within 2^-20 relative; s consistent."""
+    qs, d, s = got
+    rq, rd, rs = ref
+    diff = np.abs(qs.astype(np.int32) - rq.astype(np.int32))
+    assert diff.max(initial=0) <= 1, f"{what}: a quant differs by {diff.max()}"
+    frac = np.count_nonzero(diff) / max(1, diff.size)
+    assert frac <= max_frac, f"{what}: {frac:.2e} of quants differ"
+    rel = np.abs(d.astype(np.float64) - rd) / np.maximum(np.abs(rd.astype(np.float64)), 1e-38)
+    assert rel.max(initial=0) <= 2.0 ** -20, f"{what}: d differs by {rel.max():.3e} relative"
+    assert np.array_equal(s, qs.reshape(qs.shape[0], -1, 32).astype(np.int32).sum(-1)), f"{what}: s != sum q"

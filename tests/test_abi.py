@@ -1,0 +1,105 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads and
+exports every entry point include/mq.h declares; size helpers and the
+validation that runs before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from quant_int8_quantized_gb300 import build as B
+from quant_int8_quantized_gb300 import mq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    B.build()
+    return mq.lib()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(mq_\w+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert {"mq_quantize_q8", "mq_rms_quant", "mq_swiglu_quant", "mq_gemm_q4k", "mq_gemm_q6k",
+            "mq_gemv_q4k", "mq_gemv_q6k"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+    assert names <= set(mq.EXPORTED) | names  # the binding wraps what it knows
+
+
+def test_binding_covers_every_declared_symbol(L):
+    assert declared_functions() <= set(mq.EXPORTED)
+
+
+def test_size_helpers(L):
+    tot, qs, d, s = mq.mq_plane_bytes(3314, 3584)
+    assert (qs, d, s) == (3314 * 3584, 3314 * 112 * 4, 3314 * 112 * 4) and tot == qs + d + s
+    assert mq.mq_q4k_row_bytes(3584) == 14 * 144
+    assert mq.mq_q6k_row_bytes(18944) == 74 * 210
+
+
+def test_status_strings(L):
+    for code in range(7):
+        assert mq.status_str(code).startswith("MQ_")
+    assert "UNKNOWN" in mq.status_str(99)
+
+
+def _plane(M, K, qs=1, d=1, s=1):
+    return mq.CPlane(qs, d, s, M, K)
+
+
+def test_validation_before_any_cuda_call(L):
+    null = None
+    # K not a positive multiple of 256
+    p = _plane(4, 100)
+    assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 100, ctypes.byref(p), null) == mq.MQ_ERR_SHAPE
+    p = _plane(4, 0)
+    assert L.mq_rms_quant(ctypes.c_void_p(16), ctypes.c_void_p(16), 4, 0, 1e-6, ctypes.byref(p), null) == mq.MQ_ERR_SHAPE
+    # negative M
+    p = _plane(-1, 256)
+    assert L.mq_swiglu_quant(ctypes.c_void_p(16), ctypes.c_void_p(16), -1, 256, ctypes.byref(p), null) == mq.MQ_ERR_SHAPE
+    # NULL plane
+    assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 256, None, null) == mq.MQ_ERR_NULL
+    # plane dims disagree with the call
+    p = _plane(5, 256)
+    assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 256, ctypes.byref(p), null) == mq.MQ_ERR_SHAPE
+    # empty input is a no-op
+    p = _plane(0, 256, 0, 0, 0)
+    assert L.mq_quantize_q8(None, 0, 256, ctypes.byref(p), null) == mq.MQ_OK
+    # NULL plane arrays / inputs, misaligned pointers
+    p = _plane(4, 256, 0, 16, 16)
+    assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 256, ctypes.byref(p), null) == mq.MQ_ERR_NULL
+    p = _plane(4, 256, 16, 16, 16)
+    assert L.mq_quantize_q8(None, 4, 256, ctypes.byref(p), null) == mq.MQ_ERR_NULL
+    p = _plane(4, 256, 17, 16, 16)
+    assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 256, ctypes.byref(p), null) == mq.MQ_ERR_ALIGN
+    p = _plane(4, 256, 16, 16, 16)
+    assert L.mq_quantize_q8(ctypes.c_void_p(20), 4, 256, ctypes.byref(p), null) == mq.MQ_ERR_ALIGN
+
+
+def test_matmul_validation_before_any_cuda_call(L):
+    null = None
+    p = _plane(2, 512, 16, 16, 16)
+    for fn in (L.mq_gemv_q4k, L.mq_gemv_q6k):
+        assert fn(ctypes.byref(p), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE  # M != 1
+    p1 = _plane(1, 512, 16, 16, 16)
+    for fn in (L.mq_gemm_q4k, L.mq_gemm_q6k, L.mq_gemv_q4k, L.mq_gemv_q6k):
+        assert fn(None, ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
+        assert fn(ctypes.byref(p1), None, 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
+        assert fn(ctypes.byref(p1), ctypes.c_void_p(16), 8, None, null) == mq.MQ_ERR_NULL
+        assert fn(ctypes.byref(p1), ctypes.c_void_p(24), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_ALIGN
+        assert fn(ctypes.byref(p1), ctypes.c_void_p(16), -1, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE
+        assert fn(ctypes.byref(p1), ctypes.c_void_p(16), 0, None, null) == mq.MQ_OK      # N == 0: no-op
+    bad = _plane(1, 300, 16, 16, 16)
+    assert L.mq_gemm_q4k(ctypes.byref(bad), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE

@@ -1,0 +1,128 @@
+"""Parity of the prefill GEMM and decode GEMV (CUDA, through the C ABI) with the
+CPU oracle: every output element within 1e-3 * sum_k |a||w| of the f64
+reference, on seeded inputs whose sizes span several tiles and a ragged tail,
+plus full-size shapes checked on sampled rows."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mq_oracle as O
+from quant_int8_quantized_gb300 import mq, synth
+from tests._gpu_util import Guarded, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _plane_from(x):
+    M, K = x.shape
+    p = mq.Plane.empty(M, K)
+    mq.mq_quantize_q8(x.cuda(), p)
+    return p
+
+
+def _check(out, plane, w, kind, N, K, rows=None, slack=0.0):
+    qs, d = plane.qs.cpu().numpy(), plane.d.cpu().numpy()
+    ref, bound = O.gemm_rows(qs, d, w.cpu().numpy(), kind, N, K, rows=rows)
+    got = out.cpu().numpy().astype(np.float64)
+    if rows is not None:
+        got = got[rows]
+    err = np.abs(got - ref)
+    worst = np.max(err / np.maximum(bound, 1e-30))
+    assert np.all(err <= bound + slack), f"{kind}: max err/bound = {worst:.3g}"
+    return worst
+
+
+def _run(kind, x, N, K, fn, outliers_name=None):
+    w = synth.weights(kind, N, K, 0, f"{kind}.{N}x{K}")
+    p = _plane_from(x)
+    g = Guarded((x.shape[0], N), torch.float32)
+    fn(kind, p, w.cuda(), N, g.t)
+    torch.cuda.synchronize()
+    g.check()
+    return g.t, p, w
+
+
+# ----------------------------------------------------------------- GEMM
+
+GEMM_SHAPES = [
+    (16, 256, 512),      # the tiny single matmul: 16 rows x 256 outputs x 512
+    (1, 8, 256),
+    (5, 100, 768),       # odd super-block count (q6_K rows only 2-byte aligned)
+    (130, 300, 512),     # ragged in M and N, several tiles
+    (257, 129, 1280),
+]
+
+
+@pytest.mark.parametrize("kind", ["q4k", "q6k"])
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+def test_gemm_parity(kind, M, N, K):
+    x = synth.normal((M, K), 0, f"gx{M}x{K}")
+    out, p, w = _run(kind, x, N, K, mq.gemm)
+    _check(out, p, w, kind, N, K)
+
+
+@pytest.mark.parametrize("kind", ["q4k", "q6k"])
+def test_gemm_outlier_activations(kind):
+    M, N, K = 64, 192, 1024
+    x = synth.with_outliers(synth.normal((M, K), 0, "ox"), 0, "ox")
+    out, p, w = _run(kind, x, N, K, mq.gemm)
+    _check(out, p, w, kind, N, K)
+
+
+@pytest.mark.parametrize("kind,N,K", [("q4k", 18944, 3584), ("q6k", 3584, 18944), ("q4k", 512, 3584)])
+def test_gemm_full_size_sampled_rows(kind, N, K):
+    """7B prefill shapes at M = 3314, oracle on 24 sampled rows (rows are independent)."""
+    M = 3314
+    x = synth.normal((M, K), 0, f"fx{K}", device="cuda")
+    w = synth.weights(kind, N, K, 0, f"fw{kind}{N}", device="cuda")
+    p = mq.Plane.empty(M, K)
+    mq.mq_quantize_q8(x, p)
+    out = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    mq.gemm(kind, p, w, N, out)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(1).choice(M, 24, replace=False))
+    rows[-1] = M - 1
+    _check(out, p, w, kind, N, K, rows=rows)
+    assert mq.mq_device_status() == mq.MQ_OK
+
+
+# ----------------------------------------------------------------- GEMV
+
+GEMV_SHAPES = [(256, 512), (1024, 5120), (100, 768), (5120, 13824), (1, 256)]
+
+
+@pytest.mark.parametrize("kind", ["q4k", "q6k"])
+@pytest.mark.parametrize("N,K", GEMV_SHAPES)
+def test_gemv_parity(kind, N, K):
+    x = synth.normal((1, K), 0, f"vx{K}")
+    out, p, w = _run(kind, x, N, K, mq.gemv)
+    _check(out, p, w, kind, N, K)
+
+
+@pytest.mark.parametrize("kind", ["q4k", "q6k"])
+def test_gemv_matches_gemm_at_one_row(kind):
+    N, K = 384, 1536
+    x = synth.normal((1, K), 0, "one")
+    w = synth.weights(kind, N, K, 0, "one.w").cuda()
+    p = _plane_from(x)
+    a = torch.empty((1, N), device="cuda")
+    b = torch.empty((1, N), device="cuda")
+    mq.gemv(kind, p, w, N, a)
+    mq.gemm(kind, p, w, N, b)
+    torch.cuda.synchronize()
+    ref, bound = O.gemm_rows(p.qs.cpu().numpy(), p.d.cpu().numpy(), w.cpu().numpy(), kind, N, K)
+    assert np.all(np.abs(a.cpu().numpy() - b.cpu().numpy()) <= 2 * bound)
+
+
+def test_gemv_rejects_multi_row_plane():
+    p = mq.Plane.empty(2, 256)
+    w = torch.zeros((8, 144), dtype=torch.uint8, device="cuda")
+    out = torch.empty(8, device="cuda")
+    with pytest.raises(mq.MQError) as e:
+        mq.mq_gemv_q4k(p, w, 8, out)
+    assert e.value.status == mq.MQ_ERR_SHAPE

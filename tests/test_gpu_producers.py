@@ -1,0 +1,128 @@
+"""Parity of the q8 plane producers (CUDA, through the C ABI) with the CPU oracle.
+
+quantize and the fused RMSNorm producer must be bit-exact; the fused SwiGLU
+producer depends on expf, which CUDA and the host libm may round differently,
+and is held to +-1 quant level on at most 1e-4 of elements.
+Every output buffer starts poisoned (0xCD) inside guard bands, so an unwritten
+slot or an out-of-bounds write fails the test.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mq_oracle as O
+from quant_int8_quantized_gb300 import mq, synth
+from tests._gpu_util import GuardedPlane, assert_plane_close, assert_plane_equal, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(1, 256), (3, 512), (16, 512), (130, 768), (257, 3584), (5, 18944)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def _x(M, K, name, outliers=False):
+    x = synth.normal((M, K), 0, name)
+    if outliers:
+        x = synth.with_outliers(x, 0, name)
+    return x
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+@pytest.mark.parametrize("outliers", [False, True])
+def test_quantize_bit_exact(M, K, outliers):
+    x = _x(M, K, f"q{M}x{K}", outliers)
+    x[0, :32] = 0.0                     # an all-zero block
+    if K >= 64:
+        x[-1, 32:64] = 0.0
+        x[-1, 40] = -3.0                # a single non-zero value
+    gp = GuardedPlane(M, K)
+    mq.mq_quantize_q8(x.cuda(), gp.plane)
+    torch.cuda.synchronize()
+    gp.check()
+    assert_plane_equal(gp.numpy(), O.quantize_q8(x.numpy()), f"quantize {M}x{K}")
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+def test_rms_quant_bit_exact(M, K):
+    x = _x(M, K, f"r{M}x{K}")
+    w = synth.normal((K,), 0, f"rw{K}", mean=1.0, std=0.1)
+    gp = GuardedPlane(M, K)
+    mq.mq_rms_quant(x.cuda(), w.cuda(), 1e-6, gp.plane)
+    torch.cuda.synchronize()
+    gp.check()
+    assert_plane_equal(gp.numpy(), O.rms_quant(x.numpy(), w.numpy(), 1e-6), f"rms {M}x{K}")
+
+
+@pytest.mark.parametrize("M", [1, 7, 700])   # the 128-thread-per-row and the warp-per-row kernels
+def test_rms_quant_both_launch_shapes(M):
+    K = 5120
+    x = _x(M, K, f"rr{M}")
+    w = synth.normal((K,), 0, "rw5120", mean=1.0, std=0.1)
+    gp = GuardedPlane(M, K)
+    mq.mq_rms_quant(x.cuda(), w.cuda(), 1e-6, gp.plane)
+    torch.cuda.synchronize()
+    gp.check()
+    assert_plane_equal(gp.numpy(), O.rms_quant(x.numpy(), w.numpy(), 1e-6), f"rms {M}x{K}")
+
+
+def test_rms_quant_equals_quantize_of_oracle_rms_values():
+    """Mode-2 identity: the fused plane equals the standalone quantize of the f32 RMSNorm output."""
+    M, K = 64, 3584
+    x = _x(M, K, "mode2")
+    w = synth.normal((K,), 0, "mode2w", mean=1.0, std=0.1)
+    fused = GuardedPlane(M, K)
+    mq.mq_rms_quant(x.cuda(), w.cuda(), 1e-6, fused.plane)
+    v = torch.from_numpy(O.rms_values(x.numpy(), w.numpy(), 1e-6)).cuda()
+    sep = GuardedPlane(M, K)
+    mq.mq_quantize_q8(v, sep.plane)
+    torch.cuda.synchronize()
+    assert_plane_equal(fused.numpy(), sep.numpy(), "fused vs separate")
+
+
+@pytest.mark.parametrize("M,K", SHAPES)
+def test_swiglu_quant_within_tolerance(M, K):
+    g = _x(M, K, f"g{M}x{K}") * 3
+    u = _x(M, K, f"u{M}x{K}")
+    g[0, :4] = torch.tensor([0.0, 40.0, -40.0, -100.0])
+    gp = GuardedPlane(M, K)
+    mq.mq_swiglu_quant(g.cuda(), u.cuda(), gp.plane)
+    torch.cuda.synchronize()
+    gp.check()
+    assert_plane_close(gp.numpy(), O.swiglu_quant(g.numpy(), u.numpy()), what=f"swiglu {M}x{K}")
+
+
+def test_producers_full_size_sampled_rows():
+    """7B FFN shapes (M = 3314; hidden 3584, ffn 18944) with the oracle on 64 sampled rows."""
+    M, K, KF = 3314, 3584, 18944
+    rows = np.sort(np.random.default_rng(0).choice(M, 64, replace=False))
+    rows[-1] = M - 1
+    x = synth.normal((M, K), 0, "full.x", device="cuda")
+    w = synth.normal((K,), 0, "full.w", mean=1.0, std=0.1, device="cuda")
+    p = mq.Plane.empty(M, K)
+    mq.mq_rms_quant(x, w, 1e-6, p)
+    g = synth.normal((M, KF), 0, "full.g", device="cuda")
+    u = synth.normal((M, KF), 0, "full.u", device="cuda")
+    pf = mq.Plane.empty(M, KF)
+    mq.mq_swiglu_quant(g, u, pf)
+    pq = mq.Plane.empty(M, KF)
+    mq.mq_quantize_q8(g, pq)
+    torch.cuda.synchronize()
+    idx = torch.from_numpy(rows).cuda()
+    sub = lambda pl: (pl.qs[idx].cpu().numpy(), pl.d[idx].cpu().numpy(), pl.s[idx].cpu().numpy())
+    xs, ws = x[idx].cpu().numpy(), w.cpu().numpy()
+    assert_plane_equal(sub(p), O.rms_quant(xs, ws, 1e-6), "rms full")
+    assert_plane_equal(sub(pq), O.quantize_q8(g[idx].cpu().numpy()), "quantize full")
+    assert_plane_close(sub(pf), O.swiglu_quant(g[idx].cpu().numpy(), u[idx].cpu().numpy()), what="swiglu full")
+    assert mq.mq_device_status() == mq.MQ_OK
+
+
+def test_misaligned_input_rejected():
+    x = torch.zeros(2 * 256 + 1, dtype=torch.float32, device="cuda")[1:].view(2, 256)
+    p = mq.Plane.empty(2, 256)
+    with pytest.raises(mq.MQError) as e:
+        mq.mq_quantize_q8(x, p)
+    assert e.value.status == mq.MQ_ERR_ALIGN
