@@ -1,0 +1,442 @@
+"""Benchmark of the block-quantized matmul hot path on one GB300 (or N replicas).
+
+Step = one pass of the 7B-shaped full matmul stack at M = 3314 tokens:
+28 layers of {RMSNorm->q8 plane; Q, K (q4_K), V (q6_K) GEMMs; attention
+stand-in -> q8 plane (standalone quantize); O (q4_K) GEMM; RMSNorm->q8 plane;
+gate, up (q4_K) GEMMs; SwiGLU->q8 plane; down (q6_K) GEMM}, then RMSNorm->q8 of
+the last token and the q6_K lm_head GEMV (152064 x 3584). Weights are distinct
+per layer (4.6 GB in total, far above the 129 MB L2, so every step streams
+them from HBM). value = tokens/s = 3314 / step time.
+
+Also measured in the same run (separately timed):
+  * decode: the 14B-shaped 48-layer M = 1 sweep (rms->q8, attn_q/k/v/o,
+    gate/up GEMVs, SwiGLU->q8, down GEMV), GB/s of algorithmic bytes;
+  * e2e: the same prefill step with its inputs copied from pinned host memory
+    and the logits copied back inside the timed region;
+  * roofline: the q4_K GEMM launches (the dominant kernel), timed with CUDA
+    events on their stream, against the measured f16/bf16 tensor peak;
+  * cpu_baseline: the CPU oracle on a bounded sample of the same workload.
+
+`--impl reference` times the CPU oracle alone (the reference arm).
+Multi-GPU: replicas only (one process per GPU, each its own full workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_TOK = 3314
+HID, FFN, KVD, VOCAB, LAYERS = 3584, 18944, 512, 152064, 28
+D_HID, D_FFN, D_KV, D_LAYERS = 5120, 13824, 1024, 48
+EPS = 1e-6
+METRIC = "prefill effective int8 TOPS & tok/s (7B-shaped stack, M=3314); decode GEMV GB/s"
+
+# (name, kind, N, K, input) per layer; input: "rms" (rms plane), "attn" (stand-in plane), "swiglu"
+PREFILL_MATS = [("q", "q4k", HID, HID, "rms"), ("k", "q4k", KVD, HID, "rms"), ("v", "q6k", KVD, HID, "rms"),
+                ("o", "q4k", HID, HID, "attn"), ("gate", "q4k", FFN, HID, "rms2"), ("up", "q4k", FFN, HID, "rms2"),
+                ("down", "q6k", HID, FFN, "swiglu")]
+DECODE_MATS = [("q", "q4k", D_HID, D_HID), ("k", "q6k", D_KV, D_HID), ("v", "q6k", D_KV, D_HID),
+               ("o", "q4k", D_HID, D_HID), ("gate", "q4k", D_FFN, D_HID), ("up", "q4k", D_FFN, D_HID),
+               ("down", "q6k", D_HID, D_FFN)]
+BYTES_PER_SB = {"q4k": 144, "q6k": 210}
+
+
+def wbytes(kind, N, K):
+    return N * (K // 256) * BYTES_PER_SB[kind]
+
+
+def plane_bytes(M, K):
+    return M * K + M * (K // 32) * 8
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+class Stack:
+    """Device-resident 7B-shaped prefill stack and 14B-shaped decode sweep."""
+
+    def __init__(self, dev, seed=0, decode=True):
+        from quant_int8_quantized_gb300 import mq, synth
+        self.mq, self.dev = mq, dev
+        S = synth
+        self.x = S.normal((M_TOK, HID), seed, "x", device=dev)
+        self.attn = S.normal((M_TOK, HID), seed, "attn", device=dev)
+        self.rms_w = [S.normal((HID,), seed, f"L{l}.rms1", 1.0, 0.1, device=dev) for l in range(LAYERS)]
+        self.rms2_w = [S.normal((HID,), seed, f"L{l}.rms2", 1.0, 0.1, device=dev) for l in range(LAYERS)]
+        self.final_w = S.normal((HID,), seed, "final_norm", 1.0, 0.1, device=dev)
+        self.W = [{n: S.weights(kind, N, K, seed, f"L{l}.{n}", device=dev) for n, kind, N, K, _ in PREFILL_MATS}
+                  for l in range(LAYERS)]
+        self.lm_head = S.q6k_weights(VOCAB, HID, seed, "lm_head", device=dev)
+        f32 = dict(dtype=torch.float32, device=dev)
+        self.out = {n: torch.empty((M_TOK, N), **f32) for n, _, N, _, _ in PREFILL_MATS}
+        self.p_rms = mq.Plane.empty(M_TOK, HID, dev)
+        self.p_rms2 = mq.Plane.empty(M_TOK, HID, dev)
+        self.p_attn = mq.Plane.empty(M_TOK, HID, dev)
+        self.p_ffn = mq.Plane.empty(M_TOK, FFN, dev)
+        self.p_last = mq.Plane.empty(1, HID, dev)
+        self.logits = torch.empty((VOCAB,), **f32)
+        self.q4_events = []
+        if decode:
+            self.dx = S.normal((1, D_HID), seed, "d.x", device=dev)
+            self.dattn = S.normal((1, D_HID), seed, "d.attn", device=dev)
+            self.dg = S.normal((1, D_FFN), seed, "d.g", device=dev)
+            self.du = S.normal((1, D_FFN), seed, "d.u", device=dev)
+            self.drms = [S.normal((D_HID,), seed, f"D{l}.rms", 1.0, 0.1, device=dev) for l in range(D_LAYERS)]
+            self.DW = [{n: S.weights(kind, N, K, seed, f"D{l}.{n}", device=dev) for n, kind, N, K in DECODE_MATS}
+                       for l in range(D_LAYERS)]
+            self.dout = {n: torch.empty((N,), **f32) for n, _, N, _ in DECODE_MATS}
+            self.dp_h = mq.Plane.empty(1, D_HID, dev)
+            self.dp_a = mq.Plane.empty(1, D_HID, dev)
+            self.dp_f = mq.Plane.empty(1, D_FFN, dev)
+
+    # launches per prefill step: 28 * (2 rms + 1 quantize + 1 swiglu + 7 gemm) + rms + gemv
+    LAUNCHES_PER_STEP = LAYERS * 11 + 2
+    LAUNCHES_PER_DECODE = D_LAYERS * 10
+
+    def step(self, time_q4=False):
+        mq = self.mq
+        planes = {"rms": self.p_rms, "rms2": self.p_rms2, "attn": self.p_attn, "swiglu": self.p_ffn}
+        for l in range(LAYERS):
+            W = self.W[l]
+            mq.mq_rms_quant(self.x, self.rms_w[l], EPS, self.p_rms)
+            mq.mq_quantize_q8(self.attn, self.p_attn)
+            mq.mq_rms_quant(self.x, self.rms2_w[l], EPS, self.p_rms2)
+            for name, kind, N, K, src in PREFILL_MATS:
+                if name == "down":
+                    mq.mq_swiglu_quant(self.out["gate"], self.out["up"], self.p_ffn)
+                if time_q4 and kind == "q4k":
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    mq.gemm(kind, planes[src], W[name], N, self.out[name])
+                    e1.record()
+                    self.q4_events.append((e0, e1, 2.0 * M_TOK * N * K))
+                else:
+                    mq.gemm(kind, planes[src], W[name], N, self.out[name])
+        mq.mq_rms_quant(self.out["down"][-1:], self.final_w, EPS, self.p_last)
+        mq.mq_gemv_q6k(self.p_last, self.lm_head, VOCAB, self.logits)
+
+    def decode_step(self):
+        mq = self.mq
+        for l in range(D_LAYERS):
+            W = self.DW[l]
+            mq.mq_rms_quant(self.dx, self.drms[l], EPS, self.dp_h)
+            for n in ("q", "k", "v"):
+                mq.gemv(dict((a, b) for a, b, _, _ in DECODE_MATS)[n], self.dp_h, W[n], self.dout[n].numel(),
+                        self.dout[n])
+            mq.mq_quantize_q8(self.dattn, self.dp_a)
+            mq.mq_gemv_q4k(self.dp_a, W["o"], D_HID, self.dout["o"])
+            mq.mq_gemv_q4k(self.dp_h, W["gate"], D_FFN, self.dout["gate"])
+            mq.mq_gemv_q4k(self.dp_h, W["up"], D_FFN, self.dout["up"])
+            mq.mq_swiglu_quant(self.dg, self.du, self.dp_f)
+            mq.mq_gemv_q6k(self.dp_f, W["down"], D_HID, self.dout["down"])
+
+    @staticmethod
+    def prefill_flops():
+        per_layer = sum(2.0 * M_TOK * N * K for _, _, N, K, _ in PREFILL_MATS)
+        return LAYERS * per_layer + 2.0 * VOCAB * HID
+
+    @staticmethod
+    def decode_bytes():
+        per_layer = sum(wbytes(kind, N, K) + 4 * N for _, kind, N, K in DECODE_MATS)
+        per_layer += 4 * D_HID * 2 + plane_bytes(1, D_HID) * 2 + 8 * D_FFN + plane_bytes(1, D_FFN)  # producers
+        per_layer += 4 * D_HID                                                                        # rms weight
+        return D_LAYERS * per_layer
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+
+def oracle_sample_tok_s(tokens=2, frac=4, seed=0):
+    """Time the CPU oracle on a bounded sample of the prefill stack and extrapolate to tok/s.
+
+    Sample: `tokens` tokens through one full layer's producers, and through every
+    matmul of that layer restricted to one in `frac` of its output rows (the
+    oracle's cost is linear in output rows: it dequantizes exactly the rows it
+    computes), plus the last-token lm_head on one in 8*frac of its rows. The
+    layer time (matmul part scaled by `frac`) is multiplied by 28 layers.
+    """
+    from oracle import mq_oracle as O
+    from quant_int8_quantized_gb300 import synth as S
+    x = S.normal((tokens, HID), seed, "x").numpy()
+    attn = S.normal((tokens, HID), seed, "attn").numpy()
+    w1 = S.normal((HID,), seed, "L0.rms1", 1.0, 0.1).numpy()
+    w2 = S.normal((HID,), seed, "L0.rms2", 1.0, 0.1).numpy()
+    g = S.normal((tokens, FFN), seed, "L0.g").numpy()
+    u = S.normal((tokens, FFN), seed, "L0.u").numpy()
+    Ws = {n: S.weights(kind, N // frac, K, seed, f"L0.{n}").numpy() for n, kind, N, K, _ in PREFILL_MATS}
+    lm_rows = VOCAB // (8 * frac)
+    lm = S.q6k_weights(lm_rows, HID, seed, "lm_head").numpy()
+    t0 = time.perf_counter()
+    planes = {"rms": O.rms_quant(x, w1, EPS), "attn": O.quantize_q8(attn), "rms2": O.rms_quant(x, w2, EPS),
+              "swiglu": O.swiglu_quant(g, u)}
+    t_prod = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    last = None
+    for name, kind, N, K, src in PREFILL_MATS:
+        qs, d, _ = planes[src]
+        last, _ = O.gemm_rows(qs, d, Ws[name], kind, N // frac, K)
+    t_mat = (time.perf_counter() - t0) * frac
+    t0 = time.perf_counter()
+    qs, d, _ = O.rms_quant(np.resize(last[-1:], (1, HID)).astype(np.float32), w1, EPS)
+    O.gemm_rows(qs, d, lm, "q6k", lm_rows, HID)
+    t_lm = (time.perf_counter() - t0) * (VOCAB / lm_rows)
+    est = LAYERS * (t_prod + t_mat) + t_lm
+    sample = (f"{tokens} token(s): layer-0 producers in full, its 7 matmuls on 1/{frac} of their output rows "
+              f"(x{frac}), x{LAYERS} layers; lm_head on {lm_rows} of {VOCAB} rows (x{VOCAB / lm_rows:.1f})")
+    return tokens / est, est, sample
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ----------------------------------------------------------------------------- main
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("bf16_tflops_sustained"), d.get("bf16_tflops"), d.get("hbm_gbs"), "measured"
+    return 1700.0, 1900.0, 6800.0, "fallback"
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    ws, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        oracle_sample_tok_s(tokens=1, frac=16)
+    vals, ests = [], []
+    for _ in range(args.steps):
+        v, est, sample = oracle_sample_tok_s(tokens=1, frac=16)
+        vals.append(v)
+        ests.append(est)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * statistics.median(ests),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "config": {"workload": "7B-shaped matmul stack, M=3314 (oracle sample)"},
+            "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    ws, rank, local = dist_setup()
+    import __graft_entry__
+    __graft_entry__.build()
+    from quant_int8_quantized_gb300 import mq
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    st = Stack(dev, decode=not args.no_decode)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        st.step()
+        if not args.no_decode:
+            st.decode_step()
+    torch.cuda.synchronize()
+
+    # ---- prefill, inputs resident in HBM
+    barrier(ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            st.step(time_q4=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    t_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws)
+    status = mq.mq_device_status()
+    if status != mq.MQ_OK:
+        raise RuntimeError(f"device status {status}")
+    q4_t = sum(a.elapsed_time(b) for a, b, _ in st.q4_events) * 1e-3
+    q4_f = sum(f for _, _, f in st.q4_events)
+    q4_launches = len(st.q4_events)
+
+    # ---- decode sweep
+    dec = None
+    if not args.no_decode:
+        barrier(ws)
+        torch.cuda.synchronize()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(args.steps):
+            st.decode_step()
+        d1.record(stream)
+        torch.cuda.synchronize()
+        dt = max_over_ranks(d0.elapsed_time(d1) / args.steps, ws) * 1e-3
+        dec = {"workload": "14B-shaped decode sweep, 48 layers, M=1", "GBps": ws * Stack.decode_bytes() / dt / 1e9,
+               "ms_per_token": dt * 1e3, "bytes_per_token": Stack.decode_bytes()}
+
+    # ---- end to end: inputs from pinned host memory, logits back to the host
+    host_x = st.x.cpu().pin_memory()
+    host_attn = st.attn.cpu().pin_memory()
+    host_logits = torch.empty((VOCAB,), dtype=torch.float32).pin_memory()
+    barrier(ws)
+    torch.cuda.synchronize()
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0.record(stream)
+    for _ in range(args.steps):
+        st.x.copy_(host_x, non_blocking=True)
+        st.attn.copy_(host_attn, non_blocking=True)
+        st.step()
+        host_logits.copy_(st.logits, non_blocking=True)
+    h1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(h0.elapsed_time(h1) / args.steps, ws)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        v, est, sample = oracle_sample_tok_s()
+        cpu = {"value": v, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample}
+
+    peak_sus, peak_burst, hbm, peak_kind = load_peaks()
+    achieved = q4_f / q4_t / 1e12
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": ws * M_TOK / (t_ms * 1e-3), "unit": "tok/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8 activations x 4/6-bit weights, exact on the f16 tensor pipe, f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": "7B-shaped matmul stack prefill (28 layers + lm_head), M=3314",
+                       "hidden": HID, "ffn": FFN, "kv": KVD, "vocab": VOCAB, "layers": LAYERS,
+                       "weights_bytes": sum(wbytes(k, N, K) for _, k, N, K, _ in PREFILL_MATS) * LAYERS
+                       + wbytes("q6k", VOCAB, HID),
+                       "l2": "weights per step (4.6 GB) far exceed L2; no flush",
+                       "parallelism": f"replicas x{ws}"},
+            "effective_tops": ws * Stack.prefill_flops() / (t_ms * 1e-3) / 1e12,
+            "decode": dec,
+            "e2e": {"value": ws * M_TOK / (e2e_ms * 1e-3), "unit": "tok/s",
+                    "h2d_bytes_per_step": host_x.numel() * 4 + host_attn.numel() * 4,
+                    "d2h_bytes_per_step": VOCAB * 4},
+            "roofline": {"kernel": "gemm q4_K (all q4_K GEMM launches of the timed steps)", "bound": "tensor",
+                         "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
+                         "peak_kind": f"{peak_kind} bf16 sustained (f16 runs at the bf16 rate)",
+                         "launches": q4_launches, "traffic": None},
+            "gpu_launches": Stack.LAUNCHES_PER_STEP * args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
