@@ -142,7 +142,7 @@ class Stack:
         self.p_rms2 = mq.Plane.empty(M_TOK, HID, dev)
         self.p_attn = mq.Plane.empty(M_TOK, HID, dev)
         self.p_ffn = mq.Plane.empty(M_TOK, FFN, dev)
-        self.p_last = mq.Plane.empty(1, HID, dev)
+        self.p_last = mq.Plane.empty(1, HID, dev, f16=False)
         self.logits = torch.empty((VOCAB,), **f32)
         self.q4_events = []
         if decode:
@@ -154,9 +154,9 @@ class Stack:
             self.DW = [{n: S.weights(kind, N, K, seed, f"D{l}.{n}", device=dev) for n, kind, N, K in DECODE_MATS}
                        for l in range(D_LAYERS)]
             self.dout = {n: torch.empty((N,), **f32) for n, _, N, _ in DECODE_MATS}
-            self.dp_h = mq.Plane.empty(1, D_HID, dev)
-            self.dp_a = mq.Plane.empty(1, D_HID, dev)
-            self.dp_f = mq.Plane.empty(1, D_FFN, dev)
+            self.dp_h = mq.Plane.empty(1, D_HID, dev, f16=False)
+            self.dp_a = mq.Plane.empty(1, D_HID, dev, f16=False)
+            self.dp_f = mq.Plane.empty(1, D_FFN, dev, f16=False)
 
     # launches per prefill step: 28 * (2 rms + 1 quantize + 1 swiglu + 7 gemm) + rms + gemv
     LAUNCHES_PER_STEP = LAYERS * 11 + 2
@@ -322,6 +322,72 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- single-kernel cases
+
+def run_case(spec: str, steps: int, warmup: int):
+    """Time one kernel on seeded inputs: `kind:MxNxK` (gemm_q4k, gemm_q6k, gemv_q4k, gemv_q6k)
+    or `kind:MxK` (quantize, rms, swiglu). Prints one JSON line with its roofline figure."""
+    import __graft_entry__
+    __graft_entry__.build()
+    from quant_int8_quantized_gb300 import mq, synth as S
+    kind, shape = spec.split(":")
+    dims = [int(v) for v in shape.lower().split("x")]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak_sus, peak_burst, hbm, peak_kind = load_peaks()
+    if kind.startswith("gemm") or kind.startswith("gemv"):
+        M, N, K = dims
+        wk = kind[-3:]
+        x = S.normal((M, K), 0, "case.x", device=dev)
+        w = S.weights(wk, N, K, 0, "case.w", device=dev)
+        p = mq.Plane.empty(M, K, dev)
+        mq.mq_quantize_q8(x, p)
+        out = torch.empty((M, N), dtype=torch.float32, device=dev)
+        fn = (lambda: mq.gemm(wk, p, w, N, out)) if kind.startswith("gemm") else (lambda: mq.gemv(wk, p, w, N, out))
+        flops = 2.0 * M * N * K
+        nbytes = wbytes(wk, N, K) + plane_bytes(M, K) + 4 * M * N
+    else:
+        M, K = dims
+        x = S.normal((M, K), 0, "case.x", device=dev)
+        p = mq.Plane.empty(M, K, dev)
+        flops = 0.0
+        if kind == "quantize":
+            fn = lambda: mq.mq_quantize_q8(x, p)
+            nbytes = 4 * M * K + plane_bytes(M, K)
+        elif kind == "rms":
+            w = S.normal((K,), 0, "case.rmsw", 1.0, 0.1, device=dev)
+            fn = lambda: mq.mq_rms_quant(x, w, EPS, p)
+            nbytes = 4 * M * K + 4 * K + plane_bytes(M, K)
+        elif kind == "swiglu":
+            u = S.normal((M, K), 0, "case.u", device=dev)
+            fn = lambda: mq.mq_swiglu_quant(x, u, p)
+            nbytes = 8 * M * K + plane_bytes(M, K)
+        else:
+            raise ValueError(kind)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 256 MB > L2
+    for _ in range(max(1, warmup)):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush.fill_(1.0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) * 1e-3)
+    if mq.mq_device_status() != mq.MQ_OK:
+        raise RuntimeError("device status")
+    t = statistics.median(ts)
+    line = {"case": spec, "us": t * 1e6, "GBps": nbytes / t / 1e9, "hbm_frac": nbytes / t / 1e9 / hbm,
+            "algorithmic_bytes": nbytes}
+    if flops:
+        line.update({"TFLOPs": flops / t / 1e12, "tensor_frac_burst": flops / t / 1e12 / peak_burst})
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -330,7 +396,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--case", default=None, help="time one kernel, e.g. gemm_q4k:3314x18944x3584")
     args = ap.parse_args()
+    if args.case:
+        return run_case(args.case, args.steps, args.warmup)
     if args.impl == "reference":
         return run_reference(args)
     ws, rank, local = dist_setup()

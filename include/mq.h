@@ -55,23 +55,30 @@ enum {
  * q8 activation plane ([r52] §2.2; [D3-7] Excerpt C): for each row m and each
  * block b of 32 consecutive elements, int8 quants qs, an f32 scale d and the
  * int32 sum of the block's quants s:
- *     qs : int8    [M][K]      row-major, row stride K bytes
- *     d  : float   [M][K/32]   row-major
- *     s  : int32_t [M][K/32]   row-major
- * The plane is a pure function of the f32 values it quantizes, so one plane
- * may feed several GEMMs (Q/K/V, gate/up). The library reads only rows < M;
- * the GEMM supplies the zero rows of a partial 128-row tile itself.
- * The struct lives in host memory; only its three pointers are device pointers.
+ *     qs : int8     [M][K]      row-major, row stride K bytes
+ *     d  : float    [M][K/32]   row-major
+ *     s  : int32_t  [M][K/32]   row-major
+ *     qh : uint16_t [M][K]      optional: the same quants as IEEE binary16 bit
+ *                               patterns (exact: |q| <= 127), the operand form
+ *                               the f16 tensor cores read. NULL = absent.
+ * Producers write qh in the same pass when it is non-NULL; the GEMM requires
+ * it (the GEMV does not read it). The plane is a pure function of the f32
+ * values it quantizes, so one plane may feed several GEMMs (Q/K/V, gate/up).
+ * The library reads only rows < M; the GEMM supplies the zero rows of a
+ * partial 128-row tile itself. The struct lives in host memory; only its
+ * pointers are device pointers.
  */
 typedef struct mq_q8_plane {
-    int8_t*  qs;
-    float*   d;
-    int32_t* s;
+    int8_t*   qs;
+    float*    d;
+    int32_t*  s;
+    uint16_t* qh;
     int M;
     int K;
 } mq_q8_plane;
 
-/* Bytes of each plane array for an M x K activation. Returns the total. Pure host helper. */
+/* Bytes of each plane array for an M x K activation (qh, when used, takes 2*M*K
+ * bytes more). Returns qs + d + s bytes. Pure host helper. */
 size_t mq_plane_bytes(int M, int K, size_t* qs_bytes, size_t* d_bytes, size_t* s_bytes);
 
 /*
@@ -94,6 +101,7 @@ size_t mq_q6k_row_bytes(int K);
  *     amax = max|v|; d = amax / 127 (f32); q = rint(v / d) (IEEE f32 divide,
  *     ties to even) clamped to [-127, 127]; s = sum q; an all-zero block gives
  *     d = 0, q = 0, s = 0.
+ * Every producer also writes out->qh when it is non-NULL.
  * out->M, out->K must equal M, K. Input values must be finite.
  */
 int mq_quantize_q8(const float* x, int M, int K, const mq_q8_plane* out, cudaStream_t stream);
@@ -126,10 +134,10 @@ int mq_swiglu_quant(const float* g, const float* u, int M, int K,
  * k32 chunks with dual 16-sub rescale"):
  *     out[m][n] = sum_k (d_a[m][k/32] * q_a[m][k]) * w[n][k]
  * with w the dequantized weight (q4_K: d*sc*q - dmin*m per 32; q6_K:
- * d*sc*(q-32) per 16). a: plane with a->M >= 1 rows and a->K = K; w: N rows of
- * super-blocks; out: f32 [a->M][N] row-major, overwritten. Any M >= 1 is
- * accepted (the kernel is built for M >= 16). Accuracy: within
- * 1e-3 * sum_k |a||w| per element.
+ * d*sc*(q-32) per 16). a: plane with a->M >= 1 rows, a->K = K and a->qh set
+ * (MQ_ERR_NULL otherwise); w: N rows of super-blocks; out: f32 [a->M][N]
+ * row-major, overwritten. Any M >= 1 is accepted (the kernel is built for
+ * M >= 16). Accuracy: within 1e-3 * sum_k |a||w| per element.
  */
 int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);

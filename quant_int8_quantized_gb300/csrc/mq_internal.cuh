@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "mq.h"
@@ -25,6 +26,7 @@ inline int check_plane(const mq_q8_plane* p, int M, int K) {
     if (M == 0) return MQ_OK;
     if (!p->qs || !p->d || !p->s) return MQ_ERR_NULL;
     if (!aligned16(p->qs) || !aligned16(p->d) || !aligned16(p->s)) return MQ_ERR_ALIGN;
+    if (p->qh && !aligned16(p->qh)) return MQ_ERR_ALIGN;
     return MQ_OK;
 }
 
@@ -56,7 +58,7 @@ __device__ __forceinline__ float mq_f16_to_f32(uint16_t h) {
 // shuffles at offsets 4, 2, 1 (max and integer sums are exact in any order).
 // Returns the packed int8 quants; d and s are valid in every lane of the group.
 __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v2, float v3,
-                                                     float& d_out, int& s_out) {
+                                                     float& d_out, int& s_out, uint2& h_out) {
     float am = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
@@ -79,6 +81,9 @@ __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v
     s += __shfl_xor_sync(0xffffffffu, s, 1);
     d_out = d;
     s_out = s;
+    // the same four quants as binary16 (exact for |q| <= 127)
+    h_out.x = (uint32_t)__half_as_ushort(__int2half_rn(q0)) | ((uint32_t)__half_as_ushort(__int2half_rn(q1)) << 16);
+    h_out.y = (uint32_t)__half_as_ushort(__int2half_rn(q2)) | ((uint32_t)__half_as_ushort(__int2half_rn(q3)) << 16);
     return (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) | ((uint32_t)(q2 & 0xff) << 16) |
            ((uint32_t)(q3 & 0xff) << 24);
 }

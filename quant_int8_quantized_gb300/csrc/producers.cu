@@ -19,9 +19,10 @@ constexpr int kThreads = 256;
 constexpr int kRoundsPerIter = 4;   // float4 loads in flight per lane
 
 __device__ __forceinline__ void store_round(uint32_t* __restrict__ qs, float* __restrict__ d,
-                                            int32_t* __restrict__ s, long long round, int lane,
-                                            uint32_t q, float dd, int ss) {
+                                            int32_t* __restrict__ s, uint2* __restrict__ qh, long long round,
+                                            int lane, uint32_t q, float dd, int ss, uint2 h) {
     qs[round * 32 + lane] = q;
+    if (qh) qh[round * 32 + lane] = h;
     if ((lane & 7) == 0) {
         const long long b = round * 4 + (lane >> 3);
         d[b] = dd;
@@ -35,7 +36,7 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __r
                                                                uint32_t* __restrict__ qs,
                                                                float* __restrict__ d,
                                                                int32_t* __restrict__ s,
-                                                               long long rounds) {
+                                                               uint2* __restrict__ qh, long long rounds) {
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * kThreads) >> 5;
@@ -49,8 +50,9 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __r
             if (r0 + u < rounds) {   // warp-uniform
                 float dd;
                 int ss;
-                const uint32_t q = mq_quant4_group8(v[u].x, v[u].y, v[u].z, v[u].w, dd, ss);
-                store_round(qs, d, s, r0 + u, lane, q, dd, ss);
+                uint2 h;
+                const uint32_t q = mq_quant4_group8(v[u].x, v[u].y, v[u].z, v[u].w, dd, ss, h);
+                store_round(qs, d, s, qh, r0 + u, lane, q, dd, ss, h);
             }
         }
     }
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __
                                                                 uint32_t* __restrict__ qs,
                                                                 float* __restrict__ d,
                                                                 int32_t* __restrict__ s,
-                                                                long long rounds) {
+                                                                uint2* __restrict__ qh, long long rounds) {
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * kThreads) >> 5;
@@ -84,10 +86,11 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __
             if (r0 + k < rounds) {
                 float dd;
                 int ss;
+                uint2 h;
                 const uint32_t q = mq_quant4_group8(silu_mul(gv[k].x, uv[k].x), silu_mul(gv[k].y, uv[k].y),
                                                     silu_mul(gv[k].z, uv[k].z), silu_mul(gv[k].w, uv[k].w),
-                                                    dd, ss);
-                store_round(qs, d, s, r0 + k, lane, q, dd, ss);
+                                                    dd, ss, h);
+                store_round(qs, d, s, qh, r0 + k, lane, q, dd, ss, h);
             }
         }
     }
@@ -115,19 +118,21 @@ __device__ __forceinline__ float rms_scale_warp(const float4* __restrict__ xr, i
 
 __device__ __forceinline__ void rms_quant_rounds(const float4* __restrict__ xr, const float4* __restrict__ w4,
                                                  uint32_t* __restrict__ qs, float* __restrict__ d,
-                                                 int32_t* __restrict__ s, long long row_round0, int k0,
-                                                 int kstep, int nrounds, float scale, int lane) {
+                                                 int32_t* __restrict__ s, uint2* __restrict__ qh,
+                                                 long long row_round0, int k0, int kstep, int nrounds, float scale,
+                                                 int lane) {
 #pragma unroll 4
     for (int k = k0; k < nrounds; k += kstep) {
         const float4 xv = __ldg(xr + k * 32 + lane);
         const float4 wv = __ldg(w4 + k * 32 + lane);
         float dd;
         int ss;
+        uint2 h;
         const uint32_t q = mq_quant4_group8(__fmul_rn(__fmul_rn(xv.x, scale), wv.x),
                                             __fmul_rn(__fmul_rn(xv.y, scale), wv.y),
                                             __fmul_rn(__fmul_rn(xv.z, scale), wv.z),
-                                            __fmul_rn(__fmul_rn(xv.w, scale), wv.w), dd, ss);
-        store_round(qs, d, s, row_round0 + k, lane, q, dd, ss);
+                                            __fmul_rn(__fmul_rn(xv.w, scale), wv.w), dd, ss, h);
+        store_round(qs, d, s, qh, row_round0 + k, lane, q, dd, ss, h);
     }
 }
 
@@ -136,7 +141,8 @@ __global__ void __launch_bounds__(kThreads) rms_quant_rows_kernel(const float4* 
                                                                   const float4* __restrict__ w4,
                                                                   uint32_t* __restrict__ qs,
                                                                   float* __restrict__ d,
-                                                                  int32_t* __restrict__ s, int M, int K,
+                                                                  int32_t* __restrict__ s,
+                                                                  uint2* __restrict__ qh, int M, int K,
                                                                   float eps) {
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -144,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) rms_quant_rows_kernel(const float4* 
     const int nrounds = K >> 7;
     const float4* xr = x + (long long)row * (K >> 2);
     const float scale = rms_scale_warp(xr, K, eps, lane);
-    rms_quant_rounds(xr, w4, qs, d, s, (long long)row * nrounds, 0, 1, nrounds, scale, lane);
+    rms_quant_rounds(xr, w4, qs, d, s, qh, (long long)row * nrounds, 0, 1, nrounds, scale, lane);
 }
 
 // Few rows (decode): one 128-thread block per row. Warp 0 computes the scale in
@@ -154,7 +160,8 @@ __global__ void __launch_bounds__(128) rms_quant_wide_kernel(const float4* __res
                                                              const float4* __restrict__ w4,
                                                              uint32_t* __restrict__ qs,
                                                              float* __restrict__ d,
-                                                             int32_t* __restrict__ s, int M, int K,
+                                                             int32_t* __restrict__ s,
+                                                             uint2* __restrict__ qh, int M, int K,
                                                              float eps) {
     __shared__ float s_scale;
     const int lane = threadIdx.x & 31;
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(128) rms_quant_wide_kernel(const float4* __res
     }
     __syncthreads();
     const int nrounds = K >> 7;
-    rms_quant_rounds(xr, w4, qs, d, s, (long long)row * nrounds, wid, 4, nrounds, s_scale, lane);
+    rms_quant_rounds(xr, w4, qs, d, s, qh, (long long)row * nrounds, wid, 4, nrounds, s_scale, lane);
 }
 
 int flat_grid(long long rounds) {
@@ -195,7 +202,8 @@ extern "C" int mq_quantize_q8(const float* x, int M, int K, const mq_q8_plane* o
     if (rc != MQ_OK || M == 0) return rc;
     const long long rounds = (long long)M * K / 128;
     quantize_q8_kernel<<<flat_grid(rounds), kThreads, 0, stream>>>(
-        reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(out->qs), out->d, out->s, rounds);
+        reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(out->qs), out->d, out->s,
+        reinterpret_cast<uint2*>(out->qh), rounds);
     return mq::launch_status();
 }
 
@@ -206,7 +214,7 @@ extern "C" int mq_swiglu_quant(const float* g, const float* u, int M, int K, con
     const long long rounds = (long long)M * K / 128;
     swiglu_quant_kernel<<<flat_grid(rounds), kThreads, 0, stream>>>(
         reinterpret_cast<const float4*>(g), reinterpret_cast<const float4*>(u),
-        reinterpret_cast<uint32_t*>(out->qs), out->d, out->s, rounds);
+        reinterpret_cast<uint32_t*>(out->qs), out->d, out->s, reinterpret_cast<uint2*>(out->qh), rounds);
     return mq::launch_status();
 }
 
@@ -217,13 +225,14 @@ extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float 
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const float4* w4 = reinterpret_cast<const float4*>(w);
     uint32_t* qs = reinterpret_cast<uint32_t*>(out->qs);
+    uint2* qh = reinterpret_cast<uint2*>(out->qh);
     // One warp per row fills the machine once there are a few warps per SM.
     if (M >= 4 * mq::num_sms()) {
         const int rows_per_block = kThreads / 32;
         rms_quant_rows_kernel<<<(M + rows_per_block - 1) / rows_per_block, kThreads, 0, stream>>>(
-            x4, w4, qs, out->d, out->s, M, K, eps);
+            x4, w4, qs, out->d, out->s, qh, M, K, eps);
     } else {
-        rms_quant_wide_kernel<<<M, 128, 0, stream>>>(x4, w4, qs, out->d, out->s, M, K, eps);
+        rms_quant_wide_kernel<<<M, 128, 0, stream>>>(x4, w4, qs, out->d, out->s, qh, M, K, eps);
     }
     return mq::launch_status();
 }

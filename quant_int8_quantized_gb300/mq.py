@@ -31,7 +31,7 @@ class MQError(RuntimeError):
 
 class CPlane(ctypes.Structure):
     _fields_ = [("qs", ctypes.c_void_p), ("d", ctypes.c_void_p), ("s", ctypes.c_void_p),
-                ("M", ctypes.c_int), ("K", ctypes.c_int)]
+                ("qh", ctypes.c_void_p), ("M", ctypes.c_int), ("K", ctypes.c_int)]
 
 
 _lib = None
@@ -101,23 +101,29 @@ def _dev_tensor(t, dtype, name):
 
 
 class Plane:
-    """Device q8 plane: qs int8 [M, K], d f32 [M, K/32], s int32 [M, K/32]."""
+    """Device q8 plane: qs int8 [M, K], d f32 [M, K/32], s int32 [M, K/32], and
+    optionally qh f16 [M, K] (the same quants in the tensor-core operand form,
+    required by the GEMM)."""
 
-    def __init__(self, qs: torch.Tensor, d: torch.Tensor, s: torch.Tensor):
-        self.qs, self.d, self.s = qs, d, s
+    def __init__(self, qs: torch.Tensor, d: torch.Tensor, s: torch.Tensor, qh: torch.Tensor = None):
+        self.qs, self.d, self.s, self.qh = qs, d, s, qh
         self.M, self.K = int(qs.shape[0]), int(qs.shape[1])
         _dev_tensor(qs, torch.int8, "plane.qs")
         _dev_tensor(d, torch.float32, "plane.d")
         _dev_tensor(s, torch.int32, "plane.s")
+        if qh is not None:
+            _dev_tensor(qh, torch.float16, "plane.qh")
 
     @classmethod
-    def empty(cls, M: int, K: int, device="cuda") -> "Plane":
+    def empty(cls, M: int, K: int, device="cuda", f16: bool = True) -> "Plane":
         return cls(torch.empty((M, K), dtype=torch.int8, device=device),
                    torch.empty((M, K // 32), dtype=torch.float32, device=device),
-                   torch.empty((M, K // 32), dtype=torch.int32, device=device))
+                   torch.empty((M, K // 32), dtype=torch.int32, device=device),
+                   torch.empty((M, K), dtype=torch.float16, device=device) if f16 else None)
 
     def c(self) -> CPlane:
-        return CPlane(self.qs.data_ptr(), self.d.data_ptr(), self.s.data_ptr(), self.M, self.K)
+        return CPlane(self.qs.data_ptr(), self.d.data_ptr(), self.s.data_ptr(),
+                      self.qh.data_ptr() if self.qh is not None else None, self.M, self.K)
 
 
 def mq_plane_bytes(M: int, K: int):

@@ -39,14 +39,19 @@ class Guarded:
 
 
 class GuardedPlane:
-    def __init__(self, M, K):
+    def __init__(self, M, K, f16=True):
         self.g = [Guarded((M, K), torch.int8), Guarded((M, K // 32), torch.float32),
                   Guarded((M, K // 32), torch.int32)]
-        self.plane = mq.Plane(self.g[0].t, self.g[1].t, self.g[2].t)
+        if f16:
+            self.g.append(Guarded((M, K), torch.float16))
+        self.plane = mq.Plane(self.g[0].t, self.g[1].t, self.g[2].t, self.g[3].t if f16 else None)
 
     def check(self):
         for g in self.g:
             g.check()
+        if self.plane.qh is not None:   # the f16 copy holds exactly the int8 quants
+            qs = self.plane.qs.cpu().numpy().astype(np.float32)
+            assert np.array_equal(self.plane.qh.cpu().numpy().astype(np.float32), qs), "qh != qs"
 
     def numpy(self):
         return (self.plane.qs.cpu().numpy(), self.plane.d.cpu().numpy(), self.plane.s.cpu().numpy())
