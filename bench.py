@@ -52,6 +52,23 @@ DECODE_MATS = [("q", "q4k", D_HID, D_HID), ("k", "q6k", D_KV, D_HID), ("v", "q6k
                ("down", "q6k", D_HID, D_FFN)]
 BYTES_PER_SB = {"q4k": 144, "q6k": 210}
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gemm_kernel<q4_K> launch at
+# 3314 x 18944 x 3584, from one ncu capture (summary under profiles/). It describes the kernel built
+# from the sources with these SHA-256 digests and is reported as null once either file changes.
+GEMM_Q4K_TRAFFIC = {"bytes": 267776512,
+                    "sha256": {"gemm.cu": "6240fe60bd8b67eb5c70f4a83415e79dcb40216267f453493a74b16fad2e8098",
+                               "tc.cuh": "6b1f7d550e0d4c7f2abe55bdf3a9d264e868795aecd0d505c3fc5e948d07bcbd"}}
+
+
+def gemm_q4k_traffic():
+    import hashlib
+    csrc = os.path.join(ROOT, "quant_int8_quantized_gb300", "csrc")
+    for fn, digest in GEMM_Q4K_TRAFFIC["sha256"].items():
+        with open(os.path.join(csrc, fn), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != digest:
+                return None
+    return GEMM_Q4K_TRAFFIC["bytes"]
+
 
 def wbytes(kind, N, K):
     return N * (K // 256) * BYTES_PER_SB[kind]
@@ -173,7 +190,7 @@ class Stack:
             for name, kind, N, K, src in PREFILL_MATS:
                 if name == "down":
                     mq.mq_swiglu_quant(self.out["gate"], self.out["up"], self.p_ffn)
-                if time_q4 and kind == "q4k":
+                if time_q4 and name in ("gate", "up"):
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record()
                     mq.gemm(kind, planes[src], W[name], N, self.out[name])
@@ -492,10 +509,11 @@ def main():
             "e2e": {"value": ws * M_TOK / (e2e_ms * 1e-3), "unit": "tok/s",
                     "h2d_bytes_per_step": host_x.numel() * 4 + host_attn.numel() * 4,
                     "d2h_bytes_per_step": VOCAB * 4},
-            "roofline": {"kernel": "gemm q4_K (all q4_K GEMM launches of the timed steps)", "bound": "tensor",
+            "roofline": {"kernel": "gemm q4_K 3314x18944x3584 (gate and up launches of the timed steps)",
+                         "bound": "tensor",
                          "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
                          "peak_kind": f"{peak_kind} bf16 sustained (f16 runs at the bf16 rate)",
-                         "launches": q4_launches, "traffic": None},
+                         "launches": q4_launches, "traffic": gemm_q4k_traffic(), "traffic_unit": "bytes per launch"},
             "gpu_launches": Stack.LAUNCHES_PER_STEP * args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
