@@ -53,20 +53,26 @@ DECODE_MATS = [("q", "q4k", D_HID, D_HID), ("k", "q6k", D_KV, D_HID), ("v", "q6k
 BYTES_PER_SB = {"q4k": 144, "q6k": 210}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gemm_kernel<q4_K> launch at
-# 3314 x 18944 x 3584, from one ncu capture (summary under profiles/). It describes the kernel built
-# from the sources with these SHA-256 digests and is reported as null once either file changes.
+# 3314 x 18944 x 3584, from one ncu capture (summary under profiles/). It describes the device code
+# with these SHA-256 digests (gemm.cu up to its host-side section, and tc.cuh) and is reported as
+# null once either changes.
 GEMM_Q4K_TRAFFIC = {"bytes": 267776512,
-                    "sha256": {"gemm.cu": "6240fe60bd8b67eb5c70f4a83415e79dcb40216267f453493a74b16fad2e8098",
+                    "sha256": {"gemm.cu": "35950b36c45744e95345ede2b1ab1106d736ac75a8a5ea505aa3e57b51f55ab8",
                                "tc.cuh": "6b1f7d550e0d4c7f2abe55bdf3a9d264e868795aecd0d505c3fc5e948d07bcbd"}}
+HOST_SECTION = b"// ------------------------------------------------------------------ host side"
+
+
+def device_code_digest(fn):
+    import hashlib
+    with open(os.path.join(ROOT, "quant_int8_quantized_gb300", "csrc", fn), "rb") as f:
+        src = f.read()
+    return hashlib.sha256(src.split(HOST_SECTION)[0]).hexdigest()
 
 
 def gemm_q4k_traffic():
-    import hashlib
-    csrc = os.path.join(ROOT, "quant_int8_quantized_gb300", "csrc")
     for fn, digest in GEMM_Q4K_TRAFFIC["sha256"].items():
-        with open(os.path.join(csrc, fn), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != digest:
-                return None
+        if device_code_digest(fn) != digest:
+            return None
     return GEMM_Q4K_TRAFFIC["bytes"]
 
 
@@ -227,6 +233,21 @@ class Stack:
         per_layer += 4 * D_HID * 2 + plane_bytes(1, D_HID) * 2 + 8 * D_FFN + plane_bytes(1, D_FFN)  # producers
         per_layer += 4 * D_HID                                                                        # rms weight
         return D_LAYERS * per_layer
+
+
+def capture_graph(fn):
+    """Capture fn's launches (all on the current stream) into a CUDA graph."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
 
 
 # ----------------------------------------------------------------------------- CPU oracle sample
@@ -452,20 +473,28 @@ def main():
     q4_f = sum(f for _, _, f in st.q4_events)
     q4_launches = len(st.q4_events)
 
-    # ---- decode sweep
+    # ---- decode sweep: 480 small launches per token, replayed from a CUDA graph so that the
+    #      host's per-launch cost does not stand in for the kernels' time
     dec = None
     if not args.no_decode:
+        graph = capture_graph(st.decode_step)
+        for _ in range(3):
+            graph.replay()
         barrier(ws)
         torch.cuda.synchronize()
         d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         d0.record(stream)
         for _ in range(args.steps):
-            st.decode_step()
+            graph.replay()
         d1.record(stream)
         torch.cuda.synchronize()
         dt = max_over_ranks(d0.elapsed_time(d1) / args.steps, ws) * 1e-3
+        if mq.mq_device_status() != mq.MQ_OK:
+            raise RuntimeError("device status after the decode sweep")
         dec = {"workload": "14B-shaped decode sweep, 48 layers, M=1", "GBps": ws * Stack.decode_bytes() / dt / 1e9,
-               "ms_per_token": dt * 1e3, "bytes_per_token": Stack.decode_bytes()}
+               "ms_per_token": dt * 1e3, "bytes_per_token": Stack.decode_bytes(),
+               "hbm_frac": Stack.decode_bytes() / dt / 1e9 / load_peaks()[2],
+               "launches_per_token": Stack.LAUNCHES_PER_DECODE, "launch": "CUDA graph replay"}
 
     # ---- end to end: inputs from pinned host memory, logits back to the host
     host_x = st.x.cpu().pin_memory()

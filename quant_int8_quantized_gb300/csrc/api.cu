@@ -69,8 +69,9 @@ extern "C" const char* mq_status_str(int status) {
 }
 
 extern "C" int mq_device_status(cudaStream_t stream) {
-    unsigned code = 0;
-    int rc = mq::take_gemm_device_error(stream, &code);
+    unsigned gemm = 0, gemv = 0;
+    int rc = mq::take_gemm_device_error(stream, &gemm);
+    if (rc == MQ_OK) rc = mq::take_gemv_device_error(stream, &gemv);
     if (rc != MQ_OK) return rc;
-    return code ? MQ_ERR_DEVICE : MQ_OK;
+    return (gemm | gemv) ? MQ_ERR_DEVICE : MQ_OK;
 }

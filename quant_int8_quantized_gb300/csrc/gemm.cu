@@ -714,13 +714,20 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
     int rc = check_gemm(a, w, N, out);
     if (rc != MQ_OK || N == 0 || a->M == 0) return rc;
     const int M = a->M, K = a->K;
-    // The register split between warpgroups assumes the launch register count.
-    static int regs_ok = -1;
-    if (regs_ok < 0) {
+    // Once per process: the register split between warpgroups assumes the launch
+    // register count, and the kernel's shared-memory size is set. Later calls make
+    // no attribute calls, so a sequence of entry points can be captured in a graph.
+    const size_t smem = sizeof(Smem<Q6>) + 1024;
+    static int ready = -1;
+    if (ready < 0) {
         cudaFuncAttributes fa;
-        regs_ok = (cudaFuncGetAttributes(&fa, gemm_kernel<Q6>) == cudaSuccess && fa.numRegs == kLaunchRegs) ? 1 : 0;
+        ready = (cudaFuncGetAttributes(&fa, gemm_kernel<Q6>) == cudaSuccess && fa.numRegs == kLaunchRegs &&
+                 cudaFuncSetAttribute(gemm_kernel<Q6>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+                     cudaSuccess)
+                    ? 1
+                    : 0;
     }
-    if (!regs_ok) return MQ_ERR_LAUNCH;
+    if (!ready) return MQ_ERR_LAUNCH;
     const unsigned long long row = (unsigned long long)(K / mq::QK_K) * Cfg<Q6>::kSB;
     CUtensorMap tmA, tmD, tmS, tmW;
     if (Q6) {
@@ -732,9 +739,6 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
                   CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->d, (uint64_t)K / 32, (uint64_t)M, (uint64_t)K / 8, 8, BM) ||
         !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_INT32, a->s, (uint64_t)K / 32, (uint64_t)M, (uint64_t)K / 8, 8, BM))
-        return MQ_ERR_LAUNCH;
-    const size_t smem = sizeof(Smem<Q6>) + 1024;
-    if (cudaFuncSetAttribute(gemm_kernel<Q6>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return MQ_ERR_LAUNCH;
     const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = (int)(tiles < mq::num_sms() ? tiles : mq::num_sms());

@@ -3,11 +3,21 @@
 // "72 · D3-7 — attn_v-q6K MMVQ routing (2b) + rms wide-block", §2 (2b) and
 // Excerpt A2: the decode matmul streams each weight row once and takes integer
 // dot products of 4-bit / 6-bit quants with the int8 activation blocks, then
-// applies the block scales. Here one warp owns one output row. Each lane task
-// is 32 weights (16 consecutive positions of two sub-blocks), so 8 lanes cover
-// one 256-weight super-block and a warp covers 4 super-blocks per step; the
-// weight loads of a step are contiguous across the warp. The activation plane
-// (a few KB) stays in L1/L2 and is shared by every warp.
+// applies the block scales.
+//
+// q4_K: a warp owns two consecutive rows at a time (grid-stride over row pairs),
+// which share the activation loads. A lane task is 64 weights — two whole
+// 32-blocks of one super-block — so the per-block scale work (the 6-bit scale
+// decode, the f32 scaling) is spread over as many weights as possible; 4 lanes
+// cover a super-block and a warp covers 8 super-blocks per step, with the loads
+// of the next step issued before the current one is used. Lane roles are fixed,
+// so the byte positions of a lane's scales are known once.
+//
+// q6_K: one warp per row; a lane task is 32 weights (16 positions of two
+// quarters), 8 lanes per super-block, 4 super-blocks per step, kSteps steps of
+// loads in flight.
+//
+// The activation plane (a few KB) stays in L1/L2 and is shared by every warp.
 //
 // HBM roofline: the weight stream, 0.5625 B/weight (q4_K) or 0.8203 B/weight
 // (q6_K), plus 4 B per output.
@@ -18,29 +28,39 @@ namespace {
 
 constexpr int kThreads = 256;        // 8 rows per block
 constexpr int kRowsPerBlock = kThreads / 32;
-constexpr int kSteps = 4;            // steps (4 super-blocks each) with loads in flight
-
-__device__ __forceinline__ uint32_t byte_of(uint32_t w0, uint32_t w1, uint32_t w2, int i) {
-    const uint32_t w = (i < 4) ? w0 : (i < 8 ? w1 : w2);
-    return (w >> (8 * (i & 3))) & 0xffu;
-}
-
-// 6-bit scale and min of sub-block j from the 12-byte q4_K scale field.
-__device__ __forceinline__ void q4k_scale_min(uint32_t w0, uint32_t w1, uint32_t w2, int j, int& sc, int& mn) {
-    if (j < 4) {
-        sc = (int)(byte_of(w0, w1, w2, j) & 63u);
-        mn = (int)(byte_of(w0, w1, w2, j + 4) & 63u);
-    } else {
-        const uint32_t b = byte_of(w0, w1, w2, j + 4);
-        sc = (int)((b & 15u) | ((byte_of(w0, w1, w2, j - 4) >> 6) << 4));
-        mn = (int)((b >> 4) | ((byte_of(w0, w1, w2, j) >> 6) << 4));
-    }
-}
+constexpr int kSteps = 4;            // q6_K: steps (4 super-blocks each) with loads in flight
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     return v;
+}
+
+// dp4a of unsigned bytes (a) with signed bytes (b).
+__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Lane = 4*g + p: in each 8-super-block step, super-block g of the step and its
+// 32-byte quant group p, i.e. sub-blocks 2p (low nibbles) and 2p+1 (high
+// nibbles), all 32 positions. A warp takes two consecutive rows at a time, which
+// share the activation loads. The high nibbles are dotted in place (bytes
+// 16*hi) and the sum divided by 16, exactly.
+struct Q4Loads {
+    uint4 hv[2], q0[2], q1[2];   // per row: scale header, quant bytes 0-15 and 16-31 of group p
+};
+
+__device__ __forceinline__ void load_q4k(Q4Loads& L, const uint8_t* blk, size_t row_bytes, bool two, int p) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        if (r == 1 && !two) break;
+        const uint8_t* b = blk + r * row_bytes;
+        L.hv[r] = __ldg(reinterpret_cast<const uint4*>(b));
+        L.q0[r] = __ldcs(reinterpret_cast<const uint4*>(b + 16 + 32 * p));
+        L.q1[r] = __ldcs(reinterpret_cast<const uint4*>(b + 32 + 32 * p));
+    }
 }
 
 __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __restrict__ W,
@@ -49,58 +69,74 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __res
                                                             const int32_t* __restrict__ as,
                                                             float* __restrict__ out, int N, int K) {
     const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
-    if (row >= N) return;   // warp-uniform
-    const int S = K / mq::QK_K;
-    const uint8_t* wr = W + (size_t)row * S * mq::Q4K_BYTES;
-    const int t = lane & 7;
-    const int p = t >> 1;        // 32-byte group of qs: sub-blocks 2p (low nibbles), 2p+1 (high)
-    const int h = t & 1;         // which 16 of the 32 positions
-    const int j0 = 2 * p, j1 = 2 * p + 1;
-    float acc = 0.0f;
-    for (int base = 0; base < S; base += 4 * kSteps) {
-        uint4 hv[kSteps], qv[kSteps];
-#pragma unroll
-        for (int u = 0; u < kSteps; ++u) {
-            const int sb = base + 4 * u + (lane >> 3);
+    const int S = K / mq::QK_K, nst = (S + 7) / 8;
+    const int g = lane >> 2, p = lane & 3;
+    const bool hi = p >= 2;
+    const uint32_t sh0 = 16u * (uint32_t)(p & 1), sh1 = sh0 + 8u;   // byte (2p mod 4), (2p+1 mod 4) of a word
+    const size_t row_bytes = (size_t)S * mq::Q4K_BYTES;
+    const uint32_t m4 = 0x0F0F0F0Fu, m4h = 0xF0F0F0F0u;
+    const int npairs = (N + 1) / 2;
+    const int G = gridDim.x * kRowsPerBlock;
+    for (int pr = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5); pr < npairs; pr += G) {   // warp-uniform
+        const int row = 2 * pr;
+        const bool two = row + 1 < N;
+        const uint8_t* wr = W + (size_t)row * row_bytes;
+        float acc0 = 0.0f, acc1 = 0.0f;
+        Q4Loads cur, nxt;
+        if (g < S) load_q4k(cur, wr + (size_t)g * mq::Q4K_BYTES, row_bytes, two, p);
+        for (int st = 0; st < nst; ++st) {
+            const int sb = 8 * st + g, sbn = sb + 8;
+            if (sbn < S) load_q4k(nxt, wr + (size_t)sbn * mq::Q4K_BYTES, row_bytes, two, p);
             if (sb < S) {
-                const uint8_t* blk = wr + (size_t)sb * mq::Q4K_BYTES;
-                hv[u] = __ldg(reinterpret_cast<const uint4*>(blk));
-                qv[u] = __ldcs(reinterpret_cast<const uint4*>(blk + 16 + 32 * p + 16 * h));
-            }
-        }
+                const int b0 = sb * 8 + 2 * p;
+                const int4* a = reinterpret_cast<const int4*>(aq + b0 * 32);   // blocks b0, b0 + 1: 4 x 16 bytes
+                const int4 a0 = __ldg(a), a1 = __ldg(a + 1), a2 = __ldg(a + 2), a3 = __ldg(a + 3);
+                const float2 da = __ldg(reinterpret_cast<const float2*>(ad + b0));
+                const int2 sv = __ldg(reinterpret_cast<const int2*>(as + b0));
 #pragma unroll
-        for (int u = 0; u < kSteps; ++u) {
-            const int sb = base + 4 * u + (lane >> 3);
-            if (sb < S) {
-                const int b0 = sb * 8 + j0, b1 = sb * 8 + j1;
-                const int4 a0 = __ldg(reinterpret_cast<const int4*>(aq + b0 * 32 + 16 * h));
-                const int4 a1 = __ldg(reinterpret_cast<const int4*>(aq + b1 * 32 + 16 * h));
-                const uint32_t m4 = 0x0F0F0F0Fu;
-                int I0 = 0, I1 = 0;
-                I0 = __dp4a((int)(qv[u].x & m4), a0.x, I0);
-                I0 = __dp4a((int)(qv[u].y & m4), a0.y, I0);
-                I0 = __dp4a((int)(qv[u].z & m4), a0.z, I0);
-                I0 = __dp4a((int)(qv[u].w & m4), a0.w, I0);
-                I1 = __dp4a((int)((qv[u].x >> 4) & m4), a1.x, I1);
-                I1 = __dp4a((int)((qv[u].y >> 4) & m4), a1.y, I1);
-                I1 = __dp4a((int)((qv[u].z >> 4) & m4), a1.z, I1);
-                I1 = __dp4a((int)((qv[u].w >> 4) & m4), a1.w, I1);
-                const float d = mq_f16_to_f32((uint16_t)(hv[u].x & 0xffffu));
-                const float dmin = mq_f16_to_f32((uint16_t)(hv[u].x >> 16));
-                int sc0, mn0, sc1, mn1;
-                q4k_scale_min(hv[u].y, hv[u].z, hv[u].w, j0, sc0, mn0);
-                q4k_scale_min(hv[u].y, hv[u].z, hv[u].w, j1, sc1, mn1);
-                const float da0 = __ldg(ad + b0), da1 = __ldg(ad + b1);
-                acc += da0 * (d * (float)(sc0 * I0)) + da1 * (d * (float)(sc1 * I1));
-                if (h == 0) {   // the block-sum (min) term is counted once per 32-block
-                    acc -= dmin * (da0 * (float)(mn0 * __ldg(as + b0)) + da1 * (float)(mn1 * __ldg(as + b1)));
+                for (int r = 0; r < 2; ++r) {
+                    if (r == 1 && !two) break;
+                    const uint4 q0 = cur.q0[r], q1 = cur.q1[r], hv = cur.hv[r];
+                    int I0 = __dp4a((int)(q0.x & m4), a0.x, 0);
+                    I0 = __dp4a((int)(q0.y & m4), a0.y, I0);
+                    I0 = __dp4a((int)(q0.z & m4), a0.z, I0);
+                    I0 = __dp4a((int)(q0.w & m4), a0.w, I0);
+                    I0 = __dp4a((int)(q1.x & m4), a1.x, I0);
+                    I0 = __dp4a((int)(q1.y & m4), a1.y, I0);
+                    I0 = __dp4a((int)(q1.z & m4), a1.z, I0);
+                    I0 = __dp4a((int)(q1.w & m4), a1.w, I0);
+                    int H = dp4a_us(q0.x & m4h, a2.x, 0);
+                    H = dp4a_us(q0.y & m4h, a2.y, H);
+                    H = dp4a_us(q0.z & m4h, a2.z, H);
+                    H = dp4a_us(q0.w & m4h, a2.w, H);
+                    H = dp4a_us(q1.x & m4h, a3.x, H);
+                    H = dp4a_us(q1.y & m4h, a3.y, H);
+                    H = dp4a_us(q1.z & m4h, a3.z, H);
+                    H = dp4a_us(q1.w & m4h, a3.w, H);
+                    const int I1 = H >> 4;   // exact: every term is a multiple of 16
+                    const uint32_t x0 = hv.y >> sh0, y0 = hv.z >> sh0, z0 = hv.w >> sh0;
+                    const uint32_t x1 = hv.y >> sh1, y1 = hv.z >> sh1, z1 = hv.w >> sh1;
+                    const int sc0 = (int)(hi ? ((z0 & 15u) | ((x0 >> 2) & 48u)) : (x0 & 63u));
+                    const int sc1 = (int)(hi ? ((z1 & 15u) | ((x1 >> 2) & 48u)) : (x1 & 63u));
+                    const int mn0 = (int)(hi ? (((z0 >> 4) & 15u) | ((y0 >> 2) & 48u)) : (y0 & 63u));
+                    const int mn1 = (int)(hi ? (((z1 >> 4) & 15u) | ((y1 >> 2) & 48u)) : (y1 & 63u));
+                    const float d = mq_f16_to_f32((uint16_t)(hv.x & 0xffffu));
+                    const float dmin = mq_f16_to_f32((uint16_t)(hv.x >> 16));
+                    const float v = d * (da.x * (float)(sc0 * I0) + da.y * (float)(sc1 * I1)) -
+                                    dmin * (da.x * (float)(mn0 * sv.x) + da.y * (float)(mn1 * sv.y));
+                    if (r == 0) acc0 += v;
+                    else acc1 += v;
                 }
             }
+            cur = nxt;
+        }
+        acc0 = warp_sum(acc0);
+        acc1 = warp_sum(acc1);
+        if (lane == 0) {
+            out[row] = acc0;
+            if (two) out[row + 1] = acc1;
         }
     }
-    acc = warp_sum(acc);
-    if (lane == 0) out[row] = acc;
 }
 
 // q6_K rows are only 2-byte aligned (210 B super-blocks), so a lane fetches the
@@ -182,12 +218,35 @@ int check_gemv(const mq_q8_plane* a, const void* w, int N, const float* out) {
     return mq::check_arch();
 }
 
+// Persistent grid: as many blocks as are resident at once (queried once per
+// kernel), never more than there are rows for.
+template <typename Kern>
+int gemv_grid(int N, Kern kern) {
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kThreads, 0) != cudaSuccess || b < 1) b = 1;
+        per_sm = b;
+    }
+    const long long need = ((long long)N + kRowsPerBlock - 1) / kRowsPerBlock;
+    const long long cap = (long long)mq::num_sms() * per_sm;
+    return (int)(need < cap ? need : cap);
+}
+
 }  // namespace
+
+namespace mq {
+// The decode kernels have no bounded waits; nothing to report.
+int take_gemv_device_error(cudaStream_t, unsigned* code) {
+    *code = 0;
+    return MQ_OK;
+}
+}  // namespace mq
 
 extern "C" int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     int rc = check_gemv(a, w, N, out);
     if (rc != MQ_OK || N == 0) return rc;
-    gemv_q4k_kernel<<<(N + kRowsPerBlock - 1) / kRowsPerBlock, kThreads, 0, stream>>>(
+    gemv_q4k_kernel<<<gemv_grid((N + 1) / 2, gemv_q4k_kernel), kThreads, 0, stream>>>(
         static_cast<const uint8_t*>(w), a->qs, a->d, a->s, out, N, a->K);
     return mq::launch_status();
 }

@@ -42,6 +42,7 @@ int num_sms();      // SM count of the current device (cached)
 // Device-side failure record (bounded waits) -----------------------------------
 // Each translation unit with bounded waits owns one word; these read and clear it.
 int take_gemm_device_error(cudaStream_t stream, unsigned* code);
+int take_gemv_device_error(cudaStream_t stream, unsigned* code);
 
 }  // namespace mq
 

@@ -153,28 +153,42 @@ __global__ void __launch_bounds__(kThreads) rms_quant_rows_kernel(const float4* 
     rms_quant_rounds(xr, w4, qs, d, s, qh, (long long)row * nrounds, 0, 1, nrounds, scale, lane);
 }
 
-// Few rows (decode): one 128-thread block per row. Warp 0 computes the scale in
-// the same order as above and broadcasts it through shared memory; all four
-// warps then quantize interleaved rounds ("72 · D3-7", §2c(i), Excerpt C).
-__global__ void __launch_bounds__(128) rms_quant_wide_kernel(const float4* __restrict__ x,
-                                                             const float4* __restrict__ w4,
-                                                             uint32_t* __restrict__ qs,
-                                                             float* __restrict__ d,
-                                                             int32_t* __restrict__ s,
-                                                             uint2* __restrict__ qh, int M, int K,
-                                                             float eps) {
+// Few rows (decode): one block per row with one warp per 128-float round (up to
+// 32 warps; more rounds wrap around). Every warp loads its first round while
+// warp 0 computes the scale in the same order as above; the scale goes through
+// shared memory ("72 · D3-7", §2c(i), Excerpt C: a wide block per decode row).
+__global__ void __launch_bounds__(1024) rms_quant_wide_kernel(const float4* __restrict__ x,
+                                                              const float4* __restrict__ w4,
+                                                              uint32_t* __restrict__ qs,
+                                                              float* __restrict__ d,
+                                                              int32_t* __restrict__ s,
+                                                              uint2* __restrict__ qh, int M, int K,
+                                                              float eps) {
     __shared__ float s_scale;
     const int lane = threadIdx.x & 31;
-    const int wid = threadIdx.x >> 5;
+    const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int row = blockIdx.x;
+    const int nrounds = K >> 7;
     const float4* xr = x + (long long)row * (K >> 2);
+    const float4 x0 = __ldg(xr + wid * 32 + lane);   // wid < nrounds by construction of the launch
+    const float4 w0 = __ldg(w4 + wid * 32 + lane);
     if (wid == 0) {
         const float sc = rms_scale_warp(xr, K, eps, lane);
         if (lane == 0) s_scale = sc;
     }
     __syncthreads();
-    const int nrounds = K >> 7;
-    rms_quant_rounds(xr, w4, qs, d, s, qh, (long long)row * nrounds, wid, 4, nrounds, s_scale, lane);
+    const float scale = s_scale;
+    const long long round0 = (long long)row * nrounds;
+    {
+        float dd;
+        int ss;
+        uint2 h;
+        const uint32_t q = mq_quant4_group8(__fmul_rn(__fmul_rn(x0.x, scale), w0.x), __fmul_rn(__fmul_rn(x0.y, scale), w0.y),
+                                            __fmul_rn(__fmul_rn(x0.z, scale), w0.z), __fmul_rn(__fmul_rn(x0.w, scale), w0.w),
+                                            dd, ss, h);
+        store_round(qs, d, s, qh, round0 + wid, lane, q, dd, ss, h);
+    }
+    if (wid + nw < nrounds) rms_quant_rounds(xr, w4, qs, d, s, qh, round0, wid + nw, nw, nrounds, scale, lane);
 }
 
 int flat_grid(long long rounds) {
@@ -232,7 +246,8 @@ extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float 
         rms_quant_rows_kernel<<<(M + rows_per_block - 1) / rows_per_block, kThreads, 0, stream>>>(
             x4, w4, qs, out->d, out->s, qh, M, K, eps);
     } else {
-        rms_quant_wide_kernel<<<M, 128, 0, stream>>>(x4, w4, qs, out->d, out->s, qh, M, K, eps);
+        const int warps = K / 128 < 32 ? K / 128 : 32;   // one warp per round, rounds beyond 32 wrap
+        rms_quant_wide_kernel<<<M, 32 * warps, 0, stream>>>(x4, w4, qs, out->d, out->s, qh, M, K, eps);
     }
     return mq::launch_status();
 }

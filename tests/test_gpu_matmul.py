@@ -93,7 +93,7 @@ def test_gemm_full_size_sampled_rows(kind, N, K):
 
 # ----------------------------------------------------------------- GEMV
 
-GEMV_SHAPES = [(256, 512), (1024, 5120), (100, 768), (5120, 13824), (1, 256)]
+GEMV_SHAPES = [(256, 512), (1024, 5120), (100, 768), (5120, 13824), (1, 256), (7001, 3584), (3, 1280)]
 
 
 @pytest.mark.parametrize("kind", ["q4k", "q6k"])
