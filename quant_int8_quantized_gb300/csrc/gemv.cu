@@ -9,9 +9,10 @@
 // which share the activation loads. A lane task is 64 weights — two whole
 // 32-blocks of one super-block — so the per-block scale work (the 6-bit scale
 // decode, the f32 scaling) is spread over as many weights as possible; 4 lanes
-// cover a super-block and a warp covers 8 super-blocks per step, with the loads
-// of the next step issued before the current one is used. Lane roles are fixed,
-// so the byte positions of a lane's scales are known once.
+// cover a super-block and a warp covers 8 super-blocks per step. (Loads are not
+// software-pipelined across steps: the registers that would take cost more in
+// occupancy than they gain.) Lane roles are fixed, so the byte positions of a
+// lane's scales are known once.
 //
 // q6_K: one warp per row; a lane task is 32 weights (16 positions of two
 // quarters), 8 lanes per super-block, 4 super-blocks per step, kSteps steps of
@@ -82,12 +83,11 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __res
         const bool two = row + 1 < N;
         const uint8_t* wr = W + (size_t)row * row_bytes;
         float acc0 = 0.0f, acc1 = 0.0f;
-        Q4Loads cur, nxt;
-        if (g < S) load_q4k(cur, wr + (size_t)g * mq::Q4K_BYTES, row_bytes, two, p);
+        Q4Loads cur;
         for (int st = 0; st < nst; ++st) {
-            const int sb = 8 * st + g, sbn = sb + 8;
-            if (sbn < S) load_q4k(nxt, wr + (size_t)sbn * mq::Q4K_BYTES, row_bytes, two, p);
+            const int sb = 8 * st + g;
             if (sb < S) {
+                load_q4k(cur, wr + (size_t)sb * mq::Q4K_BYTES, row_bytes, two, p);
                 const int b0 = sb * 8 + 2 * p;
                 const int4* a = reinterpret_cast<const int4*>(aq + b0 * 32);   // blocks b0, b0 + 1: 4 x 16 bytes
                 const int4 a0 = __ldg(a), a1 = __ldg(a + 1), a2 = __ldg(a + 2), a3 = __ldg(a + 3);
@@ -128,7 +128,6 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __res
                     else acc1 += v;
                 }
             }
-            cur = nxt;
         }
         acc0 = warp_sum(acc0);
         acc1 = warp_sum(acc1);
