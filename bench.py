@@ -80,8 +80,15 @@ def wbytes(kind, N, K):
     return N * (K // 256) * BYTES_PER_SB[kind]
 
 
-def plane_bytes(M, K):
-    return M * K + M * (K // 32) * 8
+def plane_bytes(M, K, f16=False):
+    """Bytes of a q8 plane: qs (1 B/elem), d and s (4 B per 32-block each), and, with f16,
+    the binary16 copy of the quants (2 B/elem) that the prefill producers also write."""
+    return M * K + M * (K // 32) * 8 + (2 * M * K if f16 else 0)
+
+
+def gemm_act_bytes(kind, M, K):
+    """Activation bytes a GEMM reads: the f16 quant copy and d (and s for q4_K's min term)."""
+    return 2 * M * K + M * (K // 32) * (8 if kind == "q4k" else 4)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -383,7 +390,8 @@ def run_case(spec: str, steps: int, warmup: int):
         out = torch.empty((M, N), dtype=torch.float32, device=dev)
         fn = (lambda: mq.gemm(wk, p, w, N, out)) if kind.startswith("gemm") else (lambda: mq.gemv(wk, p, w, N, out))
         flops = 2.0 * M * N * K
-        nbytes = wbytes(wk, N, K) + plane_bytes(M, K) + 4 * M * N
+        act = gemm_act_bytes(wk, M, K) if kind.startswith("gemm") else plane_bytes(M, K) - (0 if wk == "q4k" else M * (K // 32) * 4)
+        nbytes = wbytes(wk, N, K) + act + 4 * M * N
     else:
         M, K = dims
         x = S.normal((M, K), 0, "case.x", device=dev)
@@ -391,15 +399,15 @@ def run_case(spec: str, steps: int, warmup: int):
         flops = 0.0
         if kind == "quantize":
             fn = lambda: mq.mq_quantize_q8(x, p)
-            nbytes = 4 * M * K + plane_bytes(M, K)
+            nbytes = 4 * M * K + plane_bytes(M, K, f16=True)
         elif kind == "rms":
             w = S.normal((K,), 0, "case.rmsw", 1.0, 0.1, device=dev)
             fn = lambda: mq.mq_rms_quant(x, w, EPS, p)
-            nbytes = 4 * M * K + 4 * K + plane_bytes(M, K)
+            nbytes = 4 * M * K + 4 * K + plane_bytes(M, K, f16=True)
         elif kind == "swiglu":
             u = S.normal((M, K), 0, "case.u", device=dev)
             fn = lambda: mq.mq_swiglu_quant(x, u, p)
-            nbytes = 8 * M * K + plane_bytes(M, K)
+            nbytes = 8 * M * K + plane_bytes(M, K, f16=True)
         else:
             raise ValueError(kind)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 256 MB > L2

@@ -448,53 +448,64 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     rf.next(RF);
                     uint8_t* b0 = sm.f16[f0] + kTile;
                     uint8_t* b1 = sm.f16[f1] + kTile;
+                    // Rows >= N convert to zeros (q4_K: the copy zero-filled them, so their scales
+                    // are 0; q6_K: their scale is taken as 0). For q6_K all shared-memory loads of
+                    // the thread's rows come before any store: a store may alias a later load as
+                    // far as the compiler knows, which would serialise the rows.
+                    if constexpr (!Q6) {
+                        // sub-blocks 2P (low nibbles) and 2P+1 (high nibbles), positions 8c .. 8c+7. (Here
+                        // the per-row order measured faster than loads first: fewer live registers.)
 #pragma unroll
-                    for (int k = 0; k < kConvRows; ++k) {
-                        const int r = 8 * kConvWarps * k + rbase, n = n0 + r;
-                        uint4 o0 = make_uint4(0, 0, 0, 0), o1 = o0, o2 = o0, o3 = o0;
-                        if (n < N) {
-                            if constexpr (!Q6) {
-                                // sub-blocks 2P (low nibbles) and 2P+1 (high nibbles), positions 8c .. 8c+7
-                                const uint8_t* blk = stage + r * C::kBStride;
-                                const uint4 sp = *reinterpret_cast<const uint4*>(&sm.scpack[r][2 * P]);
-                                const uint2 q = *reinterpret_cast<const uint2*>(blk + 16 + 32 * P + 8 * c);
-                                const uint32_t m4 = 0x0F0F0F0Fu;
-                                nib4_to_f16_1024(q.x & m4, sp.x, sp.y, o0.x, o0.y);
-                                nib4_to_f16_1024(q.y & m4, sp.x, sp.y, o0.z, o0.w);
-                                nib4_to_f16_1024((q.x >> 4) & m4, sp.z, sp.w, o1.x, o1.y);
-                                nib4_to_f16_1024((q.y >> 4) & m4, sp.z, sp.w, o1.z, o1.w);
-                            } else {
-                                // blocks 2P, 2P+1: half h, quarters tq0 = 2(P&1), tq0+1
-                                const int delta = (int)(((unsigned long long)n * wstride + (unsigned long long)sb * C::kSB) & 15ull);
-                                const uint8_t* blk = stage + r * C::kBStride + delta;
-                                const int h = P >> 1, tq0 = 2 * (P & 1), nsh = (P & 1) ? 4 : 0;
-                                uint32_t l0a, l0b, l1a, l1b, qa, qb;
-                                lds8_unaligned(blk + 64 * h + 8 * c, l0a, l0b);
-                                lds8_unaligned(blk + 64 * h + 32 + 8 * c, l1a, l1b);
-                                lds8_unaligned(blk + 128 + 32 * h + 8 * c, qa, qb);
-                                const int sc0 = (int)(int8_t)blk[192 + 4 * P + (c >> 1)];
-                                const int sc1 = (int)(int8_t)blk[192 + 4 * P + 2 + (c >> 1)];
-                                const uint32_t m0 = h2_of_int(16 * sc0), a0 = h2_of_int(-16 * sc0);
-                                const uint32_t m1 = h2_of_int(16 * sc1), a1 = h2_of_int(-16 * sc1);
-                                const uint32_t hm0 = h2_of_int(256 * sc0), ha0 = h2_of_int(-288 * sc0);
-                                const uint32_t hm1 = h2_of_int(256 * sc1), ha1 = h2_of_int(-288 * sc1);
-                                const uint32_t m4 = 0x0F0F0F0Fu, m2 = 0x03030303u;
-                                // block 2P: B1 = sc*lo -> o0, B2 = 16 sc (hi - 2) -> o1
-                                nib4_to_f16_one((l0a >> nsh) & m4, m0, a0, o0.x, o0.y);
-                                nib4_to_f16_one((l0b >> nsh) & m4, m0, a0, o0.z, o0.w);
-                                nib4_to_f16_one((qa >> (2 * tq0)) & m2, hm0, ha0, o1.x, o1.y);
-                                nib4_to_f16_one((qb >> (2 * tq0)) & m2, hm0, ha0, o1.z, o1.w);
-                                // block 2P+1 -> o2, o3
-                                nib4_to_f16_one((l1a >> nsh) & m4, m1, a1, o2.x, o2.y);
-                                nib4_to_f16_one((l1b >> nsh) & m4, m1, a1, o2.z, o2.w);
-                                nib4_to_f16_one((qa >> (2 * tq0 + 2)) & m2, hm1, ha1, o3.x, o3.y);
-                                nib4_to_f16_one((qb >> (2 * tq0 + 2)) & m2, hm1, ha1, o3.z, o3.w);
-                            }
-                        }
-                        *reinterpret_cast<uint4*>(b0 + tile_off(r, c)) = o0;
-                        if constexpr (!Q6) {
+                        for (int k = 0; k < kConvRows; ++k) {
+                            const int r = 8 * kConvWarps * k + rbase;
+                            const uint4 sp = *reinterpret_cast<const uint4*>(&sm.scpack[r][2 * P]);
+                            const uint2 q = *reinterpret_cast<const uint2*>(stage + r * C::kBStride + 16 + 32 * P + 8 * c);
+                            const uint32_t m4 = 0x0F0F0F0Fu;
+                            uint4 o0, o1;
+                            nib4_to_f16_1024(q.x & m4, sp.x, sp.y, o0.x, o0.y);
+                            nib4_to_f16_1024(q.y & m4, sp.x, sp.y, o0.z, o0.w);
+                            nib4_to_f16_1024((q.x >> 4) & m4, sp.z, sp.w, o1.x, o1.y);
+                            nib4_to_f16_1024((q.y >> 4) & m4, sp.z, sp.w, o1.z, o1.w);
+                            *reinterpret_cast<uint4*>(b0 + tile_off(r, c)) = o0;
                             *reinterpret_cast<uint4*>(b1 + tile_off(r, c)) = o1;
-                        } else {
+                        }
+                    } else {
+                        // blocks 2P, 2P+1: half h, quarters tq0 = 2(P&1), tq0+1
+                        const int h = P >> 1, tq0 = 2 * (P & 1), nsh = (P & 1) ? 4 : 0;
+                        uint32_t l0a[kConvRows], l0b[kConvRows], l1a[kConvRows], l1b[kConvRows], qa[kConvRows],
+                            qb[kConvRows];
+                        int sc0[kConvRows], sc1[kConvRows];
+#pragma unroll
+                        for (int k = 0; k < kConvRows; ++k) {
+                            const int r = 8 * kConvWarps * k + rbase, n = n0 + r;
+                            const int delta = (int)(((unsigned long long)n * wstride + (unsigned long long)sb * C::kSB) & 15ull);
+                            const uint8_t* blk = stage + r * C::kBStride + delta;
+                            lds8_unaligned(blk + 64 * h + 8 * c, l0a[k], l0b[k]);
+                            lds8_unaligned(blk + 64 * h + 32 + 8 * c, l1a[k], l1b[k]);
+                            lds8_unaligned(blk + 128 + 32 * h + 8 * c, qa[k], qb[k]);
+                            sc0[k] = (n < N) ? (int)(int8_t)blk[192 + 4 * P + (c >> 1)] : 0;
+                            sc1[k] = (n < N) ? (int)(int8_t)blk[192 + 4 * P + 2 + (c >> 1)] : 0;
+                        }
+#pragma unroll
+                        for (int k = 0; k < kConvRows; ++k) {
+                            const int r = 8 * kConvWarps * k + rbase;
+                            const uint32_t m0 = h2_of_int(16 * sc0[k]), a0 = h2_of_int(-16 * sc0[k]);
+                            const uint32_t m1 = h2_of_int(16 * sc1[k]), a1 = h2_of_int(-16 * sc1[k]);
+                            const uint32_t hm0 = h2_of_int(256 * sc0[k]), ha0 = h2_of_int(-288 * sc0[k]);
+                            const uint32_t hm1 = h2_of_int(256 * sc1[k]), ha1 = h2_of_int(-288 * sc1[k]);
+                            const uint32_t m4 = 0x0F0F0F0Fu, m2 = 0x03030303u;
+                            uint4 o0, o1, o2, o3;
+                            // block 2P: B1 = sc*lo -> o0, B2 = 16 sc (hi - 2) -> o1
+                            nib4_to_f16_one((l0a[k] >> nsh) & m4, m0, a0, o0.x, o0.y);
+                            nib4_to_f16_one((l0b[k] >> nsh) & m4, m0, a0, o0.z, o0.w);
+                            nib4_to_f16_one((qa[k] >> (2 * tq0)) & m2, hm0, ha0, o1.x, o1.y);
+                            nib4_to_f16_one((qb[k] >> (2 * tq0)) & m2, hm0, ha0, o1.z, o1.w);
+                            // block 2P+1 -> o2, o3
+                            nib4_to_f16_one((l1a[k] >> nsh) & m4, m1, a1, o2.x, o2.y);
+                            nib4_to_f16_one((l1b[k] >> nsh) & m4, m1, a1, o2.z, o2.w);
+                            nib4_to_f16_one((qa[k] >> (2 * tq0 + 2)) & m2, hm1, ha1, o3.x, o3.y);
+                            nib4_to_f16_one((qb[k] >> (2 * tq0 + 2)) & m2, hm1, ha1, o3.z, o3.w);
+                            *reinterpret_cast<uint4*>(b0 + tile_off(r, c)) = o0;
                             *reinterpret_cast<uint4*>(b0 + kTile + tile_off(r, c)) = o1;
                             *reinterpret_cast<uint4*>(b1 + tile_off(r, c)) = o2;
                             *reinterpret_cast<uint4*>(b1 + kTile + tile_off(r, c)) = o3;

@@ -54,9 +54,22 @@ __device__ __forceinline__ float mq_f16_to_f32(uint16_t h) {
     return f;
 }
 
+// rint(v / d) with v / d the correctly rounded f32 quotient, computed as
+// rint(v * (1/d)) unless that product lies within 6.2e-5 of a rounding boundary
+// (n + 1/2), where the exact quotient is taken instead. For |v / d| <= 128 the
+// product is within 2e-5 of the rounded quotient (two roundings of 2^-24
+// relative each), so both round to the same integer outside that band.
+__device__ __forceinline__ int mq_rint_div(float v, float d, float inv) {
+    const float t = v * inv;
+    const float r = rintf(t);
+    if (0.5f - fabsf(t - r) > 6.2e-5f) return (int)r;
+    return __float2int_rn(__fdiv_rn(v, d));
+}
+
 // Quantize four f32 values that belong to one 32-block whose 8 owners are the
 // lanes of one aligned 8-lane group. amax and the int sum are combined with xor
 // shuffles at offsets 4, 2, 1 (max and integer sums are exact in any order).
+// q = rint(v / d) with the correctly rounded quotient (see mq_rint_div).
 // Returns the packed int8 quants; d and s are valid in every lane of the group.
 __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v2, float v3,
                                                      float& d_out, int& s_out, uint2& h_out) {
@@ -67,10 +80,18 @@ __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v
     const float d = __fdiv_rn(am, 127.0f);
     int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
     if (d != 0.0f) {
-        q0 = __float2int_rn(__fdiv_rn(v0, d));
-        q1 = __float2int_rn(__fdiv_rn(v1, d));
-        q2 = __float2int_rn(__fdiv_rn(v2, d));
-        q3 = __float2int_rn(__fdiv_rn(v3, d));
+        const float inv = __frcp_rn(d);
+        if (isfinite(inv)) {
+            q0 = mq_rint_div(v0, d, inv);
+            q1 = mq_rint_div(v1, d, inv);
+            q2 = mq_rint_div(v2, d, inv);
+            q3 = mq_rint_div(v3, d, inv);
+        } else {   // d subnormal: 1/d overflows
+            q0 = __float2int_rn(__fdiv_rn(v0, d));
+            q1 = __float2int_rn(__fdiv_rn(v1, d));
+            q2 = __float2int_rn(__fdiv_rn(v2, d));
+            q3 = __float2int_rn(__fdiv_rn(v3, d));
+        }
         q0 = max(-127, min(127, q0));
         q1 = max(-127, min(127, q1));
         q2 = max(-127, min(127, q2));

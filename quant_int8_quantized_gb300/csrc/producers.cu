@@ -59,8 +59,10 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __r
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
-    // (g / (1 + expf(-g))) * u, each step a correctly rounded f32 op except expf.
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+    // (g / (1 + expf(-g))) * u, the quotient as g times the correctly rounded
+    // reciprocal (within 1 ulp of the rounded quotient; this plane is compared
+    // to the oracle within a tolerance, as expf already differs by platform).
+    return __fmul_rn(__fmul_rn(g, __frcp_rn(__fadd_rn(1.0f, expf(-g)))), u);
 }
 
 __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __restrict__ g,
@@ -136,25 +138,8 @@ __device__ __forceinline__ void rms_quant_rounds(const float4* __restrict__ xr, 
     }
 }
 
-// Many rows: one warp per row (8 rows per block).
-__global__ void __launch_bounds__(kThreads) rms_quant_rows_kernel(const float4* __restrict__ x,
-                                                                  const float4* __restrict__ w4,
-                                                                  uint32_t* __restrict__ qs,
-                                                                  float* __restrict__ d,
-                                                                  int32_t* __restrict__ s,
-                                                                  uint2* __restrict__ qh, int M, int K,
-                                                                  float eps) {
-    const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    if (row >= M) return;   // warp-uniform
-    const int nrounds = K >> 7;
-    const float4* xr = x + (long long)row * (K >> 2);
-    const float scale = rms_scale_warp(xr, K, eps, lane);
-    rms_quant_rounds(xr, w4, qs, d, s, qh, (long long)row * nrounds, 0, 1, nrounds, scale, lane);
-}
-
-// Few rows (decode): one block per row with one warp per 128-float round (up to
-// 32 warps; more rounds wrap around). Every warp loads its first round while
+// One block per row with one warp per 128-float round (at most 32 warps, or 4
+// when there are many rows; more rounds wrap around). Every warp loads its first round while
 // warp 0 computes the scale in the same order as above; the scale goes through
 // shared memory ("72 · D3-7", §2c(i), Excerpt C: a wide block per decode row).
 __global__ void __launch_bounds__(1024) rms_quant_wide_kernel(const float4* __restrict__ x,
@@ -240,14 +225,12 @@ extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float 
     const float4* w4 = reinterpret_cast<const float4*>(w);
     uint32_t* qs = reinterpret_cast<uint32_t*>(out->qs);
     uint2* qh = reinterpret_cast<uint2*>(out->qh);
-    // One warp per row fills the machine once there are a few warps per SM.
-    if (M >= 4 * mq::num_sms()) {
-        const int rows_per_block = kThreads / 32;
-        rms_quant_rows_kernel<<<(M + rows_per_block - 1) / rows_per_block, kThreads, 0, stream>>>(
-            x4, w4, qs, out->d, out->s, qh, M, K, eps);
-    } else {
-        const int warps = K / 128 < 32 ? K / 128 : 32;   // one warp per round, rounds beyond 32 wrap
-        rms_quant_wide_kernel<<<M, 32 * warps, 0, stream>>>(x4, w4, qs, out->d, out->s, qh, M, K, eps);
-    }
+    // One block per row. Its first warp computes the scale in the pinned order while every
+    // warp loads its first round; the quantize rounds are spread over the block's warps: up
+    // to 32 for a few rows (decode), 4 once there are enough rows to fill the machine.
+    const int rounds = K / 128;
+    const int cap = (M >= 4 * mq::num_sms()) ? 4 : 32;
+    const int warps = rounds < cap ? rounds : cap;
+    rms_quant_wide_kernel<<<M, 32 * warps, 0, stream>>>(x4, w4, qs, out->d, out->s, qh, M, K, eps);
     return mq::launch_status();
 }

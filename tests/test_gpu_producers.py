@@ -46,6 +46,44 @@ def test_quantize_bit_exact(M, K, outliers):
     assert_plane_equal(gp.numpy(), O.quantize_q8(x.numpy()), f"quantize {M}x{K}")
 
 
+def _boundary_blocks(seed=7):
+    """32-blocks whose element 0 is the block's amax and whose other elements sit on
+    and a few ulps around (n + 1/2) * d, d = amax / 127 rounded to f32: the
+    quotients v / d straddle the rounding boundaries of q = rint(v / d)."""
+    rng = np.random.default_rng(seed)
+    blocks = []
+    for am in [127.0, 100.0, 3.0, 0.0123, 1e-3, 2.5e-36, 5e-39]:
+        am = np.float32(am)
+        d = np.float32(am / np.float32(127.0))
+        vals = []
+        for n in rng.integers(-126, 126, size=40):
+            t = np.float32(np.float32(n + 0.5) * d)
+            for k in (-3, -1, 0, 1, 3):
+                v = t
+                for _ in range(abs(k)):
+                    v = np.nextafter(v, np.float32(np.inf if k > 0 else -np.inf), dtype=np.float32)
+                vals.append(v)
+        vals = np.array(vals, dtype=np.float32)
+        vals = vals[np.abs(vals) < am]
+        for i in range(0, len(vals) - 30, 31):
+            blocks.append(np.concatenate([[am], vals[i:i + 31]]).astype(np.float32))
+    blocks = np.stack(blocks)
+    pad = (-len(blocks)) % 8
+    if pad:
+        blocks = np.concatenate([blocks, blocks[:pad]])
+    return blocks.reshape(-1, 256)
+
+
+def test_quantize_bit_exact_at_rounding_boundaries():
+    x = torch.from_numpy(_boundary_blocks())
+    M, K = x.shape
+    gp = GuardedPlane(M, K)
+    mq.mq_quantize_q8(x.cuda(), gp.plane)
+    torch.cuda.synchronize()
+    gp.check()
+    assert_plane_equal(gp.numpy(), O.quantize_q8(x.numpy()), "quantize at rounding boundaries")
+
+
 @pytest.mark.parametrize("M,K", SHAPES)
 def test_rms_quant_bit_exact(M, K):
     x = _x(M, K, f"r{M}x{K}")
