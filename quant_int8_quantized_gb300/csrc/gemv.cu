@@ -20,6 +20,12 @@
 //
 // The activation plane (a few KB) stays in L1/L2 and is shared by every warp.
 //
+// Both are launched with programmatic stream serialization: a block lets the next
+// kernel be scheduled as soon as it starts, and loads its first weights before it
+// waits for the kernel that produced the activation plane, so the previous
+// kernel's tail overlaps this one's first DRAM round trip. Nothing is written and
+// no activation is read before that wait.
+//
 // HBM roofline: the weight stream, 0.5625 B/weight (q4_K) or 0.8203 B/weight
 // (q6_K), plus 4 B per output.
 
@@ -69,9 +75,11 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __res
                                                             const float* __restrict__ ad,
                                                             const int32_t* __restrict__ as,
                                                             float* __restrict__ out, int N, int K) {
+    mq_grid_release();
     const int lane = threadIdx.x & 31;
     const int S = K / mq::QK_K, nst = (S + 7) / 8;
     const int g = lane >> 2, p = lane & 3;
+    bool waited = false;   // weights of the first step are loaded before waiting for the plane's producer
     const bool hi = p >= 2;
     const uint32_t sh0 = 16u * (uint32_t)(p & 1), sh1 = sh0 + 8u;   // byte (2p mod 4), (2p+1 mod 4) of a word
     const size_t row_bytes = (size_t)S * mq::Q4K_BYTES;
@@ -88,6 +96,10 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __res
             const int sb = 8 * st + g;
             if (sb < S) {
                 load_q4k(cur, wr + (size_t)sb * mq::Q4K_BYTES, row_bytes, two, p);
+                if (!waited) {
+                    mq_grid_wait();
+                    waited = true;
+                }
                 const int b0 = sb * 8 + 2 * p;
                 const int4* a = reinterpret_cast<const int4*>(aq + b0 * 32);   // blocks b0, b0 + 1: 4 x 16 bytes
                 const int4 a0 = __ldg(a), a1 = __ldg(a + 1), a2 = __ldg(a + 2), a3 = __ldg(a + 3);
@@ -162,11 +174,13 @@ __global__ void __launch_bounds__(kThreads) gemv_q6k_kernel(const uint8_t* __res
                                                             const int8_t* __restrict__ aq,
                                                             const float* __restrict__ ad,
                                                             float* __restrict__ out, int N, int K) {
+    mq_grid_release();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
     if (row >= N) return;   // warp-uniform
     const int S = K / mq::QK_K;
     const uint8_t* wr = W + (size_t)row * S * mq::Q6K_BYTES;
+    bool waited = false;   // weights of the first step are loaded before waiting for the plane's producer
     const int t = lane & 7;
     const int hh = t >> 2;          // half of the super-block (128 elements)
     const int qq = (t >> 1) & 1;    // quarter pair: quarters qq (low nibbles) and qq+2 (high nibbles)
@@ -187,6 +201,10 @@ __global__ void __launch_bounds__(kThreads) gemv_q6k_kernel(const uint8_t* __res
                 const int sc1 = (int)(int8_t)__ldg(blk + 192 + g1);
                 const float d = mq_f16_to_f32(__ldg(reinterpret_cast<const unsigned short*>(blk + 208)));
                 const int b0 = sb * 8 + blk0, b1 = sb * 8 + blk1;
+                if (!waited) {
+                    mq_grid_wait();
+                    waited = true;
+                }
                 const int4 a0 = __ldg(reinterpret_cast<const int4*>(aq + b0 * 32 + 16 * h));
                 const int4 a1 = __ldg(reinterpret_cast<const int4*>(aq + b1 * 32 + 16 * h));
                 const int a0w[4] = {a0.x, a0.y, a0.z, a0.w};
@@ -245,15 +263,13 @@ int take_gemv_device_error(cudaStream_t, unsigned* code) {
 extern "C" int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     int rc = check_gemv(a, w, N, out);
     if (rc != MQ_OK || N == 0) return rc;
-    gemv_q4k_kernel<<<gemv_grid((N + 1) / 2, gemv_q4k_kernel), kThreads, 0, stream>>>(
-        static_cast<const uint8_t*>(w), a->qs, a->d, a->s, out, N, a->K);
-    return mq::launch_status();
+    return mq::launch_pdl(gemv_q4k_kernel, dim3(gemv_grid((N + 1) / 2, gemv_q4k_kernel)), dim3(kThreads), 0, stream,
+                          static_cast<const uint8_t*>(w), a->qs, a->d, a->s, out, N, a->K);
 }
 
 extern "C" int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     int rc = check_gemv(a, w, N, out);
     if (rc != MQ_OK || N == 0) return rc;
-    gemv_q6k_kernel<<<(N + kRowsPerBlock - 1) / kRowsPerBlock, kThreads, 0, stream>>>(
-        static_cast<const uint8_t*>(w), a->qs, a->d, out, N, a->K);
-    return mq::launch_status();
+    return mq::launch_pdl(gemv_q6k_kernel, dim3((N + kRowsPerBlock - 1) / kRowsPerBlock), dim3(kThreads), 0, stream,
+                          static_cast<const uint8_t*>(w), a->qs, a->d, out, N, a->K);
 }

@@ -39,6 +39,26 @@ inline int launch_status() {
 
 int num_sms();      // SM count of the current device (cached)
 
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel on the stream is finishing. Kernels launched this way call
+// mq_grid_wait() before reading anything an earlier kernel writes and before
+// writing anything, and mq_grid_release() so that their own dependents can start.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? MQ_OK : MQ_ERR_LAUNCH;
+}
+
 // Device-side failure record (bounded waits) -----------------------------------
 // Each translation unit with bounded waits owns one word; these read and clear it.
 int take_gemm_device_error(cudaStream_t stream, unsigned* code);
@@ -47,6 +67,13 @@ int take_gemv_device_error(cudaStream_t stream, unsigned* code);
 }  // namespace mq
 
 // Device helpers -----------------------------------------------------------------
+
+// Wait until the kernels this one depends on (programmatic launch) have completed
+// and their writes are visible; a no-op for an ordinary launch.
+__device__ __forceinline__ void mq_grid_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel on the stream be scheduled once every block of this one has
+// called this (or exited).
+__device__ __forceinline__ void mq_grid_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ float mq_f16_to_f32(uint16_t h) {
     float f;

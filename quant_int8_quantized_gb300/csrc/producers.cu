@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __r
                                                                float* __restrict__ d,
                                                                int32_t* __restrict__ s,
                                                                uint2* __restrict__ qh, long long rounds) {
+    mq_grid_release();
+    mq_grid_wait();
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * kThreads) >> 5;
@@ -71,6 +73,8 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __
                                                                 float* __restrict__ d,
                                                                 int32_t* __restrict__ s,
                                                                 uint2* __restrict__ qh, long long rounds) {
+    mq_grid_release();
+    mq_grid_wait();
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * kThreads) >> 5;
@@ -149,6 +153,8 @@ __global__ void __launch_bounds__(1024) rms_quant_wide_kernel(const float4* __re
                                                               int32_t* __restrict__ s,
                                                               uint2* __restrict__ qh, int M, int K,
                                                               float eps) {
+    mq_grid_release();
+    mq_grid_wait();
     __shared__ float s_scale;
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -200,10 +206,9 @@ extern "C" int mq_quantize_q8(const float* x, int M, int K, const mq_q8_plane* o
     int rc = check_producer(x, x, M, K, out);
     if (rc != MQ_OK || M == 0) return rc;
     const long long rounds = (long long)M * K / 128;
-    quantize_q8_kernel<<<flat_grid(rounds), kThreads, 0, stream>>>(
-        reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(out->qs), out->d, out->s,
-        reinterpret_cast<uint2*>(out->qh), rounds);
-    return mq::launch_status();
+    return mq::launch_pdl(quantize_q8_kernel, dim3(flat_grid(rounds)), dim3(kThreads), 0, stream,
+                          reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(out->qs), out->d, out->s,
+                          reinterpret_cast<uint2*>(out->qh), rounds);
 }
 
 extern "C" int mq_swiglu_quant(const float* g, const float* u, int M, int K, const mq_q8_plane* out,
@@ -211,10 +216,10 @@ extern "C" int mq_swiglu_quant(const float* g, const float* u, int M, int K, con
     int rc = check_producer(g, u, M, K, out);
     if (rc != MQ_OK || M == 0) return rc;
     const long long rounds = (long long)M * K / 128;
-    swiglu_quant_kernel<<<flat_grid(rounds), kThreads, 0, stream>>>(
-        reinterpret_cast<const float4*>(g), reinterpret_cast<const float4*>(u),
-        reinterpret_cast<uint32_t*>(out->qs), out->d, out->s, reinterpret_cast<uint2*>(out->qh), rounds);
-    return mq::launch_status();
+    return mq::launch_pdl(swiglu_quant_kernel, dim3(flat_grid(rounds)), dim3(kThreads), 0, stream,
+                          reinterpret_cast<const float4*>(g), reinterpret_cast<const float4*>(u),
+                          reinterpret_cast<uint32_t*>(out->qs), out->d, out->s, reinterpret_cast<uint2*>(out->qh),
+                          rounds);
 }
 
 extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float eps, const mq_q8_plane* out,
@@ -231,6 +236,6 @@ extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float 
     const int rounds = K / 128;
     const int cap = (M >= 4 * mq::num_sms()) ? 4 : 32;
     const int warps = rounds < cap ? rounds : cap;
-    rms_quant_wide_kernel<<<M, 32 * warps, 0, stream>>>(x4, w4, qs, out->d, out->s, qh, M, K, eps);
-    return mq::launch_status();
+    return mq::launch_pdl(rms_quant_wide_kernel, dim3(M), dim3(32 * warps), 0, stream, x4, w4, qs, out->d, out->s, qh,
+                          M, K, eps);
 }
