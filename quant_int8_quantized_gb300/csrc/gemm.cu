@@ -303,17 +303,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
         } else if (warp == 1) {
             // ---------------------------------------------------- MMA issuer
-            if (lane == 0) {
-                Ring rf, rm, rt;
-                const uint32_t idesc = tc::instr_desc(BM, BN, 0);
-                const uint32_t idesc32 = tc::instr_desc(BM, BN, 2);
-                bool issued = false;
-                for (int t = blockIdx.x; t < tiles && !aborted(sm); t += gridDim.x) {
-                    for (int sb = 0; sb < S && !aborted(sm); ++sb) {
-                        for (int j = 0; j < 8; ++j) {
-                            if (!wait_or_abort(sm, &sm.fullF[rf.i], rf.ph)) break;
-                            if (!wait_or_abort(sm, &sm.tempty[rt.i], rt.ph ^ 1u)) break;
-                            tc::tc_fence_after();
+            // The whole warp runs the loop and waits; lane 0 issues. (A warp whose other 31
+            // lanes stay parked while one lane runs the kernel-long loop slows every warp of
+            // its SM sub-partition.)
+            Ring rf, rm, rt;
+            const uint32_t idesc = tc::instr_desc(BM, BN, 0);
+            const uint32_t idesc32 = tc::instr_desc(BM, BN, 2);
+            bool issued = false;
+            for (int t = blockIdx.x; t < tiles && !waborted(sm); t += gridDim.x) {
+                for (int sb = 0; sb < S && !waborted(sm); ++sb) {
+                    for (int j = 0; j < 8; ++j) {
+                        if (!wwait(sm, &sm.fullF[rf.i], rf.ph)) break;
+                        if (!wwait(sm, &sm.tempty[rt.i], rt.ph ^ 1u)) break;
+                        tc::tc_fence_after();
+                        if (lane == 0) {
                             const uint32_t d = tbase + kSlotCol0 + 128u * rt.i;
                             const uint32_t sa = tc::smem_u32(sm.f16[rf.i]);
 #pragma unroll
@@ -327,15 +330,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             }
                             tc::mma_commit(&sm.emptyF[rf.i]);
                             tc::mma_commit(&sm.tfull[rt.i]);
-                            issued = true;
-                            rf.next(RF);
-                            rt.next(RT);
                         }
-                        if constexpr (!Q6) {
-                            if (aborted(sm)) break;
-                            if (!wait_or_abort(sm, &sm.fullM[rm.i], rm.ph)) break;
-                            if (!wait_or_abort(sm, &sm.tempty[rt.i], rt.ph ^ 1u)) break;
-                            tc::tc_fence_after();
+                        __syncwarp();
+                        issued = true;
+                        rf.next(RF);
+                        rt.next(RT);
+                    }
+                    if constexpr (!Q6) {
+                        if (waborted(sm)) break;
+                        if (!wwait(sm, &sm.fullM[rm.i], rm.ph)) break;
+                        if (!wwait(sm, &sm.tempty[rt.i], rt.ph ^ 1u)) break;
+                        tc::tc_fence_after();
+                        if (lane == 0) {
                             const uint32_t d = tbase + kSlotCol0 + 128u * rt.i;
                             const uint32_t sa = tc::smem_u32(sm.ms[rm.i]);
 #pragma unroll
@@ -345,17 +351,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                              k ? 1u : 0u);
                             tc::mma_commit(&sm.emptyM[rm.i]);
                             tc::mma_commit(&sm.tfull[rt.i]);
-                            rm.next(RM);
-                            rt.next(RT);
                         }
+                        __syncwarp();
+                        rm.next(RM);
+                        rt.next(RT);
                     }
                 }
-                if (issued) {   // every MMA of this CTA has completed before TMEM is freed
-                    tc::mma_commit(&sm.mma_done);
-                    tc::mbar_wait(&sm.mma_done, 0, kWaitLimitNs);
-                }
-                tc::tc_fence_before();
             }
+            if (lane == 0 && issued) {   // every MMA of this CTA has completed before TMEM is freed
+                tc::mma_commit(&sm.mma_done);
+                tc::mbar_wait(&sm.mma_done, 0, kWaitLimitNs);
+            }
+            tc::tc_fence_before();
             __syncwarp();
         }
     } else if (warp < 4 + kConvWarps) {
