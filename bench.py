@@ -367,6 +367,65 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------------------- the shape/token sweep
+
+SWEEP_M = [1, 16, 64, 512, 3314, 8192]
+SWEEP_NK = [(1024, 5120), (3584, 3584), (18944, 3584), (3584, 18944), (13824, 5120)]
+
+
+def run_sweep(steps: int, warmup: int):
+    """Time every (M, N, K, type) case of the sweep (activations with 1% x50 outliers), M = 1
+    through the decode GEMV, M >= 16 through the GEMM, with a 256 MB L2 flush before each timed
+    launch. Each case's roofline is whichever of the tensor time (2MNK / measured bf16 burst peak)
+    and the stream time (algorithmic bytes / measured HBM bandwidth) is larger; `frac` is that
+    time over the measured one."""
+    import __graft_entry__
+    __graft_entry__.build()
+    from quant_int8_quantized_gb300 import mq, synth as S
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _, peak_burst, hbm, _ = load_peaks()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for kind in ("q4k", "q6k"):
+        for N, K in SWEEP_NK:
+            w = S.weights(kind, N, K, 0, f"sweep.{kind}.{N}x{K}", device=dev)
+            for M in SWEEP_M:
+                x = S.with_outliers(S.normal((M, K), 0, f"sweep.x.{M}x{K}", device=dev), 0, f"sweep.o.{M}x{K}")
+                p = mq.Plane.empty(M, K, dev, f16=M > 1)
+                mq.mq_quantize_q8(x, p)
+                out = torch.empty((M, N), dtype=torch.float32, device=dev)
+                if M == 1:
+                    fn = lambda: mq.gemv(kind, p, w, N, out.view(-1))
+                    act = plane_bytes(1, K) - (0 if kind == "q4k" else K // 32 * 4)
+                else:
+                    fn = lambda: mq.gemm(kind, p, w, N, out)
+                    act = gemm_act_bytes(kind, M, K)
+                nbytes = wbytes(kind, N, K) + act + 4 * M * N
+                for _ in range(max(1, warmup)):
+                    fn()
+                ts = []
+                for _ in range(steps):
+                    flush.fill_(1.0)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    fn()
+                    b.record()
+                    torch.cuda.synchronize()
+                    ts.append(a.elapsed_time(b) * 1e-3)
+                t = statistics.median(ts)
+                t_tensor = 2.0 * M * N * K / (peak_burst * 1e12)
+                t_stream = nbytes / (hbm * 1e9)
+                line = {"case": f"{'gemv' if M == 1 else 'gemm'}_{kind}:{M}x{N}x{K}", "us": t * 1e6,
+                        "TFLOPs": 2.0 * M * N * K / t / 1e12, "GBps": nbytes / t / 1e9,
+                        "bound": "tensor" if t_tensor >= t_stream else "hbm",
+                        "frac": max(t_tensor, t_stream) / t}
+                print(json.dumps(line))
+                del x, p, out
+    if mq.mq_device_status() != mq.MQ_OK:
+        raise RuntimeError("device status")
+    return 0
+
+
 # ----------------------------------------------------------------------------- single-kernel cases
 
 def run_case(spec: str, steps: int, warmup: int):
@@ -443,9 +502,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--case", default=None, help="time one kernel, e.g. gemm_q4k:3314x18944x3584")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the 60-case shape/token sweep; one JSON line per case with its roofline fraction")
     args = ap.parse_args()
     if args.case:
         return run_case(args.case, args.steps, args.warmup)
+    if args.sweep:
+        return run_sweep(args.steps, args.warmup)
     if args.impl == "reference":
         return run_reference(args)
     ws, rank, local = dist_setup()

@@ -138,6 +138,10 @@ int mq_swiglu_quant(const float* g, const float* u, int M, int K,
  * (MQ_ERR_NULL otherwise); w: N rows of super-blocks; out: f32 [a->M][N]
  * row-major, overwritten. Any M >= 1 is accepted (the kernel is built for
  * M >= 16). Accuracy: within 1e-3 * sum_k |a||w| per element.
+ * When the output has fewer 128 x 128 tiles than the GPU has SMs (small M or
+ * N), the K axis is split across several thread blocks, `out` is zeroed on
+ * `stream` and the partial sums are added with f32 atomics: the result is then
+ * within the same bound, but its last bits may differ from run to run.
  */
 int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);

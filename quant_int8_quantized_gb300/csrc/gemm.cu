@@ -115,6 +115,16 @@ struct Ring {
     }
 };
 
+// A work unit: one output tile and one slice [sb0, sb1) of its super-blocks. With
+// split-K, splits > 1 units share a tile and add their partial sums into it.
+struct Work {
+    int m0, n0, sb0, sb1;
+};
+__device__ __forceinline__ Work work_of(int u, int splits, int num_mt, int S) {
+    const int t = u / splits, sp = u - t * splits;
+    return Work{(t % num_mt) * BM, (t / num_mt) * BN, (sp * S) / splits, ((sp + 1) * S) / splits};
+}
+
 __device__ __forceinline__ uint32_t tile_off(int r, int kg) {
     return (uint32_t)((r >> 3) * kSBO + kg * kLBO + (r & 7) * 16);
 }
@@ -226,8 +236,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                                            const __grid_constant__ CUtensorMap tmS,
                                                            const __grid_constant__ CUtensorMap tmW,
                                                            const uint8_t* __restrict__ W, float* __restrict__ out,
-                                                           int M, int N, int K, unsigned long long wstride,
-                                                           unsigned long long wtotal) {
+                                                           int M, int N, int K, int splits,
+                                                           unsigned long long wstride, unsigned long long wtotal) {
     using C = Cfg<Q6>;
     constexpr int RF = C::RF;
     extern __shared__ uint8_t smem_raw[];
@@ -235,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = K / mq::QK_K;
     const int num_mt = (M + BM - 1) / BM, num_nt = (N + BN - 1) / BN;
-    const int tiles = num_mt * num_nt;
+    const int units = num_mt * num_nt * splits;
 
     if (tid == 0) {
         for (int i = 0; i < RB; ++i) { tc::mbar_init(&sm.fullB[i], 1); tc::mbar_init(&sm.emptyB[i], kConvWarps); }
@@ -261,9 +271,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             Ring rb, rd, rf;
             uint32_t issB = 0, issD = 0, issF = 0;        // bit i: stage i has a copy in flight
             uint32_t phB = 0, phD = 0, phF = 0;           // bit i: parity of that copy
-            for (int t = blockIdx.x; t < tiles && !waborted(sm); t += gridDim.x) {
-                const int m0 = (t % num_mt) * BM, n0 = (t / num_mt) * BN;
-                for (int sb = 0; sb < S && !waborted(sm); ++sb) {
+            for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
+                const Work wk = work_of(u, splits, num_mt, S);
+                const int m0 = wk.m0, n0 = wk.n0;
+                for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
                     // activation d and s of this super-block
                     if (lane == 0 && wait_or_abort(sm, &sm.emptyD[rd.i], rd.ph ^ 1u)) {
                         tc::mbar_arrive_expect_tx(&sm.fullD[rd.i], 2 * kDRaw);
@@ -310,8 +321,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint32_t idesc = tc::instr_desc(BM, BN, 0);
             const uint32_t idesc32 = tc::instr_desc(BM, BN, 2);
             bool issued = false;
-            for (int t = blockIdx.x; t < tiles && !waborted(sm); t += gridDim.x) {
-                for (int sb = 0; sb < S && !waborted(sm); ++sb) {
+            for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
+                const Work wk = work_of(u, splits, num_mt, S);
+                for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
                     for (int j = 0; j < 8; ++j) {
                         if (!wwait(sm, &sm.fullF[rf.i], rf.ph)) break;
                         if (!wwait(sm, &sm.tempty[rt.i], rt.ph ^ 1u)) break;
@@ -372,16 +384,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int rbase = 8 * (warp - 4) + (lane & 7); // rows rbase + 64k: a quarter-warp covers 8 consecutive rows
         Ring rb, rf, rm, rs;
         if constexpr (Q6) {   // the first super-block of the first tile
-            if (blockIdx.x < tiles) q6_fetch(sm.braw[0], W, (blockIdx.x / num_mt) * BN, 0, N, wstride, wtotal, rbase, c);
+            if (blockIdx.x < units) {
+                const Work w0 = work_of(blockIdx.x, splits, num_mt, S);
+                q6_fetch(sm.braw[0], W, w0.n0, w0.sb0, N, wstride, wtotal, rbase, c);
+            }
         }
-        for (int tt = blockIdx.x; tt < tiles && !waborted(sm); tt += gridDim.x) {
-            const int n0 = (tt / num_mt) * BN;
-            for (int sb = 0; sb < S && !waborted(sm); ++sb) {
+        for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
+            const Work wk = work_of(u, splits, num_mt, S);
+            const int n0 = wk.n0;
+            for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
                 if constexpr (Q6) {
                     // prefetch the next super-block into the other stage, then wait for this one
-                    const int nsb = (sb + 1 < S) ? sb + 1 : 0;
-                    const int ntt = (sb + 1 < S) ? tt : tt + (int)gridDim.x;
-                    if (ntt < tiles) q6_fetch(sm.braw[rb.i ^ 1], W, (ntt / num_mt) * BN, nsb, N, wstride, wtotal, rbase, c);
+                    const int nu = (sb + 1 < wk.sb1) ? u : u + (int)gridDim.x;
+                    if (nu < units) {
+                        const Work nw = (nu == u) ? wk : work_of(nu, splits, num_mt, S);
+                        q6_fetch(sm.braw[rb.i ^ 1], W, nw.n0, (nu == u) ? sb + 1 : nw.sb0, N, wstride, wtotal, rbase, c);
+                    }
                     else tc::cp_async_commit();
                     tc::cp_async_wait<1>();
                     __syncwarp();
@@ -542,10 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int rloc = 32 * q + lane;
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         Ring rd, rt, rs, rm;
-        for (int tt = blockIdx.x; tt < tiles && !waborted(sm); tt += gridDim.x) {
-            const int m0 = (tt % num_mt) * BM, n0 = (tt / num_mt) * BN;
+        for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
+            const Work wk = work_of(u, splits, num_mt, S);
+            const int m0 = wk.m0, n0 = wk.n0;
             const int m = m0 + rloc;
-            for (int sb = 0; sb < S && !waborted(sm); ++sb) {
+            for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
                 if (!wwait(sm, &sm.fullD[rd.i], rd.ph)) break;
                 float da[8];
                 {
@@ -620,12 +639,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     ms_slot = kSlotCol0 + 128u * rt.i;
                 }
                 if (!wwait(sm, &sm.fullS[rs.i], rs.ph)) break;
-                const bool last = (sb == S - 1);
+                const bool first = (sb == wk.sb0), last = (sb == wk.sb1 - 1);
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     const int col = 64 * cq + 16 * h;
                     uint32_t o[16], mv[16];
-                    if (sb > 0) tc::tmem_ld16(tbase + lane_bits + kOutCol + col, o);
+                    if (!first) tc::tmem_ld16(tbase + lane_bits + kOutCol + col, o);
                     if constexpr (!Q6) tc::tmem_ld16(tbase + lane_bits + ms_slot + col, mv);
                     tc::tmem_ld_wait();
                     const float4* wdp = reinterpret_cast<const float4*>(&sm.wd[rs.i][col]);
@@ -644,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             const int cc = 4 * u + e;                 // 0..15 within the chunk
                             const int ai = 8 * h + (cc >> 1);         // float2 index in acc
                             const float av = (cc & 1) ? acc[ai].y : acc[ai].x;
-                            float v = (sb > 0) ? __uint_as_float(o[cc]) : 0.0f;
+                            float v = first ? 0.0f : __uint_as_float(o[cc]);
                             v = fmaf(w4[e], av, v);
                             if constexpr (!Q6) v = fmaf(-m4v[e], __uint_as_float(mv[cc]), v);
                             o[cc] = __float_as_uint(v);               // the result overwrites the loaded value
@@ -653,15 +672,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (last) {
                         if (m < M) {
                             float* orow = out + (size_t)m * N + n0 + col;
+                            // split-K: partial sums are added into the zeroed output
                             if (n0 + col + 16 <= N && (N & 3) == 0) {
 #pragma unroll
-                                for (int u = 0; u < 4; ++u)
-                                    reinterpret_cast<float4*>(orow)[u] =
-                                        make_float4(__uint_as_float(o[4 * u]), __uint_as_float(o[4 * u + 1]),
-                                                    __uint_as_float(o[4 * u + 2]), __uint_as_float(o[4 * u + 3]));
+                                for (int x = 0; x < 4; ++x) {
+                                    const float4 v4 = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
+                                                                  __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]));
+                                    if (splits > 1) atomicAdd(reinterpret_cast<float4*>(orow) + x, v4);
+                                    else reinterpret_cast<float4*>(orow)[x] = v4;
+                                }
                             } else {
-                                for (int u = 0; u < 16; ++u)
-                                    if (n0 + col + u < N) orow[u] = __uint_as_float(o[u]);
+                                for (int x = 0; x < 16; ++x) {
+                                    if (n0 + col + x < N) {
+                                        if (splits > 1) atomicAdd(orow + x, __uint_as_float(o[x]));
+                                        else orow[x] = __uint_as_float(o[x]);
+                                    }
+                                }
                             }
                         }
                     } else {
@@ -717,6 +743,24 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Split-K when there are too few tiles to fill the SMs: each tile's super-blocks are
+// divided among `splits` work units (at least 2 super-blocks each), chosen to
+// minimise the number of unit waves per split plus a small per-split cost.
+int choose_splits(long long tiles, int S, int sms) {
+    if (tiles >= sms) return 1;
+    int best = 1;
+    double best_cost = 1e30;
+    for (int s = 1; s <= 32 && 2 * s <= S; ++s) {
+        const long long waves = (tiles * s + sms - 1) / sms;
+        const double cost = (double)waves / s + 0.01 * s;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
 int check_gemm(const mq_q8_plane* a, const void* w, int N, const float* out) {
     if (!a) return MQ_ERR_NULL;
     if (N < 0 || a->M < 0 || !mq::valid_k(a->K)) return MQ_ERR_SHAPE;
@@ -759,9 +803,14 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
         !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_INT32, a->s, (uint64_t)K / 32, (uint64_t)M, (uint64_t)K / 8, 8, BM))
         return MQ_ERR_LAUNCH;
     const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int grid = (int)(tiles < mq::num_sms() ? tiles : mq::num_sms());
+    const int sms = mq::num_sms();
+    const int splits = choose_splits(tiles, K / mq::QK_K, sms);
+    if (splits > 1 && cudaMemsetAsync(out, 0, (size_t)M * N * sizeof(float), stream) != cudaSuccess)
+        return MQ_ERR_LAUNCH;
+    const long long units = tiles * splits;
+    const int grid = (int)(units < sms ? units : sms);
     gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmA, tmD, tmS, tmW, static_cast<const uint8_t*>(w), out, M, N, K,
-                                                      row, row * (unsigned long long)N);
+                                                      splits, row, row * (unsigned long long)N);
     return mq::launch_status();
 }
 
