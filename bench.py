@@ -316,16 +316,17 @@ def load_peaks():
     return 1700.0, 1900.0, 6800.0, "fallback"
 
 
-def dist_setup():
+def dist_setup(backend: str = "nccl"):
+    """Read RANK / LOCAL_RANK / WORLD_SIZE; for more than one rank join the process group
+    (NCCL on the GPU box; the multi-process tests pass "gloo" and stay on the CPU)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if backend == "nccl":
+        torch.cuda.set_device(local if ws > 1 else 0)
     if ws > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
+        dist.init_process_group(backend)
     return ws, rank, local
 
 
@@ -335,13 +336,20 @@ def barrier(ws):
         dist.barrier()
 
 
-def max_over_ranks(v, ws):
+def max_over_ranks(v, ws, device="cuda"):
+    """The largest of every rank's v (each rank times its own replica; the job takes the slowest)."""
     if ws == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tok_s(ws, t_ms):
+    """Whole-job throughput of ws replicas of the prefill step, each M_TOK tokens, that took at
+    most t_ms per step (weak scaling: the work per GPU is fixed)."""
+    return ws * M_TOK / (t_ms * 1e-3)
 
 
 def run_reference(args):
@@ -593,7 +601,7 @@ def main():
     achieved = q4_f / q4_t / 1e12
     if rank == 0:
         line = {
-            "metric": METRIC, "value": ws * M_TOK / (t_ms * 1e-3), "unit": "tok/s", "n_gpus": ws,
+            "metric": METRIC, "value": job_tok_s(ws, t_ms), "unit": "tok/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "int8 activations x 4/6-bit weights, exact on the f16 tensor pipe, f32 accumulate",
@@ -606,7 +614,7 @@ def main():
                        "parallelism": f"replicas x{ws}"},
             "effective_tops": ws * Stack.prefill_flops() / (t_ms * 1e-3) / 1e12,
             "decode": dec,
-            "e2e": {"value": ws * M_TOK / (e2e_ms * 1e-3), "unit": "tok/s",
+            "e2e": {"value": job_tok_s(ws, e2e_ms), "unit": "tok/s",
                     "h2d_bytes_per_step": host_x.numel() * 4 + host_attn.numel() * 4,
                     "d2h_bytes_per_step": VOCAB * 4},
             "roofline": {"kernel": "gemm q4_K 3314x18944x3584 (gate and up launches of the timed steps)",
