@@ -129,9 +129,20 @@ __device__ __forceinline__ uint32_t tile_off(int r, int kg) {
     return (uint32_t)((r >> 3) * kSBO + kg * kLBO + (r & 7) * 16);
 }
 
+// Non-suspending test of a phase (acquire semantics, like the waits). A phase that
+// has already completed is seen sooner this way than by a suspending try_wait.
+__device__ __forceinline__ bool mbar_ready(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(ok)
+                 : "r"(tc::smem_u32(bar)), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
 template <bool Q6>
 __device__ __forceinline__ bool wait_or_abort(Smem<Q6>& sm, uint64_t* bar, uint32_t parity) {
-    if (tc::mbar_wait(bar, parity, kWaitLimitNs)) return true;
+    if (mbar_ready(bar, parity) || tc::mbar_wait(bar, parity, kWaitLimitNs)) return true;
     atomicOr(&g_gemm_error, 1u);
     *(volatile int*)&sm.abort = 1;
     return false;
@@ -146,7 +157,7 @@ __device__ __forceinline__ bool aborted(Smem<Q6>& sm) {
 // so that the warp never diverges in front of a warp-collective operation.
 template <bool Q6>
 __device__ __forceinline__ bool wwait(Smem<Q6>& sm, uint64_t* bar, uint32_t parity) {
-    const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(bar, parity, kWaitLimitNs));
+    const bool ok = __all_sync(0xffffffffu, mbar_ready(bar, parity) || tc::mbar_wait(bar, parity, kWaitLimitNs));
     if (!ok) {
         if ((threadIdx.x & 31) == 0) atomicOr(&g_gemm_error, 1u);
         *(volatile int*)&sm.abort = 1;
