@@ -15,8 +15,10 @@
 // lane's scales are known once.
 //
 // q6_K: one warp per row; a lane task is 32 weights (16 positions of two
-// quarters), 8 lanes per super-block, 4 super-blocks per step, kSteps steps of
-// loads in flight.
+// quarters), 8 lanes per super-block, 4 super-blocks per step. The row is staged
+// through shared memory by cp.async copies of its 16-byte-aligned window, two
+// 8-super-block chunks in flight, so that the global loads are few, wide and
+// coalesced although the rows are only 2-byte aligned.
 //
 // The activation plane (a few KB) stays in L1/L2 and is shared by every warp.
 //
@@ -30,12 +32,12 @@
 // (q6_K), plus 4 B per output.
 
 #include "mq_internal.cuh"
+#include "tc.cuh"
 
 namespace {
 
 constexpr int kThreads = 256;        // 8 rows per block
 constexpr int kRowsPerBlock = kThreads / 32;
-constexpr int kSteps = 4;            // q6_K: steps (4 super-blocks each) with loads in flight
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -150,67 +152,112 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __res
     }
 }
 
-// q6_K rows are only 2-byte aligned (210 B super-blocks), so a lane fetches the
-// 16 bytes it needs as five aligned words and realigns them with funnel shifts.
-// The words never leave the super-block.
-__device__ __forceinline__ void load16_realign(const uint8_t* p, uint32_t out[4]) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~(uintptr_t)3);
-    const uint32_t sh = (uint32_t)(a & 3) * 8;
-    uint32_t v[5];
-#pragma unroll
-    for (int i = 0; i < 5; ++i) v[i] = __ldcs(w + i);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) out[i] = __funnelshift_r(v[i], v[i + 1], sh);
-}
-
 // Bytes of 6-bit quants q (0..63) -> bytes of q - 32 as int8: q + 96 never
 // carries out of a byte, and flipping bit 7 then subtracts 128.
 __device__ __forceinline__ int q6_minus32(uint32_t lo4, uint32_t hi2) {
     return (int)(((lo4 | (hi2 << 4)) + 0x60606060u) ^ 0x80808080u);
 }
 
+// q6_K rows are only 2-byte aligned (210 B super-blocks). Each warp streams its
+// row through a ring of kQ6Stages shared-memory buffers, kQ6Chunk super-blocks a
+// buffer: the 16-byte-aligned window around a chunk arrives by 16-byte cp.async
+// copies (coalesced, no registers held while in flight), and lanes realign their
+// bytes from shared memory (five aligned words and four funnel shifts per 16 B).
+constexpr int kQ6Chunk = 8;                       // super-blocks per buffer
+constexpr int kQ6Stages = 3;                      // buffers per warp (two chunks in flight)
+constexpr int kQ6ChunkBytes = 1696;               // 16-aligned window of 8 x 210 B at an even offset
+static_assert(kQ6ChunkBytes % 16 == 0 && kQ6ChunkBytes >= ((14 + kQ6Chunk * mq::Q6K_BYTES + 15) / 16) * 16,
+              "q6_K chunk buffer");
+
+__device__ __forceinline__ void lds16_realign(uint32_t a, uint32_t out[4]) {
+    const uint32_t w = a & ~3u, sh = (a & 3u) * 8;
+    uint32_t v[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) v[i] = tc::lds_u32(w + 4 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) out[i] = __funnelshift_r(v[i], v[i + 1], sh);
+}
+
+// Copies chunk c of a row (super-blocks 8c .. 8c+7) into buffer dst; the last
+// 16-byte piece of the matrix is read only up to its end.
+__device__ __forceinline__ void q6_issue_chunk(uint32_t dst, const uint8_t* wr, const uint8_t* wend, int c, int S,
+                                               int lane) {
+    const int n = min(kQ6Chunk, S - c * kQ6Chunk);
+    const uint8_t* a = wr + (size_t)c * kQ6Chunk * mq::Q6K_BYTES;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(a) & ~(uintptr_t)15;
+    const uintptr_t hi = (reinterpret_cast<uintptr_t>(a) + (uintptr_t)n * mq::Q6K_BYTES + 15) & ~(uintptr_t)15;
+    const int pieces = (int)((hi - lo) >> 4);
+    for (int i = lane; i < pieces; i += 32) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(lo) + 16 * i;
+        const ptrdiff_t left = wend - src;
+        tc::cp_async16_zfill(dst + 16 * i, src, left < 16 ? (uint32_t)left : 16u);
+    }
+}
+
+// Lane = 8*g + t. Step k of a chunk takes super-blocks 2g + k (k = 0, 1): the
+// four super-blocks of a step then start at word offsets that differ mod 4, so
+// the lanes' shared-memory words fall in distinct banks. Within a super-block,
+// t = 4*hh + 2*qq + h: half hh, quarters qq (low nibbles) and qq + 2 (high
+// nibbles), positions 16h .. 16h + 15 — two 16-element sub-blocks.
 __global__ void __launch_bounds__(kThreads) gemv_q6k_kernel(const uint8_t* __restrict__ W,
                                                             const int8_t* __restrict__ aq,
                                                             const float* __restrict__ ad,
                                                             float* __restrict__ out, int N, int K) {
+    __shared__ __align__(16) uint8_t stage[kRowsPerBlock][kQ6Stages][kQ6ChunkBytes];
     mq_grid_release();
-    const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int row = blockIdx.x * kRowsPerBlock + wid;
     if (row >= N) return;   // warp-uniform
     const int S = K / mq::QK_K;
+    const int nc = (S + kQ6Chunk - 1) / kQ6Chunk;
     const uint8_t* wr = W + (size_t)row * S * mq::Q6K_BYTES;
-    bool waited = false;   // weights of the first step are loaded before waiting for the plane's producer
-    const int t = lane & 7;
+    const uint8_t* wend = W + (size_t)N * S * mq::Q6K_BYTES;
+    const uint32_t buf0 = tc::smem_u32(&stage[wid][0][0]);
+    // Weights do not depend on the previous kernel: the first chunks are requested
+    // before waiting for the plane's producer.
+#pragma unroll
+    for (int c = 0; c < kQ6Stages - 1; ++c) {
+        if (c < nc) q6_issue_chunk(buf0 + c * kQ6ChunkBytes, wr, wend, c, S, lane);
+        tc::cp_async_commit();
+    }
+    mq_grid_wait();
+    const int g = lane >> 3, t = lane & 7;
     const int hh = t >> 2;          // half of the super-block (128 elements)
     const int qq = (t >> 1) & 1;    // quarter pair: quarters qq (low nibbles) and qq+2 (high nibbles)
     const int h = t & 1;            // which 16 of the 32 positions
     const int g0 = 8 * hh + 2 * qq + h, g1 = g0 + 4;       // 16-element sub-blocks (scale index)
     const int blk0 = 4 * hh + qq, blk1 = blk0 + 2;          // 32-element activation blocks in the super-block
+    const uint32_t off_ql = 64 * hh + 32 * qq + 16 * h, off_qh = 128 + 32 * hh + 16 * h;
+    const int s0 = 2 * qq, s1 = 2 * qq + 4;                 // qh bit position of quarters qq and qq+2
+    const uint32_t m4 = 0x0F0F0F0Fu, m2 = 0x03030303u;
     float acc = 0.0f;
-    for (int base = 0; base < S; base += 4 * kSteps) {
+    for (int c = 0; c < nc; ++c) {
+        if (c + kQ6Stages - 1 < nc)
+            q6_issue_chunk(buf0 + ((c + kQ6Stages - 1) % kQ6Stages) * kQ6ChunkBytes, wr, wend, c + kQ6Stages - 1, S,
+                           lane);
+        tc::cp_async_commit();
+        tc::cp_async_wait<kQ6Stages - 1>();   // this lane's copies of chunk c have landed
+        __syncwarp();                          // and every other lane's
+        const uint32_t base = buf0 + (c % kQ6Stages) * kQ6ChunkBytes +
+                              (uint32_t)(reinterpret_cast<uintptr_t>(wr + (size_t)c * kQ6Chunk * mq::Q6K_BYTES) & 15);
+        const int n = min(kQ6Chunk, S - c * kQ6Chunk);
 #pragma unroll
-        for (int u = 0; u < kSteps; ++u) {
-            const int sb = base + 4 * u + (lane >> 3);
-            if (sb < S) {
-                const uint8_t* blk = wr + (size_t)sb * mq::Q6K_BYTES;
+        for (int k = 0; k < 2; ++k) {
+            const int j = 2 * g + k;
+            if (j < n) {
+                const uint32_t blk = base + j * mq::Q6K_BYTES;
                 uint32_t ql[4], qh[4];
-                load16_realign(blk + 64 * hh + 32 * qq + 16 * h, ql);
-                load16_realign(blk + 128 + 32 * hh + 16 * h, qh);
-                const int sc0 = (int)(int8_t)__ldg(blk + 192 + g0);
-                const int sc1 = (int)(int8_t)__ldg(blk + 192 + g1);
-                const float d = mq_f16_to_f32(__ldg(reinterpret_cast<const unsigned short*>(blk + 208)));
+                lds16_realign(blk + off_ql, ql);
+                lds16_realign(blk + off_qh, qh);
+                const int sc0 = tc::lds_s8(blk + 192 + g0);
+                const int sc1 = tc::lds_s8(blk + 192 + g1);
+                const float d = mq_f16_to_f32((uint16_t)tc::lds_u16(blk + 208));
+                const int sb = c * kQ6Chunk + j;
                 const int b0 = sb * 8 + blk0, b1 = sb * 8 + blk1;
-                if (!waited) {
-                    mq_grid_wait();
-                    waited = true;
-                }
                 const int4 a0 = __ldg(reinterpret_cast<const int4*>(aq + b0 * 32 + 16 * h));
                 const int4 a1 = __ldg(reinterpret_cast<const int4*>(aq + b1 * 32 + 16 * h));
                 const int a0w[4] = {a0.x, a0.y, a0.z, a0.w};
                 const int a1w[4] = {a1.x, a1.y, a1.z, a1.w};
-                const uint32_t m4 = 0x0F0F0F0Fu, m2 = 0x03030303u;
-                const int s0 = 2 * qq, s1 = 2 * qq + 4;   // qh bit position of quarters qq and qq+2
                 int I0 = 0, I1 = 0;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -220,6 +267,7 @@ __global__ void __launch_bounds__(kThreads) gemv_q6k_kernel(const uint8_t* __res
                 acc += d * (__ldg(ad + b0) * (float)(sc0 * I0) + __ldg(ad + b1) * (float)(sc1 * I1));
             }
         }
+        __syncwarp();   // buffer c % kQ6Stages is read by every lane before it is refilled
     }
     acc = warp_sum(acc);
     if (lane == 0) out[row] = acc;

@@ -102,65 +102,110 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __
     }
 }
 
-// RMSNorm scale of one row, computed by one full warp in the fixed order:
-// lane l serially adds float4 l, l+32, ... (each as ((x0*x0 + x1*x1) + x2*x2) +
-// x3*x3, every op separately rounded), then an xor butterfly 16, 8, 4, 2, 1.
-// ("55 · r52", §3.2 phase 1; "72 · D3-7", §2c(i) and Excerpt C.)
-__device__ __forceinline__ float rms_scale_warp(const float4* __restrict__ xr, int K, float eps, int lane) {
-    const int K4 = K >> 2;
-    float ss = 0.0f;
-#pragma unroll 8
-    for (int i = lane; i < K4; i += 32) {
-        const float4 v = __ldg(xr + i);
-        float t = __fadd_rn(__fmul_rn(v.x, v.x), __fmul_rn(v.y, v.y));
-        t = __fadd_rn(t, __fmul_rn(v.z, v.z));
-        t = __fadd_rn(t, __fmul_rn(v.w, v.w));
-        ss = __fadd_rn(ss, t);
-    }
+// RMSNorm scale of one row in the fixed order: lane l serially adds float4 l,
+// l+32, ... (each as ((x0*x0 + x1*x1) + x2*x2) + x3*x3, every op separately
+// rounded), then an xor butterfly 16, 8, 4, 2, 1; scale = 1 / sqrt(ss/K + eps)
+// ("55 · r52", §3.2 phase 1; "72 · D3-7", §2c(i) and Excerpt C).
+__device__ __forceinline__ float sum_sq4(float4 v) {
+    float t = __fadd_rn(__fmul_rn(v.x, v.x), __fmul_rn(v.y, v.y));
+    t = __fadd_rn(t, __fmul_rn(v.z, v.z));
+    return __fadd_rn(t, __fmul_rn(v.w, v.w));
+}
+
+__device__ __forceinline__ float rms_scale_finish(float ss, int K, float eps) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
     return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
 }
 
-__device__ __forceinline__ void rms_quant_rounds(const float4* __restrict__ xr, const float4* __restrict__ w4,
-                                                 uint32_t* __restrict__ qs, float* __restrict__ d,
-                                                 int32_t* __restrict__ s, uint2* __restrict__ qh,
-                                                 long long row_round0, int k0, int kstep, int nrounds, float scale,
-                                                 int lane) {
-#pragma unroll 4
-    for (int k = k0; k < nrounds; k += kstep) {
-        const float4 xv = __ldg(xr + k * 32 + lane);
-        const float4 wv = __ldg(w4 + k * 32 + lane);
-        float dd;
-        int ss;
-        uint2 h;
-        const uint32_t q = mq_quant4_group8(__fmul_rn(__fmul_rn(xv.x, scale), wv.x),
-                                            __fmul_rn(__fmul_rn(xv.y, scale), wv.y),
-                                            __fmul_rn(__fmul_rn(xv.z, scale), wv.z),
-                                            __fmul_rn(__fmul_rn(xv.w, scale), wv.w), dd, ss, h);
-        store_round(qs, d, s, qh, row_round0 + k, lane, q, dd, ss, h);
+__device__ __forceinline__ float rms_scale_warp(const float4* __restrict__ xr, int K, float eps, int lane) {
+    const int K4 = K >> 2;
+    float ss = 0.0f;
+#pragma unroll 8
+    for (int i = lane; i < K4; i += 32) ss = __fadd_rn(ss, sum_sq4(__ldg(xr + i)));
+    return rms_scale_finish(ss, K, eps);
+}
+
+__device__ __forceinline__ void rms_quant_one(float4 xv, float4 wv, float scale, uint32_t* __restrict__ qs,
+                                              float* __restrict__ d, int32_t* __restrict__ s,
+                                              uint2* __restrict__ qh, long long round, int lane) {
+    float dd;
+    int ss;
+    uint2 h;
+    const uint32_t q = mq_quant4_group8(__fmul_rn(__fmul_rn(xv.x, scale), wv.x), __fmul_rn(__fmul_rn(xv.y, scale), wv.y),
+                                        __fmul_rn(__fmul_rn(xv.z, scale), wv.z), __fmul_rn(__fmul_rn(xv.w, scale), wv.w),
+                                        dd, ss, h);
+    store_round(qs, d, s, qh, round, lane, q, dd, ss, h);
+}
+
+// Rows of at most 32 * kRegRounds rounds (K <= 16384): one block per row, round
+// r held in registers by warp r % nw, all of a row's loads in flight at once.
+// Each lane leaves the sum of squares of its float4 of each round in shared
+// memory; warp 0 adds them per lane in round order — the same sequence as
+// rms_scale_warp — and the scale goes through shared memory. The row is read
+// from HBM once ("72 · D3-7", Excerpt C: a wide block per decode row).
+constexpr int kRegRounds = 4;
+
+__global__ void __launch_bounds__(1024) rms_quant_staged_kernel(const float4* __restrict__ x,
+                                                                const float4* __restrict__ w4,
+                                                                uint32_t* __restrict__ qs,
+                                                                float* __restrict__ d,
+                                                                int32_t* __restrict__ s,
+                                                                uint2* __restrict__ qh, int K, float eps) {
+    mq_grid_release();
+    mq_grid_wait();
+    extern __shared__ float s_sq[];   // [rounds][32]
+    __shared__ float s_scale;
+    const int lane = threadIdx.x & 31;
+    const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int nrounds = K >> 7;
+    const float4* xr = x + (long long)blockIdx.x * (K >> 2);
+    float4 xv[kRegRounds];
+#pragma unroll
+    for (int i = 0; i < kRegRounds; ++i) {
+        const int r = wid + i * nw;
+        if (r < nrounds) xv[i] = __ldcs(xr + r * 32 + lane);
+    }
+#pragma unroll
+    for (int i = 0; i < kRegRounds; ++i) {
+        const int r = wid + i * nw;
+        if (r < nrounds) s_sq[r * 32 + lane] = sum_sq4(xv[i]);
+    }
+    __syncthreads();
+    if (wid == 0) {
+        float ss = 0.0f;
+#pragma unroll 8
+        for (int r = 0; r < nrounds; ++r) ss = __fadd_rn(ss, s_sq[r * 32 + lane]);
+        const float sc = rms_scale_finish(ss, K, eps);
+        if (lane == 0) s_scale = sc;
+    }
+    __syncthreads();
+    const float scale = s_scale;
+    const long long round0 = (long long)blockIdx.x * nrounds;
+#pragma unroll
+    for (int i = 0; i < kRegRounds; ++i) {
+        const int r = wid + i * nw;
+        if (r < nrounds) rms_quant_one(xv[i], __ldg(w4 + r * 32 + lane), scale, qs, d, s, qh, round0 + r, lane);
     }
 }
 
-// One block per row with one warp per 128-float round (at most 32 warps, or 4
-// when there are many rows; more rounds wrap around). Every warp loads its first round while
-// warp 0 computes the scale in the same order as above; the scale goes through
-// shared memory ("72 · D3-7", §2c(i), Excerpt C: a wide block per decode row).
+// Longer rows: one block per row with one warp per round (at most 32 warps, or 4
+// when there are many rows; more rounds wrap around). Every warp loads its first
+// round while warp 0 computes the scale with rms_scale_warp (the row is read
+// twice, the second time mostly from cache).
 __global__ void __launch_bounds__(1024) rms_quant_wide_kernel(const float4* __restrict__ x,
                                                               const float4* __restrict__ w4,
                                                               uint32_t* __restrict__ qs,
                                                               float* __restrict__ d,
                                                               int32_t* __restrict__ s,
-                                                              uint2* __restrict__ qh, int M, int K,
-                                                              float eps) {
+                                                              uint2* __restrict__ qh, int K, float eps) {
     mq_grid_release();
     mq_grid_wait();
     __shared__ float s_scale;
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int row = blockIdx.x;
     const int nrounds = K >> 7;
-    const float4* xr = x + (long long)row * (K >> 2);
+    const float4* xr = x + (long long)blockIdx.x * (K >> 2);
     const float4 x0 = __ldg(xr + wid * 32 + lane);   // wid < nrounds by construction of the launch
     const float4 w0 = __ldg(w4 + wid * 32 + lane);
     if (wid == 0) {
@@ -169,17 +214,11 @@ __global__ void __launch_bounds__(1024) rms_quant_wide_kernel(const float4* __re
     }
     __syncthreads();
     const float scale = s_scale;
-    const long long round0 = (long long)row * nrounds;
-    {
-        float dd;
-        int ss;
-        uint2 h;
-        const uint32_t q = mq_quant4_group8(__fmul_rn(__fmul_rn(x0.x, scale), w0.x), __fmul_rn(__fmul_rn(x0.y, scale), w0.y),
-                                            __fmul_rn(__fmul_rn(x0.z, scale), w0.z), __fmul_rn(__fmul_rn(x0.w, scale), w0.w),
-                                            dd, ss, h);
-        store_round(qs, d, s, qh, round0 + wid, lane, q, dd, ss, h);
-    }
-    if (wid + nw < nrounds) rms_quant_rounds(xr, w4, qs, d, s, qh, round0, wid + nw, nw, nrounds, scale, lane);
+    const long long round0 = (long long)blockIdx.x * nrounds;
+    rms_quant_one(x0, w0, scale, qs, d, s, qh, round0 + wid, lane);
+#pragma unroll 4
+    for (int k = wid + nw; k < nrounds; k += nw)
+        rms_quant_one(__ldg(xr + k * 32 + lane), __ldg(w4 + k * 32 + lane), scale, qs, d, s, qh, round0 + k, lane);
 }
 
 int flat_grid(long long rounds) {
@@ -230,12 +269,18 @@ extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float 
     const float4* w4 = reinterpret_cast<const float4*>(w);
     uint32_t* qs = reinterpret_cast<uint32_t*>(out->qs);
     uint2* qh = reinterpret_cast<uint2*>(out->qh);
-    // One block per row. Its first warp computes the scale in the pinned order while every
-    // warp loads its first round; the quantize rounds are spread over the block's warps: up
-    // to 32 for a few rows (decode), 4 once there are enough rows to fill the machine.
+    // One block per row. Rows of up to 128 rounds are read once into registers: one warp
+    // per round for a few rows (decode), four rounds a warp once there are enough rows to
+    // fill the machine. Longer rows take the kernel that reads them twice.
     const int rounds = K / 128;
-    const int cap = (M >= 4 * mq::num_sms()) ? 4 : 32;
+    const bool many = M >= 4 * mq::num_sms();
+    if (rounds <= 32 * kRegRounds) {
+        const int warps = many ? (rounds + kRegRounds - 1) / kRegRounds : (rounds < 32 ? rounds : 32);
+        return mq::launch_pdl(rms_quant_staged_kernel, dim3(M), dim3(32 * warps), (size_t)rounds * 32 * sizeof(float),
+                              stream, x4, w4, qs, out->d, out->s, qh, K, eps);
+    }
+    const int cap = many ? 4 : 32;
     const int warps = rounds < cap ? rounds : cap;
     return mq::launch_pdl(rms_quant_wide_kernel, dim3(M), dim3(32 * warps), 0, stream, x4, w4, qs, out->d, out->s, qh,
-                          M, K, eps);
+                          K, eps);
 }
