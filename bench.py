@@ -10,7 +10,8 @@ them from HBM). value = tokens/s = 3314 / step time.
 
 Also measured in the same run (separately timed):
   * decode: the 14B-shaped 48-layer M = 1 sweep (rms->q8, attn_q/k/v/o,
-    gate/up GEMVs, SwiGLU->q8, down GEMV), GB/s of algorithmic bytes;
+    gate/up GEMVs, SwiGLU->q8, down GEMV; k|v and gate|up stored stacked and
+    run as one GEMV each), GB/s of algorithmic bytes;
   * e2e: the same prefill step with its inputs copied from pinned host memory
     and the logits copied back inside the timed region;
   * roofline: the q4_K GEMM launches (the dominant kernel), timed with CUDA
@@ -50,6 +51,9 @@ PREFILL_MATS = [("q", "q4k", HID, HID, "rms"), ("k", "q4k", KVD, HID, "rms"), ("
 DECODE_MATS = [("q", "q4k", D_HID, D_HID), ("k", "q6k", D_KV, D_HID), ("v", "q6k", D_KV, D_HID),
                ("o", "q4k", D_HID, D_HID), ("gate", "q4k", D_FFN, D_HID), ("up", "q4k", D_FFN, D_HID),
                ("down", "q6k", D_HID, D_FFN)]
+# Decode storage: projections that read the same plane and share a quant type are stored as one
+# stacked matrix and run as one GEMV (k|v, gate|up); the rows, bytes and products are the same.
+DECODE_STACKS = [("q", ("q",)), ("kv", ("k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")), ("down", ("down",))]
 BYTES_PER_SB = {"q4k": 144, "q6k": 210}
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gemm_kernel<q4_K> launch at
@@ -181,16 +185,22 @@ class Stack:
             self.dg = S.normal((1, D_FFN), seed, "d.g", device=dev)
             self.du = S.normal((1, D_FFN), seed, "d.u", device=dev)
             self.drms = [S.normal((D_HID,), seed, f"D{l}.rms", 1.0, 0.1, device=dev) for l in range(D_LAYERS)]
-            self.DW = [{n: S.weights(kind, N, K, seed, f"D{l}.{n}", device=dev) for n, kind, N, K in DECODE_MATS}
-                       for l in range(D_LAYERS)]
-            self.dout = {n: torch.empty((N,), **f32) for n, _, N, _ in DECODE_MATS}
+            mats = {n: (kind, N, K) for n, kind, N, K in DECODE_MATS}
+            self.dstack = {}
+            for name, parts in DECODE_STACKS:
+                kinds, Ks = {mats[p][0] for p in parts}, {mats[p][2] for p in parts}
+                assert len(kinds) == 1 and len(Ks) == 1
+                self.dstack[name] = (kinds.pop(), sum(mats[p][1] for p in parts), Ks.pop())
+            self.DW = [{n: S.weights(kind, N, K, seed, f"D{l}.{n}", device=dev)
+                        for n, (kind, N, K) in self.dstack.items()} for l in range(D_LAYERS)]
+            self.dout = {n: torch.empty((N,), **f32) for n, (_, N, _) in self.dstack.items()}
             self.dp_h = mq.Plane.empty(1, D_HID, dev, f16=False)
             self.dp_a = mq.Plane.empty(1, D_HID, dev, f16=False)
             self.dp_f = mq.Plane.empty(1, D_FFN, dev, f16=False)
 
     # launches per prefill step: 28 * (2 rms + 1 quantize + 1 swiglu + 7 gemm) + rms + gemv
     LAUNCHES_PER_STEP = LAYERS * 11 + 2
-    LAUNCHES_PER_DECODE = D_LAYERS * 10
+    LAUNCHES_PER_DECODE = D_LAYERS * 8   # rms, q, k|v, quantize, o, gate|up, swiglu, down
 
     def step(self, time_q4=False):
         mq = self.mq
@@ -219,13 +229,11 @@ class Stack:
         for l in range(D_LAYERS):
             W = self.DW[l]
             mq.mq_rms_quant(self.dx, self.drms[l], EPS, self.dp_h)
-            for n in ("q", "k", "v"):
-                mq.gemv(dict((a, b) for a, b, _, _ in DECODE_MATS)[n], self.dp_h, W[n], self.dout[n].numel(),
-                        self.dout[n])
+            mq.mq_gemv_q4k(self.dp_h, W["q"], D_HID, self.dout["q"])
+            mq.mq_gemv_q6k(self.dp_h, W["kv"], 2 * D_KV, self.dout["kv"])
             mq.mq_quantize_q8(self.dattn, self.dp_a)
             mq.mq_gemv_q4k(self.dp_a, W["o"], D_HID, self.dout["o"])
-            mq.mq_gemv_q4k(self.dp_h, W["gate"], D_FFN, self.dout["gate"])
-            mq.mq_gemv_q4k(self.dp_h, W["up"], D_FFN, self.dout["up"])
+            mq.mq_gemv_q4k(self.dp_h, W["gate_up"], 2 * D_FFN, self.dout["gate_up"])
             mq.mq_swiglu_quant(self.dg, self.du, self.dp_f)
             mq.mq_gemv_q6k(self.dp_f, W["down"], D_HID, self.dout["down"])
 
@@ -573,7 +581,8 @@ def main():
         dec = {"workload": "14B-shaped decode sweep, 48 layers, M=1", "GBps": ws * Stack.decode_bytes() / dt / 1e9,
                "ms_per_token": dt * 1e3, "bytes_per_token": Stack.decode_bytes(),
                "hbm_frac": Stack.decode_bytes() / dt / 1e9 / load_peaks()[2],
-               "launches_per_token": Stack.LAUNCHES_PER_DECODE, "launch": "CUDA graph replay"}
+               "launches_per_token": Stack.LAUNCHES_PER_DECODE, "launch": "CUDA graph replay",
+               "stacked": "k|v and gate|up weights stored as one matrix each, one GEMV per pair"}
 
     # ---- end to end: inputs from pinned host memory, logits back to the host
     host_x = st.x.cpu().pin_memory()

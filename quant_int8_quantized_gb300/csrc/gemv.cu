@@ -152,94 +152,118 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __res
     }
 }
 
-// Bytes of 6-bit quants q (0..63) -> bytes of q - 32 as int8: q + 96 never
-// carries out of a byte, and flipping bit 7 then subtracts 128.
-__device__ __forceinline__ int q6_minus32(uint32_t lo4, uint32_t hi2) {
-    return (int)(((lo4 | (hi2 << 4)) + 0x60606060u) ^ 0x80808080u);
-}
-
 // q6_K rows are only 2-byte aligned (210 B super-blocks). Each warp streams its
 // row through a ring of kQ6Stages shared-memory buffers, kQ6Chunk super-blocks a
-// buffer: the 16-byte-aligned window around a chunk arrives by 16-byte cp.async
-// copies (coalesced, no registers held while in flight), and lanes realign their
-// bytes from shared memory (five aligned words and four funnel shifts per 16 B).
+// buffer (rows of up to three chunks get four buffers, so that all of a row is
+// requested at once; longer rows get three, which leaves room for more warps): the 16-byte-aligned window around a chunk arrives by 16-byte cp.async
+// copies (coalesced, no registers held while in flight). W is 16-byte aligned and
+// a chunk is 1680 = 105 * 16 bytes, so every chunk of a row starts at the same
+// offset mis (mod 16) inside its window.
+constexpr int kQ6Rows = 2;                        // rows (warps) per block: small blocks spread evenly over the SMs
 constexpr int kQ6Chunk = 8;                       // super-blocks per buffer
-constexpr int kQ6Stages = 3;                      // buffers per warp (two chunks in flight)
 constexpr int kQ6ChunkBytes = 1696;               // 16-aligned window of 8 x 210 B at an even offset
+constexpr int kQ6PieceIters = (kQ6ChunkBytes / 16 + 31) / 32;
 static_assert(kQ6ChunkBytes % 16 == 0 && kQ6ChunkBytes >= ((14 + kQ6Chunk * mq::Q6K_BYTES + 15) / 16) * 16,
               "q6_K chunk buffer");
+static_assert((kQ6Chunk * mq::Q6K_BYTES) % 16 == 0, "chunks keep the row's offset mod 16");
 
-__device__ __forceinline__ void lds16_realign(uint32_t a, uint32_t out[4]) {
-    const uint32_t w = a & ~3u, sh = (a & 3u) * 8;
+// 16 bytes at a shared address a = 2 (mod 4): five aligned words, halves recombined.
+__device__ __forceinline__ void lds16_off2(uint32_t a, uint32_t out[4]) {
     uint32_t v[5];
 #pragma unroll
-    for (int i = 0; i < 5; ++i) v[i] = tc::lds_u32(w + 4 * i);
+    for (int i = 0; i < 5; ++i) v[i] = tc::lds_u32(a - 2 + 4 * i);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) out[i] = __funnelshift_r(v[i], v[i + 1], sh);
+    for (int i = 0; i < 4; ++i) out[i] = __byte_perm(v[i], v[i + 1], 0x5432);
 }
 
-// Copies chunk c of a row (super-blocks 8c .. 8c+7) into buffer dst; the last
-// 16-byte piece of the matrix is read only up to its end.
-__device__ __forceinline__ void q6_issue_chunk(uint32_t dst, const uint8_t* wr, const uint8_t* wend, int c, int S,
-                                               int lane) {
-    const int n = min(kQ6Chunk, S - c * kQ6Chunk);
-    const uint8_t* a = wr + (size_t)c * kQ6Chunk * mq::Q6K_BYTES;
-    const uintptr_t lo = reinterpret_cast<uintptr_t>(a) & ~(uintptr_t)15;
-    const uintptr_t hi = (reinterpret_cast<uintptr_t>(a) + (uintptr_t)n * mq::Q6K_BYTES + 15) & ~(uintptr_t)15;
-    const int pieces = (int)((hi - lo) >> 4);
-    for (int i = lane; i < pieces; i += 32) {
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(lo) + 16 * i;
-        const ptrdiff_t left = wend - src;
-        tc::cp_async16_zfill(dst + 16 * i, src, left < 16 ? (uint32_t)left : 16u);
+// Requests `pieces` 16-byte pieces from lo into the buffer at dst. Only the
+// matrix's last chunk can end inside a piece; there the piece is read only up to
+// the matrix end and zero-filled.
+__device__ __forceinline__ void q6_issue_chunk(uint32_t dst, const uint8_t* lo, int pieces, bool last,
+                                               const uint8_t* wend, int lane) {
+#pragma unroll
+    for (int k = 0; k < kQ6PieceIters; ++k) {
+        const int i = lane + 32 * k;
+        if (i < pieces) {
+            const uint8_t* src = lo + 16 * i;
+            uint32_t bytes = 16;
+            if (last) {
+                const ptrdiff_t left = wend - src;
+                bytes = left < 16 ? (uint32_t)left : 16u;
+            }
+            tc::cp_async16_zfill(dst + 16 * i, src, bytes);
+        }
     }
 }
 
-// Lane = 8*g + t. Step k of a chunk takes super-blocks 2g + k (k = 0, 1): the
-// four super-blocks of a step then start at word offsets that differ mod 4, so
-// the lanes' shared-memory words fall in distinct banks. Within a super-block,
-// t = 4*hh + 2*qq + h: half hh, quarters qq (low nibbles) and qq + 2 (high
-// nibbles), positions 16h .. 16h + 15 — two 16-element sub-blocks.
-__global__ void __launch_bounds__(kThreads) gemv_q6k_kernel(const uint8_t* __restrict__ W,
-                                                            const int8_t* __restrict__ aq,
-                                                            const float* __restrict__ ad,
-                                                            float* __restrict__ out, int N, int K) {
-    __shared__ __align__(16) uint8_t stage[kRowsPerBlock][kQ6Stages][kQ6ChunkBytes];
+// Lane = 8*g + t. Step k of a chunk takes super-blocks j = 2g + k (k = 0, 1): the
+// four super-blocks of a step start at word offsets that differ mod 4 (their
+// shared-memory words fall in distinct banks) and share one alignment mod 4,
+// which alternates between the two steps. Within a super-block, t = 4*hh + 2*qq
+// + h: half hh, quarters qq (low nibbles of ql) and qq + 2 (high nibbles),
+// positions 16h .. 16h + 15 — two 16-element sub-blocks.
+//
+// Integer dot of sub-block quants q = lo + 16*hi (q - 32 is the weight) with
+// activation bytes a, from unsigned-by-signed dp4a on bytes masked in place:
+//   L = sum (lo << 4e) a  (e = 0 for low nibbles, 1 for high nibbles),
+//   H = sum (hi << 2p) a  (p = the quarter: its qh bit pair),
+//   S = sum a,
+//   sum (q - 32) a = (L >> 4e) + 16 * (H >> 2p) - 32 * S,
+// every shift exact because each sum is a multiple of the power of two.
+template <int kQ6Stages>
+__global__ void __launch_bounds__(32 * kQ6Rows) gemv_q6k_kernel(const uint8_t* __restrict__ W,
+                                                                const int8_t* __restrict__ aq,
+                                                                const float* __restrict__ ad,
+                                                                float* __restrict__ out, int N, int K) {
+    __shared__ __align__(16) uint8_t stage[kQ6Rows][kQ6Stages][kQ6ChunkBytes];
     mq_grid_release();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int row = blockIdx.x * kRowsPerBlock + wid;
+    const int row = blockIdx.x * kQ6Rows + wid;
     if (row >= N) return;   // warp-uniform
     const int S = K / mq::QK_K;
     const int nc = (S + kQ6Chunk - 1) / kQ6Chunk;
-    const uint8_t* wr = W + (size_t)row * S * mq::Q6K_BYTES;
+    const size_t row_off = (size_t)row * S * mq::Q6K_BYTES;
+    const uint32_t mis = (uint32_t)(row_off & 15);
+    const uint8_t* wlo = W + (row_off - mis);   // aligned window start of chunk 0
     const uint8_t* wend = W + (size_t)N * S * mq::Q6K_BYTES;
+    const bool last_row = row == N - 1;
     const uint32_t buf0 = tc::smem_u32(&stage[wid][0][0]);
+    auto pieces_of = [&](int c) {
+        const int n = min(kQ6Chunk, S - c * kQ6Chunk);
+        return (int)((mis + (uint32_t)n * mq::Q6K_BYTES + 15) >> 4);
+    };
     // Weights do not depend on the previous kernel: the first chunks are requested
     // before waiting for the plane's producer.
 #pragma unroll
     for (int c = 0; c < kQ6Stages - 1; ++c) {
-        if (c < nc) q6_issue_chunk(buf0 + c * kQ6ChunkBytes, wr, wend, c, S, lane);
+        if (c < nc)
+            q6_issue_chunk(buf0 + c * kQ6ChunkBytes, wlo + (size_t)c * kQ6Chunk * mq::Q6K_BYTES, pieces_of(c),
+                           last_row && c == nc - 1, wend, lane);
         tc::cp_async_commit();
     }
     mq_grid_wait();
     const int g = lane >> 3, t = lane & 7;
-    const int hh = t >> 2;          // half of the super-block (128 elements)
-    const int qq = (t >> 1) & 1;    // quarter pair: quarters qq (low nibbles) and qq+2 (high nibbles)
-    const int h = t & 1;            // which 16 of the 32 positions
+    const int hh = t >> 2, qq = (t >> 1) & 1, h = t & 1;
     const int g0 = 8 * hh + 2 * qq + h, g1 = g0 + 4;       // 16-element sub-blocks (scale index)
-    const int blk0 = 4 * hh + qq, blk1 = blk0 + 2;          // 32-element activation blocks in the super-block
+    const int blk0 = 4 * hh + qq;                           // 32-element activation block of quarter qq
     const uint32_t off_ql = 64 * hh + 32 * qq + 16 * h, off_qh = 128 + 32 * hh + 16 * h;
-    const int s0 = 2 * qq, s1 = 2 * qq + 4;                 // qh bit position of quarters qq and qq+2
-    const uint32_t m4 = 0x0F0F0F0Fu, m2 = 0x03030303u;
+    const uint32_t mh0 = 0x03030303u << (2 * qq), mh1 = 0x03030303u << (2 * qq + 4);
+    const int shl0 = 4 - 2 * qq, shr1 = 2 * qq;
+    const int8_t* aql = aq + blk0 * 32 + 16 * h;            // + 256 per super-block; quarter qq+2 at +64
+    const float* adl = ad + blk0;                           // + 8 per super-block; quarter qq+2 at +2
     float acc = 0.0f;
+    int stg = 0;
     for (int c = 0; c < nc; ++c) {
-        if (c + kQ6Stages - 1 < nc)
-            q6_issue_chunk(buf0 + ((c + kQ6Stages - 1) % kQ6Stages) * kQ6ChunkBytes, wr, wend, c + kQ6Stages - 1, S,
-                           lane);
+        const int cn = c + kQ6Stages - 1;
+        if (cn < nc) {
+            const int sn = stg == 0 ? kQ6Stages - 1 : stg - 1;   // (c + kQ6Stages - 1) mod kQ6Stages
+            q6_issue_chunk(buf0 + sn * kQ6ChunkBytes, wlo + (size_t)cn * kQ6Chunk * mq::Q6K_BYTES, pieces_of(cn),
+                           last_row && cn == nc - 1, wend, lane);
+        }
         tc::cp_async_commit();
         tc::cp_async_wait<kQ6Stages - 1>();   // this lane's copies of chunk c have landed
         __syncwarp();                          // and every other lane's
-        const uint32_t base = buf0 + (c % kQ6Stages) * kQ6ChunkBytes +
-                              (uint32_t)(reinterpret_cast<uintptr_t>(wr + (size_t)c * kQ6Chunk * mq::Q6K_BYTES) & 15);
+        const uint32_t base = buf0 + stg * kQ6ChunkBytes + mis;
         const int n = min(kQ6Chunk, S - c * kQ6Chunk);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -247,27 +271,41 @@ __global__ void __launch_bounds__(kThreads) gemv_q6k_kernel(const uint8_t* __res
             if (j < n) {
                 const uint32_t blk = base + j * mq::Q6K_BYTES;
                 uint32_t ql[4], qh[4];
-                lds16_realign(blk + off_ql, ql);
-                lds16_realign(blk + off_qh, qh);
+                if (((mis + 2 * k) & 3u) == 0) {   // warp-uniform
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        ql[i] = tc::lds_u32(blk + off_ql + 4 * i);
+                        qh[i] = tc::lds_u32(blk + off_qh + 4 * i);
+                    }
+                } else {
+                    lds16_off2(blk + off_ql, ql);
+                    lds16_off2(blk + off_qh, qh);
+                }
                 const int sc0 = tc::lds_s8(blk + 192 + g0);
                 const int sc1 = tc::lds_s8(blk + 192 + g1);
                 const float d = mq_f16_to_f32((uint16_t)tc::lds_u16(blk + 208));
                 const int sb = c * kQ6Chunk + j;
-                const int b0 = sb * 8 + blk0, b1 = sb * 8 + blk1;
-                const int4 a0 = __ldg(reinterpret_cast<const int4*>(aq + b0 * 32 + 16 * h));
-                const int4 a1 = __ldg(reinterpret_cast<const int4*>(aq + b1 * 32 + 16 * h));
+                const int4 a0 = __ldg(reinterpret_cast<const int4*>(aql + sb * 256));
+                const int4 a1 = __ldg(reinterpret_cast<const int4*>(aql + sb * 256 + 64));
                 const int a0w[4] = {a0.x, a0.y, a0.z, a0.w};
                 const int a1w[4] = {a1.x, a1.y, a1.z, a1.w};
-                int I0 = 0, I1 = 0;
+                int L0 = 0, L1 = 0, H0 = 0, H1 = 0, S0 = 0, S1 = 0;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    I0 = __dp4a(q6_minus32(ql[i] & m4, (qh[i] >> s0) & m2), a0w[i], I0);
-                    I1 = __dp4a(q6_minus32((ql[i] >> 4) & m4, (qh[i] >> s1) & m2), a1w[i], I1);
+                    L0 = dp4a_us(ql[i] & 0x0F0F0F0Fu, a0w[i], L0);
+                    L1 = dp4a_us(ql[i] & 0xF0F0F0F0u, a1w[i], L1);
+                    H0 = dp4a_us(qh[i] & mh0, a0w[i], H0);
+                    H1 = dp4a_us(qh[i] & mh1, a1w[i], H1);
+                    S0 = __dp4a(0x01010101, a0w[i], S0);
+                    S1 = __dp4a(0x01010101, a1w[i], S1);
                 }
-                acc += d * (__ldg(ad + b0) * (float)(sc0 * I0) + __ldg(ad + b1) * (float)(sc1 * I1));
+                const int I0 = L0 + (H0 << shl0) - (S0 << 5);
+                const int I1 = (L1 >> 4) + (H1 >> shr1) - (S1 << 5);
+                acc += d * (__ldg(adl + sb * 8) * (float)(sc0 * I0) + __ldg(adl + sb * 8 + 2) * (float)(sc1 * I1));
             }
         }
-        __syncwarp();   // buffer c % kQ6Stages is read by every lane before it is refilled
+        __syncwarp();   // buffer stg is read by every lane before it is refilled
+        stg = stg == kQ6Stages - 1 ? 0 : stg + 1;
     }
     acc = warp_sum(acc);
     if (lane == 0) out[row] = acc;
@@ -318,6 +356,8 @@ extern "C" int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* ou
 extern "C" int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     int rc = check_gemv(a, w, N, out);
     if (rc != MQ_OK || N == 0) return rc;
-    return mq::launch_pdl(gemv_q6k_kernel, dim3((N + kRowsPerBlock - 1) / kRowsPerBlock), dim3(kThreads), 0, stream,
+    const int chunks = (a->K / mq::QK_K + kQ6Chunk - 1) / kQ6Chunk;
+    return mq::launch_pdl(chunks <= 3 ? gemv_q6k_kernel<4> : gemv_q6k_kernel<3>, dim3((N + kQ6Rows - 1) / kQ6Rows),
+                          dim3(32 * kQ6Rows), 0, stream,
                           static_cast<const uint8_t*>(w), a->qs, a->d, out, N, a->K);
 }

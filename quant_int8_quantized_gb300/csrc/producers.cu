@@ -16,7 +16,7 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRoundsPerIter = 4;   // float4 loads in flight per lane
+constexpr int kRoundsPerIter = 4;   // float4 loads in flight per lane (inputs of a few rows: 1, more warps)
 
 __device__ __forceinline__ void store_round(uint32_t* __restrict__ qs, float* __restrict__ d,
                                             int32_t* __restrict__ s, uint2* __restrict__ qh, long long round,
@@ -32,6 +32,7 @@ __device__ __forceinline__ void store_round(uint32_t* __restrict__ qs, float* __
 
 // x is viewed as a flat array of M*K floats (rows are contiguous, K % 128 == 0),
 // so every round lies inside one row and the plane arrays are flat too.
+template <int R>
 __global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __restrict__ x,
                                                                uint32_t* __restrict__ qs,
                                                                float* __restrict__ d,
@@ -42,13 +43,13 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __r
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * kThreads) >> 5;
-    for (long long r0 = warp * kRoundsPerIter; r0 < rounds; r0 += nwarps * kRoundsPerIter) {
-        float4 v[kRoundsPerIter];
+    for (long long r0 = warp * R; r0 < rounds; r0 += nwarps * R) {
+        float4 v[R];
 #pragma unroll
-        for (int u = 0; u < kRoundsPerIter; ++u)
+        for (int u = 0; u < R; ++u)
             if (r0 + u < rounds) v[u] = __ldcs(x + (r0 + u) * 32 + lane);
 #pragma unroll
-        for (int u = 0; u < kRoundsPerIter; ++u) {
+        for (int u = 0; u < R; ++u) {
             if (r0 + u < rounds) {   // warp-uniform
                 float dd;
                 int ss;
@@ -67,6 +68,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fmul_rn(__fmul_rn(g, __frcp_rn(__fadd_rn(1.0f, expf(-g)))), u);
 }
 
+template <int R>
 __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __restrict__ g,
                                                                 const float4* __restrict__ u,
                                                                 uint32_t* __restrict__ qs,
@@ -78,17 +80,17 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __
     const int lane = threadIdx.x & 31;
     const long long warp = ((long long)blockIdx.x * kThreads + threadIdx.x) >> 5;
     const long long nwarps = ((long long)gridDim.x * kThreads) >> 5;
-    for (long long r0 = warp * kRoundsPerIter; r0 < rounds; r0 += nwarps * kRoundsPerIter) {
-        float4 gv[kRoundsPerIter], uv[kRoundsPerIter];
+    for (long long r0 = warp * R; r0 < rounds; r0 += nwarps * R) {
+        float4 gv[R], uv[R];
 #pragma unroll
-        for (int k = 0; k < kRoundsPerIter; ++k) {
+        for (int k = 0; k < R; ++k) {
             if (r0 + k < rounds) {
                 gv[k] = __ldcs(g + (r0 + k) * 32 + lane);
                 uv[k] = __ldcs(u + (r0 + k) * 32 + lane);
             }
         }
 #pragma unroll
-        for (int k = 0; k < kRoundsPerIter; ++k) {
+        for (int k = 0; k < R; ++k) {
             if (r0 + k < rounds) {
                 float dd;
                 int ss;
@@ -146,6 +148,7 @@ __device__ __forceinline__ void rms_quant_one(float4 xv, float4 wv, float scale,
 // from HBM once ("72 · D3-7", Excerpt C: a wide block per decode row).
 constexpr int kRegRounds = 4;
 
+template <bool kPrefetchW>
 __global__ void __launch_bounds__(1024) rms_quant_staged_kernel(const float4* __restrict__ x,
                                                                 const float4* __restrict__ w4,
                                                                 uint32_t* __restrict__ qs,
@@ -171,6 +174,14 @@ __global__ void __launch_bounds__(1024) rms_quant_staged_kernel(const float4* __
         const int r = wid + i * nw;
         if (r < nrounds) s_sq[r * 32 + lane] = sum_sq4(xv[i]);
     }
+    float4 wv[kRegRounds];   // for a few rows the weight row is fetched while warp 0 computes the scale
+    if constexpr (kPrefetchW) {
+#pragma unroll
+        for (int i = 0; i < kRegRounds; ++i) {
+            const int r = wid + i * nw;
+            if (r < nrounds) wv[i] = __ldg(w4 + r * 32 + lane);
+        }
+    }
     __syncthreads();
     if (wid == 0) {
         float ss = 0.0f;
@@ -185,7 +196,8 @@ __global__ void __launch_bounds__(1024) rms_quant_staged_kernel(const float4* __
 #pragma unroll
     for (int i = 0; i < kRegRounds; ++i) {
         const int r = wid + i * nw;
-        if (r < nrounds) rms_quant_one(xv[i], __ldg(w4 + r * 32 + lane), scale, qs, d, s, qh, round0 + r, lane);
+        if (r < nrounds)
+            rms_quant_one(xv[i], kPrefetchW ? wv[i] : __ldg(w4 + r * 32 + lane), scale, qs, d, s, qh, round0 + r, lane);
     }
 }
 
@@ -221,8 +233,13 @@ __global__ void __launch_bounds__(1024) rms_quant_wide_kernel(const float4* __re
         rms_quant_one(__ldg(xr + k * 32 + lane), __ldg(w4 + k * 32 + lane), scale, qs, d, s, qh, round0 + k, lane);
 }
 
-int flat_grid(long long rounds) {
-    const long long per_block = (kThreads / 32) * kRoundsPerIter;
+// Inputs that would not give every SM two blocks at four rounds a warp (decode
+// rows) are spread one round per warp: the rounds' latencies then overlap across
+// warps instead of queueing inside one.
+bool few_rounds(long long rounds) { return rounds < 2LL * mq::num_sms() * (kThreads / 32) * kRoundsPerIter; }
+
+int flat_grid(long long rounds, int rounds_per_iter) {
+    const long long per_block = (kThreads / 32) * rounds_per_iter;
     long long blocks = (rounds + per_block - 1) / per_block;
     const long long cap = (long long)mq::num_sms() * 8;
     if (blocks > cap) blocks = cap;
@@ -245,7 +262,9 @@ extern "C" int mq_quantize_q8(const float* x, int M, int K, const mq_q8_plane* o
     int rc = check_producer(x, x, M, K, out);
     if (rc != MQ_OK || M == 0) return rc;
     const long long rounds = (long long)M * K / 128;
-    return mq::launch_pdl(quantize_q8_kernel, dim3(flat_grid(rounds)), dim3(kThreads), 0, stream,
+    const bool few = few_rounds(rounds);
+    return mq::launch_pdl(few ? quantize_q8_kernel<1> : quantize_q8_kernel<kRoundsPerIter>,
+                          dim3(flat_grid(rounds, few ? 1 : kRoundsPerIter)), dim3(kThreads), 0, stream,
                           reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(out->qs), out->d, out->s,
                           reinterpret_cast<uint2*>(out->qh), rounds);
 }
@@ -255,7 +274,9 @@ extern "C" int mq_swiglu_quant(const float* g, const float* u, int M, int K, con
     int rc = check_producer(g, u, M, K, out);
     if (rc != MQ_OK || M == 0) return rc;
     const long long rounds = (long long)M * K / 128;
-    return mq::launch_pdl(swiglu_quant_kernel, dim3(flat_grid(rounds)), dim3(kThreads), 0, stream,
+    const bool few = few_rounds(rounds);
+    return mq::launch_pdl(few ? swiglu_quant_kernel<1> : swiglu_quant_kernel<kRoundsPerIter>,
+                          dim3(flat_grid(rounds, few ? 1 : kRoundsPerIter)), dim3(kThreads), 0, stream,
                           reinterpret_cast<const float4*>(g), reinterpret_cast<const float4*>(u),
                           reinterpret_cast<uint32_t*>(out->qs), out->d, out->s, reinterpret_cast<uint2*>(out->qh),
                           rounds);
@@ -276,8 +297,9 @@ extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float 
     const bool many = M >= 4 * mq::num_sms();
     if (rounds <= 32 * kRegRounds) {
         const int warps = many ? (rounds + kRegRounds - 1) / kRegRounds : (rounds < 32 ? rounds : 32);
-        return mq::launch_pdl(rms_quant_staged_kernel, dim3(M), dim3(32 * warps), (size_t)rounds * 32 * sizeof(float),
-                              stream, x4, w4, qs, out->d, out->s, qh, K, eps);
+        return mq::launch_pdl(many ? rms_quant_staged_kernel<false> : rms_quant_staged_kernel<true>, dim3(M),
+                              dim3(32 * warps), (size_t)rounds * 32 * sizeof(float), stream, x4, w4, qs, out->d, out->s,
+                              qh, K, eps);
     }
     const int cap = many ? 4 : 32;
     const int warps = rounds < cap ? rounds : cap;

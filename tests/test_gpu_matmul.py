@@ -104,6 +104,30 @@ def test_gemv_parity(kind, N, K):
     _check(out, p, w, kind, N, K)
 
 
+@pytest.mark.parametrize("N,K", [(33, 1280), (64, 2048), (9, 2304), (17, 8448)])
+def test_gemv_q6k_exact_integer_dots(N, K):
+    """Unit super-block scales, sub-block scales of +-1 and integer activations whose every
+    32-block holds a 127 (so d_a = 1 and q_a = x): every output is an exact integer below
+    2^24, so the GPU must equal the f64 oracle bit for bit. Quants cover 0..63 uniformly."""
+    rng = np.random.default_rng(K + N)
+    S = K // 256
+    blk = rng.integers(0, 256, size=(N, S, 210), dtype=np.uint8)
+    blk[:, :, 192:208] = rng.choice(np.array([-1, 1], np.int8), size=(N, S, 16)).view(np.uint8)
+    blk[:, :, 208:210] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+    w = torch.from_numpy(np.ascontiguousarray(blk.reshape(N, S * 210))).cuda()
+    xi = rng.integers(-127, 128, size=(1, K)).astype(np.float32)
+    xi[0, rng.integers(0, 32) :: 32] = 127.0
+    p = _plane_from(torch.from_numpy(xi))
+    assert np.all(p.d.cpu().numpy() == 1.0)
+    g = Guarded((1, N), torch.float32)
+    mq.gemv("q6k", p, w, N, g.t)
+    torch.cuda.synchronize()
+    g.check()
+    ref, _ = O.gemm_rows(p.qs.cpu().numpy(), p.d.cpu().numpy(), w.cpu().numpy(), "q6k", N, K)
+    assert np.all(np.abs(ref) < 2 ** 24)
+    assert np.array_equal(g.t.cpu().numpy().astype(np.float64), ref)
+
+
 @pytest.mark.parametrize("kind", ["q4k", "q6k"])
 def test_gemv_matches_gemm_at_one_row(kind):
     N, K = 384, 1536
