@@ -60,9 +60,9 @@ BYTES_PER_SB = {"q4k": 144, "q6k": 210}
 # 3314 x 18944 x 3584, from one ncu capture (summary under profiles/). It describes the device code
 # with these SHA-256 digests (gemm.cu up to its host-side section, and tc.cuh) and is reported as
 # null once either changes.
-GEMM_Q4K_TRAFFIC = {"bytes": 266917376,
-                    "sha256": {"gemm.cu": "19b9e87390a78a980b7667168b15cd6bd890a622d91865a1744ccd5e33492775",
-                               "tc.cuh": "6b1f7d550e0d4c7f2abe55bdf3a9d264e868795aecd0d505c3fc5e948d07bcbd"}}
+GEMM_Q4K_TRAFFIC = {"bytes": 66138624 + 200217344,
+                    "sha256": {"gemm.cu": "6ad7761e96a45ad50606d9aa33d85690e1d9f3e28fcc78d20dae7df646677392",
+                               "tc.cuh": "25feaa86f9ca28303a0195f1711d084df49768cda449362a899d426fc7305d29"}}
 HOST_SECTION = b"// ------------------------------------------------------------------ host side"
 
 
@@ -560,7 +560,7 @@ def main():
     q4_f = sum(f for _, _, f in st.q4_events)
     q4_launches = len(st.q4_events)
 
-    # ---- decode sweep: 480 small launches per token, replayed from a CUDA graph so that the
+    # ---- decode sweep: 384 small launches per token, replayed from a CUDA graph so that the
     #      host's per-launch cost does not stand in for the kernels' time
     dec = None
     if not args.no_decode:
