@@ -123,7 +123,14 @@ int mq_rms_quant(const float* x, const float* w, int M, int K, float eps,
 /*
  * mq_swiglu_quant — fused SwiGLU -> q8 plane that never writes the f32
  * product ([r52] §3.2, the mode-2 swiglu kernel). g, u: f32 [M][K].
- *     v = (g / (1 + expf(-g))) * u, then the mq_quantize_q8 block rule on v.
+ *     v = (g / (1 + exp(-g))) * u, then the mq_quantize_q8 block rule on v.
+ * The division is IEEE f32. exp is fixed bit for bit, since an f32 exp has no
+ * single correct result: Cody-Waite range reduction (n = rint(x log2 e),
+ * r = (x - n ln2_hi) - n ln2_lo, as two fused multiply-adds) and the degree-7
+ * Taylor series in Horner form (one fused multiply-add a step), each step one
+ * correctly rounded f32 operation, scaled exactly by 2^n; 0 below x = -86,
+ * +inf above x = 88; within 0.91 ulp of e^x. The plane is thus a function of g
+ * and u alone, like the other producers' planes.
  */
 int mq_swiglu_quant(const float* g, const float* u, int M, int K,
                     const mq_q8_plane* out, cudaStream_t stream);

@@ -28,8 +28,14 @@ Readings taken where the pages are silent (each also listed in the design doc):
       partials are combined by an xor butterfly at offsets 16, 8, 4, 2, 1.
   R9  scale = 1 / sqrt(ss / K + eps) with correctly rounded f32 sqrt and divide
       (the pages use rsqrtf, an approximation with no exact CPU counterpart).
-  R10 SwiGLU uses the platform's f32 exp; planes are compared within +-1 quant
-      level on at most 1e-4 of elements.
+  R10 SwiGLU's exp is pinned, since an f32 exp has no single correct result:
+      e^x by Cody-Waite range reduction (n = rint(x log2 e), r = (x - n ln2_hi)
+      - n ln2_lo with a 16-bit ln2_hi, two fused multiply-adds) and the degree-7
+      Taylor series in Horner form (one fused multiply-add a step, emulated
+      exactly by fma_f32), then the exact scaling by 2^n; 0 below x = -86 and
+      +inf above x = 88. With it the SwiGLU
+      plane is bit-exact like the others; v = (g / (1 + e^-g)) * u with an IEEE
+      f32 division, as the pages write it.
   R11 the GEMM/GEMV error bound is per output element:
       |gpu - oracle| <= 1e-3 * sum_k |a[m,k]| * |w[n,k]|, a the dequantized q8
       activation.
@@ -39,6 +45,8 @@ invariants, brute force). Parity unpinned: whether R1/R2 match the byte order
 of real GGUF files (no such file is available).
 """
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -204,12 +212,64 @@ def rms_quant(x: np.ndarray, w: np.ndarray, eps: float):
     return quantize_q8(rms_values(x, w, eps))
 
 
+def fma_f32(a, b, c) -> np.ndarray:
+    """a*b + c rounded once to f32 (IEEE fused multiply-add) for f32 a, b, c.
+
+    a*b is exact in f64 (two 24-bit significands). s = a*b + c is rounded to f64
+    and its error e = (a*b + c) - s recovered exactly (Knuth's TwoSum). Rounding s
+    to f32 is then the correct rounding of a*b + c, unless s lies exactly halfway
+    between two f32 values while e != 0 (a midpoint has at most 25 significant
+    bits, so no other midpoint can separate s from the exact value); there the
+    exact value lies on e's side of the midpoint. Results stay normal here.
+    """
+    f64 = np.float64
+    a64, b64, c64 = (np.asarray(v, np.float32).astype(f64) for v in (a, b, c))
+    p = a64 * b64
+    s = p + c64
+    bv = s - p
+    e = (p - (s - bv)) + (c64 - bv)
+    r = s.astype(np.float32)
+    other = np.nextafter(r, np.where(s > r.astype(f64), np.float32(np.inf), np.float32(-np.inf)))
+    mid = (r.astype(f64) + other.astype(f64)) * 0.5
+    tie = (s != r.astype(f64)) & (s == mid) & (e != 0)
+    fixed = np.where(e > 0, np.maximum(r, other), np.minimum(r, other))
+    return np.where(tie, fixed, r).astype(np.float32)
+
+
+def exp_f32(x: np.ndarray) -> np.ndarray:
+    """e^x in f32 (R10): Cody-Waite range reduction and the Taylor series.
+
+    n = rint(x * log2(e)) (product rounded to f32, then ties-to-even),
+    r = fma(-n, ln2_lo, fma(-n, ln2_hi, x)) with ln2_hi = 0.693145751953125 (16
+    significant bits) and ln2_lo = ln 2 - ln2_hi in f32,
+    p = 1 + r(1 + r(1/2! + r(1/3! + ... + r/7!))) in Horner form, one fused
+    multiply-add per step, each coefficient 1/k! rounded to f32, and
+    e^x = p * 2^n (exact: n is in [-124, 127] on [-86, 88], so the product stays
+    normal). Below -86, e^x < 2^-124 and 1 + e^x rounds to 1, so 0 is returned;
+    above 88, +inf.
+    """
+    f32 = np.float32
+    x = np.asarray(x, f32)
+    log2e = f32(1.0 / math.log(2.0))
+    ln2_hi = f32(0.693145751953125)
+    ln2_lo = f32(math.log(2.0) - 0.693145751953125)
+    coef = [f32(1.0 / math.factorial(k)) for k in range(8)]
+    xc = np.clip(x, f32(-86.0), f32(88.0))
+    n = np.rint(xc * log2e)
+    r = fma_f32(-n, ln2_lo, fma_f32(-n, ln2_hi, xc))
+    p = np.full_like(xc, coef[7])
+    for k in range(6, -1, -1):
+        p = fma_f32(p, r, coef[k])
+    e = (p * np.ldexp(f32(1.0), n.astype(np.int32))).astype(f32)
+    e = np.where(x < f32(-86.0), f32(0.0), e)
+    return np.where(x > f32(88.0), f32(np.inf), e).astype(f32)
+
+
 def swiglu_values(g: np.ndarray, u: np.ndarray) -> np.ndarray:
     """v = (g / (1 + exp(-g))) * u in f32 ([r52] §3.2 mode-2 swiglu kernel; R10)."""
     g = np.asarray(g, np.float32)
     u = np.asarray(u, np.float32)
-    with np.errstate(over="ignore"):
-        e = np.exp(-g)
+    e = exp_f32(-g)
     return ((g / (np.float32(1.0) + e)) * u).astype(np.float32)
 
 

@@ -65,16 +65,3 @@ def assert_plane_equal(got, ref, what=""):
     assert bad.size == 0, f"{what}: {len(bad)} qs mismatches, first at {bad[:5].tolist()}"
     assert np.array_equal(d.view(np.uint32), rd.view(np.uint32)), f"{what}: d differs"
     assert np.array_equal(s, rs), f"{what}: s differs"
-
-
-def assert_plane_close(got, ref, max_frac=1e-4, what=""):
-    """+-1 quant level on at most max_frac of elements; d within 2^-20 relative; s consistent."""
-    qs, d, s = got
-    rq, rd, rs = ref
-    diff = np.abs(qs.astype(np.int32) - rq.astype(np.int32))
-    assert diff.max(initial=0) <= 1, f"{what}: a quant differs by {diff.max()}"
-    frac = np.count_nonzero(diff) / max(1, diff.size)
-    assert frac <= max_frac, f"{what}: {frac:.2e} of quants differ"
-    rel = np.abs(d.astype(np.float64) - rd) / np.maximum(np.abs(rd.astype(np.float64)), 1e-38)
-    assert rel.max(initial=0) <= 2.0 ** -20, f"{what}: d differs by {rel.max():.3e} relative"
-    assert np.array_equal(s, qs.reshape(qs.shape[0], -1, 32).astype(np.int32).sum(-1)), f"{what}: s != sum q"

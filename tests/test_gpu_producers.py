@@ -12,7 +12,7 @@ import torch
 
 from oracle import mq_oracle as O
 from quant_int8_quantized_gb300 import mq, synth
-from tests._gpu_util import GuardedPlane, assert_plane_close, assert_plane_equal, require_gpu
+from tests._gpu_util import GuardedPlane, assert_plane_equal, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -122,7 +122,7 @@ def test_rms_quant_equals_quantize_of_oracle_rms_values():
 
 
 @pytest.mark.parametrize("M,K", SHAPES)
-def test_swiglu_quant_within_tolerance(M, K):
+def test_swiglu_quant_bit_exact(M, K):
     g = _x(M, K, f"g{M}x{K}") * 3
     u = _x(M, K, f"u{M}x{K}")
     g[0, :4] = torch.tensor([0.0, 40.0, -40.0, -100.0])
@@ -130,7 +130,7 @@ def test_swiglu_quant_within_tolerance(M, K):
     mq.mq_swiglu_quant(g.cuda(), u.cuda(), gp.plane)
     torch.cuda.synchronize()
     gp.check()
-    assert_plane_close(gp.numpy(), O.swiglu_quant(g.numpy(), u.numpy()), what=f"swiglu {M}x{K}")
+    assert_plane_equal(gp.numpy(), O.swiglu_quant(g.numpy(), u.numpy()), f"swiglu {M}x{K}")
 
 
 def test_producers_full_size_sampled_rows():
@@ -154,7 +154,7 @@ def test_producers_full_size_sampled_rows():
     xs, ws = x[idx].cpu().numpy(), w.cpu().numpy()
     assert_plane_equal(sub(p), O.rms_quant(xs, ws, 1e-6), "rms full")
     assert_plane_equal(sub(pq), O.quantize_q8(g[idx].cpu().numpy()), "quantize full")
-    assert_plane_close(sub(pf), O.swiglu_quant(g[idx].cpu().numpy(), u[idx].cpu().numpy()), what="swiglu full")
+    assert_plane_equal(sub(pf), O.swiglu_quant(g[idx].cpu().numpy(), u[idx].cpu().numpy()), "swiglu full")
     assert mq.mq_device_status() == mq.MQ_OK
 
 

@@ -10,7 +10,7 @@ element within 1e-3 * sum_k |a||w|.
 
 FFN chain (one 7B-shaped layer, M = 3314): RMSNorm->q8 plane (bit-exact on
 sampled rows), gate and up q4_K GEMMs, SwiGLU->q8 of the GPU's gate and up
-outputs (tolerance rule), down q6_K GEMM on that plane — each stage checked
+outputs (bit-exact), down q6_K GEMM on that plane — each stage checked
 against the oracle applied to the GPU's own input of that stage.
 """
 import numpy as np
@@ -19,7 +19,7 @@ import torch
 
 from oracle import mq_oracle as O
 from quant_int8_quantized_gb300 import mq, synth
-from tests._gpu_util import assert_plane_close, assert_plane_equal, require_gpu
+from tests._gpu_util import assert_plane_equal, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -108,7 +108,7 @@ def test_ffn_layer_chain():
     # stage 3: SwiGLU of the GPU's gate and up outputs
     ref = O.swiglu_quant(g[rt].cpu().numpy(), u[rt].cpu().numpy())
     got = (p_f.qs[rt].cpu().numpy(), p_f.d[rt].cpu().numpy(), p_f.s[rt].cpu().numpy())
-    assert_plane_close(got, ref, what="ffn swiglu plane")
+    assert_plane_equal(got, ref, "ffn swiglu plane")
     # stage 4: down on the GPU's SwiGLU plane
     cols_h = _sample(H, 256, 6, [H - 1])
     _check_sampled(y, p_f, Wd, "q6k", H, F, rows, cols_h)

@@ -8,6 +8,8 @@ import json
 import math
 import os
 
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
@@ -266,6 +268,57 @@ def test_rms_other_order_agrees_within_one_level():
     qs2, d2, _ = O.quantize_q8(v)
     assert np.max(np.abs(qs.astype(int) - qs2.astype(int))) <= 1
     assert np.max(np.abs(d - d2) / d) <= 2.0 ** -21
+
+
+def test_exp_f32_within_1_ulp_of_f64_exp():
+    """R10's exp against the f64 exp on a dense grid of its whole range: a dropped Taylor
+    term, a wrong reduction constant or a wrong 2^n scaling each cost far more than 1 ulp."""
+    x = np.linspace(-86.0, 88.0, 400_001).astype(np.float32)
+    e = O.exp_f32(x).astype(np.float64)
+    t = np.exp(x.astype(np.float64))
+    ulp = np.spacing(t.astype(np.float32)).astype(np.float64)
+    assert np.max(np.abs(e - t) / ulp) <= 1.0
+
+
+def _round_f32(t):
+    """Correct (ties-to-even) rounding of an exact rational to f32, by comparing the
+    three f32 values around float(t) exactly."""
+    c = np.float32(float(t))
+    cands = [np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))]
+    return min(cands, key=lambda v: (abs(Fraction(float(v)) - t), int(np.float32(v).view(np.uint32)) & 1))
+
+
+def test_fma_f32_is_correctly_rounded():
+    rng = np.random.default_rng(11)
+    n = 3000
+    a = (rng.standard_normal(n) * np.exp2(rng.integers(-20, 20, n))).astype(np.float32)
+    b = (rng.standard_normal(n) * np.exp2(rng.integers(-20, 20, n))).astype(np.float32)
+    c = (rng.standard_normal(n) * np.exp2(rng.integers(-40, 40, n))).astype(np.float32)
+    got = O.fma_f32(a, b, c)
+    for i in range(n):
+        exact = Fraction(float(a[i])) * Fraction(float(b[i])) + Fraction(float(c[i]))
+        assert got[i] == _round_f32(exact), (a[i], b[i], c[i])
+    # a*b = 1 + 2^-11 + 2^-24 sits on an f32 midpoint: alone it rounds to even; a tiny c
+    # that f64 loses must still push it up (a plain f64 sum then f32 rounding would not)
+    a1 = np.float32(1 + 2.0 ** -12)
+    assert O.fma_f32(a1, a1, np.float32(0.0)) == np.float32(1 + 2.0 ** -11)
+    assert O.fma_f32(a1, a1, np.float32(2.0 ** -60)) == np.float32(1 + 2.0 ** -11 + 2.0 ** -23)
+    assert np.float32(float(a1) * float(a1) + 2.0 ** -60) == np.float32(1 + 2.0 ** -11)
+
+
+def test_exp_f32_special_cases():
+    assert O.exp_f32(np.float32(0.0)) == np.float32(1.0)
+    # at x = f32(k ln 2) the reduction gives n = k and r ~ 0: e^x is 2^k times e^r
+    k = np.arange(-120, 127)
+    xf = (k * np.log(2.0)).astype(np.float32)
+    e = O.exp_f32(xf).astype(np.float64)
+    r = xf.astype(np.float64) - k * np.log(2.0)
+    assert np.all(np.abs(e / (np.exp2(k.astype(np.float64)) * np.exp(r)) - 1.0) < 2.0 ** -22)
+    assert np.all(O.exp_f32(np.array([-86.5, -1e30], np.float32)) == 0.0)
+    assert np.all(np.isinf(O.exp_f32(np.array([88.5, 1e30], np.float32))))
+    # the Taylor coefficients are 1/k! correctly rounded to f32: e^r on tiny r is 1 + r
+    r = np.float32(2.0 ** -20)
+    assert O.exp_f32(r) == np.float32(1.0) + r
 
 
 def test_swiglu_values_close_to_f64_definition():
