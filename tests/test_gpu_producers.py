@@ -107,6 +107,18 @@ def test_rms_quant_both_launch_shapes(M):
     assert_plane_equal(gp.numpy(), O.rms_quant(x.numpy(), w.numpy(), 1e-6), f"rms {M}x{K}")
 
 
+@pytest.mark.parametrize("M,K", [(700, 1280), (640, 4096), (609, 256), (1000, 3584)])
+def test_rms_quant_many_rows(M, K):
+    """Enough rows to fill the machine (four rounds a warp), ragged round counts."""
+    x = _x(M, K, f"rw{M}x{K}")
+    w = synth.normal((K,), 0, f"rww{K}", mean=1.0, std=0.1)
+    gp = GuardedPlane(M, K)
+    mq.mq_rms_quant(x.cuda(), w.cuda(), 1e-6, gp.plane)
+    torch.cuda.synchronize()
+    gp.check()
+    assert_plane_equal(gp.numpy(), O.rms_quant(x.numpy(), w.numpy(), 1e-6), f"rms {M}x{K}")
+
+
 def test_rms_quant_equals_quantize_of_oracle_rms_values():
     """Mode-2 identity: the fused plane equals the standalone quantize of the f32 RMSNorm output."""
     M, K = 64, 3584
