@@ -166,15 +166,16 @@ __device__ __forceinline__ void rms_quant_one(float4 xv, float4 wv, float scale,
     store_round(qs, d, s, qh, round, lane, q, dd, ss, h);
 }
 
-// Rows of at most 32 * kRegRounds rounds (K <= 16384): one block per row, round
-// r held in registers by warp r % nw, all of a row's loads in flight at once.
+// Rows of at most 32 * kRegRoundsMax rounds (K <= 16384): one block per row, round
+// r held in registers by warp r % nw (at most kRegRounds rounds a warp), all of
+// a row's loads in flight at once.
 // Each lane leaves the sum of squares of its float4 of each round in shared
 // memory; warp 0 adds them per lane in round order — the same sequence as
 // rms_scale_warp — and the scale goes through shared memory. The row is read
 // from HBM once ("72 · D3-7", Excerpt C: a wide block per decode row).
-constexpr int kRegRounds = 4;
+constexpr int kRegRoundsMax = 4;
 
-template <bool kPrefetchW>
+template <bool kPrefetchW, int kRegRounds>
 __global__ void __launch_bounds__(1024) rms_quant_staged_kernel(const float4* __restrict__ x,
                                                                 const float4* __restrict__ w4,
                                                                 uint32_t* __restrict__ qs,
@@ -317,15 +318,23 @@ extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float 
     uint32_t* qs = reinterpret_cast<uint32_t*>(out->qs);
     uint2* qh = reinterpret_cast<uint2*>(out->qh);
     // One block per row. Rows of up to 128 rounds are read once into registers: one warp
-    // per round for a few rows (decode), four rounds a warp once there are enough rows to
-    // fill the machine. Longer rows take the kernel that reads them twice.
+    // per round for a few rows (decode); two rounds a warp (four for rows over 64 rounds)
+    // once there are enough rows to fill the machine. Longer rows take the kernel that
+    // reads them twice.
     const int rounds = K / 128;
     const bool many = M >= 4 * mq::num_sms();
-    if (rounds <= 32 * kRegRounds) {
-        const int warps = many ? (rounds + kRegRounds - 1) / kRegRounds : (rounds < 32 ? rounds : 32);
-        return mq::launch_pdl(many ? rms_quant_staged_kernel<false> : rms_quant_staged_kernel<true>, dim3(M),
-                              dim3(32 * warps), (size_t)rounds * 32 * sizeof(float), stream, x4, w4, qs, out->d, out->s,
-                              qh, K, eps);
+    if (rounds <= 32 * kRegRoundsMax) {
+        const size_t smem = (size_t)rounds * 32 * sizeof(float);
+        if (!many)
+            return mq::launch_pdl(rms_quant_staged_kernel<true, kRegRoundsMax>, dim3(M),
+                                  dim3(32 * (rounds < 32 ? rounds : 32)), smem, stream, x4, w4, qs, out->d, out->s, qh,
+                                  K, eps);
+        if (rounds <= 64)   // two rounds a warp (measured faster than four at 3314 x 3584)
+            return mq::launch_pdl(rms_quant_staged_kernel<false, 2>, dim3(M), dim3(32 * ((rounds + 1) / 2)), smem,
+                                  stream, x4, w4, qs, out->d, out->s, qh, K, eps);
+        return mq::launch_pdl(rms_quant_staged_kernel<false, kRegRoundsMax>, dim3(M),
+                              dim3(32 * ((rounds + kRegRoundsMax - 1) / kRegRoundsMax)), smem, stream, x4, w4, qs, out->d,
+                              out->s, qh, K, eps);
     }
     const int cap = many ? 4 : 32;
     const int warps = rounds < cap ? rounds : cap;

@@ -107,9 +107,10 @@ def test_rms_quant_both_launch_shapes(M):
     assert_plane_equal(gp.numpy(), O.rms_quant(x.numpy(), w.numpy(), 1e-6), f"rms {M}x{K}")
 
 
-@pytest.mark.parametrize("M,K", [(700, 1280), (640, 4096), (609, 256), (1000, 3584)])
+@pytest.mark.parametrize("M,K", [(700, 1280), (640, 4096), (609, 256), (1000, 3584), (608, 10240), (610, 18944)])
 def test_rms_quant_many_rows(M, K):
-    """Enough rows to fill the machine (four rounds a warp), ragged round counts."""
+    """Enough rows to fill the machine: two rounds a warp, four for rows over 64 rounds, and
+    the twice-reading kernel for rows over 128 rounds; ragged round counts."""
     x = _x(M, K, f"rw{M}x{K}")
     w = synth.normal((K,), 0, f"rww{K}", mean=1.0, std=0.1)
     gp = GuardedPlane(M, K)
