@@ -14,7 +14,7 @@ Sources (engineering write-ups of the "minfer" inference engine):
   [r52]  "55 · r52 — skip-write mode 2: skipping the f32 intermediate write-out"
   [D3-7] "72 · D3-7 — attn_v-q6K MMVQ routing (2b) + rms wide-block / positions memo (2c)"
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
   R1  q4_K super-block byte order (the pages only name the type).
   R2  q6_K super-block byte order.
   R3  an all-zero activation block has d = 0, q = 0, s = 0.
