@@ -62,7 +62,7 @@ BYTES_PER_SB = {"q4k": 144, "q6k": 210}
 # null once either changes.
 GEMM_Q4K_TRAFFIC = {"bytes": 66138624 + 200217344,
                     "sha256": {"gemm.cu": "6ad7761e96a45ad50606d9aa33d85690e1d9f3e28fcc78d20dae7df646677392",
-                               "tc.cuh": "25feaa86f9ca28303a0195f1711d084df49768cda449362a899d426fc7305d29"}}
+                               "tc.cuh": "f0d689cbcc636b3cfce09941783428102221b5a2de96435c0e8a1236d316203f"}}
 HOST_SECTION = b"// ------------------------------------------------------------------ host side"
 
 

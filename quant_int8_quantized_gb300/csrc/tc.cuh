@@ -1,5 +1,6 @@
-// Thin inline-PTX wrappers for sm_100-family tensor-core (tcgen05), mbarrier and
-// bulk-copy (TMA) instructions used by the prefill GEMM.
+// Thin inline-PTX wrappers for sm_100-family tensor-core (tcgen05), mbarrier,
+// bulk-copy (TMA), cp.async and shared-memory load instructions, used by the
+// prefill GEMM and the decode GEMV.
 #pragma once
 
 #include <cstdint>
@@ -200,14 +201,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
         : "memory");
 }
 
-// 1-D bulk copy global -> shared; src, dst 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
 // Per-thread asynchronous 16-byte copy global -> shared (both 16-byte aligned).
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
@@ -264,11 +257,6 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
 __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
     asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
-__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
 
