@@ -115,14 +115,33 @@ struct Ring {
     }
 };
 
-// A work unit: one output tile and one slice [sb0, sb1) of its super-blocks. With
-// split-K, splits > 1 units share a tile and add their partial sums into it.
+// A work unit: one output tile and one slice [sb0, sb1) of its super-blocks. Tiles
+// are numbered m-fastest; units that share a tile add their partial sums into the
+// output, which the host zeroed beforehand.
+//   q4_K: every tile is split into `splits` slices (1 unless there are fewer tiles
+//         than SMs); unit u is slice u % splits of tile u / splits.
+//   q6_K: the first `whole` units are whole tiles (full waves over the CTAs); each
+//         tile of the last, partial wave is split into `splits` slices.
+// (The q4_K kernel keeps the plain mapping: the same hybrid there measured slower
+// through the code it makes, not through its schedule.)
 struct Work {
     int m0, n0, sb0, sb1;
 };
-__device__ __forceinline__ Work work_of(int u, int splits, int num_mt, int S) {
-    const int t = u / splits, sp = u - t * splits;
-    return Work{(t % num_mt) * BM, (t / num_mt) * BN, (sp * S) / splits, ((sp + 1) * S) / splits};
+template <bool Q6>
+__device__ __forceinline__ Work work_of(int u, int whole, int splits, int num_mt, int S) {
+    if constexpr (!Q6) {
+        const int t = u / splits, sp = u - t * splits;
+        return Work{(t % num_mt) * BM, (t / num_mt) * BN, (sp * S) / splits, ((sp + 1) * S) / splits};
+    } else {
+        int t = u, sp = 0, ns = 1;
+        if (u >= whole) {
+            const int v = u - whole;
+            t = whole + v / splits;
+            sp = v - (t - whole) * splits;
+            ns = splits;
+        }
+        return Work{(t % num_mt) * BM, (t / num_mt) * BN, (sp * S) / ns, ((sp + 1) * S) / ns};
+    }
 }
 
 __device__ __forceinline__ uint32_t tile_off(int r, int kg) {
@@ -247,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                                            const __grid_constant__ CUtensorMap tmS,
                                                            const __grid_constant__ CUtensorMap tmW,
                                                            const uint8_t* __restrict__ W, float* __restrict__ out,
-                                                           int M, int N, int K, int splits,
+                                                           int M, int N, int K, int whole, int splits,
                                                            unsigned long long wstride, unsigned long long wtotal) {
     using C = Cfg<Q6>;
     constexpr int RF = C::RF;
@@ -256,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = K / mq::QK_K;
     const int num_mt = (M + BM - 1) / BM, num_nt = (N + BN - 1) / BN;
-    const int units = num_mt * num_nt * splits;
+    const int units = Q6 ? whole + (num_mt * num_nt - whole) * splits : num_mt * num_nt * splits;
 
     if (tid == 0) {
         for (int i = 0; i < RB; ++i) { tc::mbar_init(&sm.fullB[i], 1); tc::mbar_init(&sm.emptyB[i], kConvWarps); }
@@ -283,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t issB = 0, issD = 0, issF = 0;        // bit i: stage i has a copy in flight
             uint32_t phB = 0, phD = 0, phF = 0;           // bit i: parity of that copy
             for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-                const Work wk = work_of(u, splits, num_mt, S);
+                const Work wk = work_of<Q6>(u, whole, splits, num_mt, S);
                 const int m0 = wk.m0, n0 = wk.n0;
                 for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
                     // activation d and s of this super-block
@@ -333,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint32_t idesc32 = tc::instr_desc(BM, BN, 2);
             bool issued = false;
             for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-                const Work wk = work_of(u, splits, num_mt, S);
+                const Work wk = work_of<Q6>(u, whole, splits, num_mt, S);
                 for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
                     for (int j = 0; j < 8; ++j) {
                         if (!wwait(sm, &sm.fullF[rf.i], rf.ph)) break;
@@ -396,19 +415,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         Ring rb, rf, rm, rs;
         if constexpr (Q6) {   // the first super-block of the first tile
             if (blockIdx.x < units) {
-                const Work w0 = work_of(blockIdx.x, splits, num_mt, S);
+                const Work w0 = work_of<Q6>(blockIdx.x, whole, splits, num_mt, S);
                 q6_fetch(sm.braw[0], W, w0.n0, w0.sb0, N, wstride, wtotal, rbase, c);
             }
         }
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of(u, splits, num_mt, S);
+            const Work wk = work_of<Q6>(u, whole, splits, num_mt, S);
             const int n0 = wk.n0;
             for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
                 if constexpr (Q6) {
                     // prefetch the next super-block into the other stage, then wait for this one
                     const int nu = (sb + 1 < wk.sb1) ? u : u + (int)gridDim.x;
                     if (nu < units) {
-                        const Work nw = (nu == u) ? wk : work_of(nu, splits, num_mt, S);
+                        const Work nw = (nu == u) ? wk : work_of<Q6>(nu, whole, splits, num_mt, S);
                         q6_fetch(sm.braw[rb.i ^ 1], W, nw.n0, (nu == u) ? sb + 1 : nw.sb0, N, wstride, wtotal, rbase, c);
                     }
                     else tc::cp_async_commit();
@@ -572,7 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         Ring rd, rt, rs, rm;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of(u, splits, num_mt, S);
+            const Work wk = work_of<Q6>(u, whole, splits, num_mt, S);
+            const bool add = Q6 ? (u >= whole && splits > 1) : (splits > 1);   // partial sums of a split tile
             const int m0 = wk.m0, n0 = wk.n0;
             const int m = m0 + rloc;
             for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
@@ -689,13 +709,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                 for (int x = 0; x < 4; ++x) {
                                     const float4 v4 = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
                                                                   __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]));
-                                    if (splits > 1) atomicAdd(reinterpret_cast<float4*>(orow) + x, v4);
+                                    if (add) atomicAdd(reinterpret_cast<float4*>(orow) + x, v4);
                                     else reinterpret_cast<float4*>(orow)[x] = v4;
                                 }
                             } else {
                                 for (int x = 0; x < 16; ++x) {
                                     if (n0 + col + x < N) {
-                                        if (splits > 1) atomicAdd(orow + x, __uint_as_float(o[x]));
+                                        if (add) atomicAdd(orow + x, __uint_as_float(o[x]));
                                         else orow[x] = __uint_as_float(o[x]);
                                     }
                                 }
@@ -754,9 +774,10 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Split-K when there are too few tiles to fill the SMs: each tile's super-blocks are
-// divided among `splits` work units (at least 2 super-blocks each), chosen to
-// minimise the number of unit waves per split plus a small per-split cost.
+// Split-K for the tiles of the last, partial wave (all tiles when there are fewer
+// than SMs): each such tile's super-blocks are divided among `splits` work units
+// (at least 2 super-blocks each), chosen to minimise the number of unit waves per
+// split plus a small per-split cost.
 int choose_splits(long long tiles, int S, int sms) {
     if (tiles >= sms) return 1;
     int best = 1;
@@ -813,15 +834,25 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
         !make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->d, (uint64_t)K / 32, (uint64_t)M, (uint64_t)K / 8, 8, BM) ||
         !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_INT32, a->s, (uint64_t)K / 32, (uint64_t)M, (uint64_t)K / 8, 8, BM))
         return MQ_ERR_LAUNCH;
-    const long long tiles = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const long long num_mt = (M + BM - 1) / BM, tiles = num_mt * ((N + BN - 1) / BN);
     const int sms = mq::num_sms();
-    const int splits = choose_splits(tiles, K / mq::QK_K, sms);
-    if (splits > 1 && cudaMemsetAsync(out, 0, (size_t)M * N * sizeof(float), stream) != cudaSuccess)
-        return MQ_ERR_LAUNCH;
-    const long long units = tiles * splits;
+    // q6_K: full waves of whole tiles, and the tiles of the last, partial wave split along
+    // K. q4_K: split only when there are fewer tiles than SMs (then every tile is).
+    const long long whole = Q6 ? (tiles / sms) * sms : 0;
+    const int splits = tiles > whole ? choose_splits(tiles - whole, K / mq::QK_K, sms) : 1;
+    if (splits > 1) {
+        // The split tiles are the last ones in m-fastest order: they lie in the tile columns
+        // from the one holding tile `whole` on. Zero those columns (whole tiles among them
+        // overwrite the zeros with plain stores).
+        const size_t col0 = (size_t)(whole / num_mt) * BN;
+        if (cudaMemset2DAsync(out + col0, (size_t)N * sizeof(float), 0, ((size_t)N - col0) * sizeof(float),
+                              (size_t)M, stream) != cudaSuccess)
+            return MQ_ERR_LAUNCH;
+    }
+    const long long units = whole + (tiles - whole) * splits;
     const int grid = (int)(units < sms ? units : sms);
     gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmA, tmD, tmS, tmW, static_cast<const uint8_t*>(w), out, M, N, K,
-                                                      splits, row, row * (unsigned long long)N);
+                                                      (int)whole, splits, row, row * (unsigned long long)N);
     return mq::launch_status();
 }
 
