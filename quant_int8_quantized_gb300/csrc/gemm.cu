@@ -63,7 +63,7 @@ constexpr int kEpiWarps = 8;            // 2 per TMEM lane quarter, 64 columns e
 constexpr int kThreads = 128 + 32 * kConvWarps + 32 * kEpiWarps;
 constexpr int kLaunchRegs = 96;         // 65536 / 640, rounded down to the allocation unit
 #ifndef MQ_REGS_OVERRIDE
-constexpr int kRegsWG0 = 48, kRegsConv = 72, kRegsEpi = 144;
+constexpr int kRegsWG0 = 48, kRegsConv = 64, kRegsEpi = 152;   // measured best of the splits that fit
 #else
 constexpr int kRegsWG0 = MQ_R0, kRegsConv = MQ_RC, kRegsEpi = MQ_RE;
 #endif
