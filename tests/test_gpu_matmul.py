@@ -74,6 +74,17 @@ def test_gemm_outlier_activations(kind):
     _check(out, p, w, kind, N, K)
 
 
+@pytest.mark.parametrize("kind", ["q4k", "q6k"])
+@pytest.mark.parametrize("M,N,K", [(1100, 2176, 2048), (300, 8320, 1280)])
+def test_gemm_partial_last_wave_every_element(kind, M, N, K):
+    """153 tiles (one full wave of 152 SMs + 1) and 195 tiles (+ 43): the q6_K kernel splits the
+    last wave's tiles along K into the zeroed tile columns, q4_K runs them whole. Every output
+    element is checked."""
+    x = synth.normal((M, K), 0, f"lw{M}x{K}")
+    out, p, w = _run(kind, x, N, K, mq.gemm)
+    _check(out, p, w, kind, N, K)
+
+
 @pytest.mark.parametrize("kind,N,K", [("q4k", 18944, 3584), ("q6k", 3584, 18944), ("q4k", 512, 3584)])
 def test_gemm_full_size_sampled_rows(kind, N, K):
     """7B prefill shapes at M = 3314, oracle on 24 sampled rows (rows are independent)."""
