@@ -148,7 +148,10 @@ int mq_swiglu_quant(const float* g, const float* u, int M, int K,
  * When the output has fewer 128 x 128 tiles than the GPU has SMs (small M or
  * N), the K axis is split across several thread blocks, `out` is zeroed on
  * `stream` and the partial sums are added with f32 atomics: the result is then
- * within the same bound, but its last bits may differ from run to run.
+ * within the same bound, but its last bits may differ from run to run. The
+ * q6_K GEMM does the same for the tiles of its last, partial wave when the
+ * tile count is not a multiple of the SM count: only the output columns
+ * holding those tiles are zeroed, and only those tiles' last bits may vary.
  */
 int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
