@@ -17,8 +17,9 @@
 // q6_K: one warp per row; a lane task is 32 weights (16 positions of two
 // quarters), 8 lanes per super-block, 4 super-blocks per step. The row is staged
 // through shared memory by cp.async copies of its 16-byte-aligned window, two
-// 8-super-block chunks in flight, so that the global loads are few, wide and
-// coalesced although the rows are only 2-byte aligned.
+// 8-super-block chunks in flight (three for rows of at most three chunks), so
+// that the global loads are few, wide and coalesced although the rows are only
+// 2-byte aligned. Two rows (warps) a block.
 //
 // The activation plane (a few KB) stays in L1/L2 and is shared by every warp.
 //
@@ -37,7 +38,7 @@
 namespace {
 
 constexpr int kThreads = 128;        // q4_K: 4 warps (row pairs) per block; measured faster than 256 and 512
-constexpr int kRowsPerBlock = kThreads / 32;
+constexpr int kRowsPerBlock = kThreads / 32;   // q4_K: warps (row pairs) per block
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
