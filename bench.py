@@ -11,7 +11,8 @@ them from HBM). value = tokens/s = 3314 / step time.
 Also measured in the same run (separately timed):
   * decode: the 14B-shaped 48-layer M = 1 sweep (rms->q8, attn_q/k/v/o,
     gate/up GEMVs, SwiGLU->q8, down GEMV; k|v and gate|up stored stacked and
-    run as one GEMV each), GB/s of algorithmic bytes;
+    run as one GEMV each; the k|v GEMV on a second stream beside attn_q, both
+    reading the rms plane), GB/s of algorithmic bytes;
   * e2e: the same prefill step with its inputs copied from pinned host memory
     and the logits copied back inside the timed region;
   * roofline: the q4_K GEMM launches (the dominant kernel), timed with CUDA
@@ -197,6 +198,11 @@ class Stack:
             self.dp_h = mq.Plane.empty(1, D_HID, dev, f16=False)
             self.dp_a = mq.Plane.empty(1, D_HID, dev, f16=False)
             self.dp_f = mq.Plane.empty(1, D_FFN, dev, f16=False)
+            # q and k|v only read the rms plane: k|v runs on a second stream, joined before the
+            # attention stand-in, so the two GEMVs overlap (inside the captured graph too)
+            self.side = torch.cuda.Stream(device=dev)
+            self.ev_h = torch.cuda.Event()
+            self.ev_kv = torch.cuda.Event()
 
     # launches per prefill step: 28 * (2 rms + 1 quantize + 1 swiglu + 7 gemm) + rms + gemv
     LAUNCHES_PER_STEP = LAYERS * 11 + 2
@@ -226,11 +232,16 @@ class Stack:
 
     def decode_step(self):
         mq = self.mq
+        main = torch.cuda.current_stream()
         for l in range(D_LAYERS):
             W = self.DW[l]
             mq.mq_rms_quant(self.dx, self.drms[l], EPS, self.dp_h)
+            self.ev_h.record(main)
+            self.side.wait_event(self.ev_h)
+            mq.mq_gemv_q6k(self.dp_h, W["kv"], 2 * D_KV, self.dout["kv"], stream=self.side)
+            self.ev_kv.record(self.side)
             mq.mq_gemv_q4k(self.dp_h, W["q"], D_HID, self.dout["q"])
-            mq.mq_gemv_q6k(self.dp_h, W["kv"], 2 * D_KV, self.dout["kv"])
+            main.wait_event(self.ev_kv)
             mq.mq_quantize_q8(self.dattn, self.dp_a)
             mq.mq_gemv_q4k(self.dp_a, W["o"], D_HID, self.dout["o"])
             mq.mq_gemv_q4k(self.dp_h, W["gate_up"], 2 * D_FFN, self.dout["gate_up"])
@@ -582,7 +593,8 @@ def main():
                "ms_per_token": dt * 1e3, "bytes_per_token": Stack.decode_bytes(),
                "hbm_frac": Stack.decode_bytes() / dt / 1e9 / load_peaks()[2],
                "launches_per_token": Stack.LAUNCHES_PER_DECODE, "launch": "CUDA graph replay",
-               "stacked": "k|v and gate|up weights stored as one matrix each, one GEMV per pair"}
+               "stacked": "k|v and gate|up weights stored as one matrix each, one GEMV per pair",
+               "streams": "the k|v GEMV runs on a second stream beside attn_q (both read only the rms plane)"}
 
     # ---- end to end: inputs from pinned host memory, logits back to the host
     host_x = st.x.cpu().pin_memory()
