@@ -161,15 +161,15 @@ int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
  * ([D3-7] §2 (2b) and Excerpt A/A2, the MMVQ decode path): the same result as
  * the GEMM with a->M == 1. out: f32 [N]. Returns MQ_ERR_SHAPE if a->M != 1.
  *
- * Launch overlap: these two, and the three producers above, are launched with
- * programmatic stream serialization, so each may start while the kernels
- * enqueued before it on `stream` are finishing. Every one waits for them to
- * complete before it reads the plane (or its producer inputs) and before it
- * writes anything, so chains of these calls keep stream order. The GEMVs read
- * their first weight rows before that wait: `w` must not be written by a kernel
- * enqueued earlier on the same stream unless an event wait or a synchronization
- * separates the two (weights written by cudaMemcpy* or before the stream work
- * began are always safe).
+ * Launch overlap: the three producers above are launched with programmatic
+ * stream serialization, so each may start while the kernel enqueued before it
+ * on `stream` is finishing. Each waits for that kernel to complete before it
+ * reads its inputs (with coherent loads) and before it writes anything, so
+ * chains of these calls keep stream order. The RMSNorm weight `w` is read
+ * through the read-only path: it must not be written by a kernel still running
+ * when mq_rms_quant's kernel starts (an event wait or a synchronization between
+ * the two suffices; weights written by cudaMemcpy* or before the stream work
+ * began are always safe). The GEMVs and GEMMs are ordinary launches.
  */
 int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);

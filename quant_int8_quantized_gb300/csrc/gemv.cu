@@ -23,11 +23,13 @@
 //
 // The activation plane (a few KB) stays in L1/L2 and is shared by every warp.
 //
-// Both are launched with programmatic stream serialization: a block lets the next
-// kernel be scheduled as soon as it starts, and loads its first weights before it
-// waits for the kernel that produced the activation plane, so the previous
-// kernel's tail overlaps this one's first DRAM round trip. Nothing is written and
-// no activation is read before that wait.
+// Both are ordinary launches: they start once the kernel that produced the
+// activation plane has completed, so the plane is read-only for their whole
+// lifetime and may be read through the non-coherent path (__ldg). (Launched
+// early with programmatic serialization, such loads returned a stale plane under
+// graph replay, and the coherent loads that fix that made these kernels slower
+// than the overlap gained.) A block lets the next kernel on the stream be
+// scheduled as soon as it starts, which the producers use.
 //
 // HBM roofline: the weight stream, 0.5625 B/weight (q4_K) or 0.8203 B/weight
 // (q6_K), plus 4 B per output.
@@ -82,7 +84,6 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __res
     const int lane = threadIdx.x & 31;
     const int S = K / mq::QK_K, nst = (S + 7) / 8;
     const int g = lane >> 2, p = lane & 3;
-    bool waited = false;   // weights of the first step are loaded before waiting for the plane's producer
     const bool hi = p >= 2;
     const uint32_t sh0 = 16u * (uint32_t)(p & 1), sh1 = sh0 + 8u;   // byte (2p mod 4), (2p+1 mod 4) of a word
     const size_t row_bytes = (size_t)S * mq::Q4K_BYTES;
@@ -99,10 +100,6 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __res
             const int sb = 8 * st + g;
             if (sb < S) {
                 load_q4k(cur, wr + (size_t)sb * mq::Q4K_BYTES, row_bytes, two, p);
-                if (!waited) {
-                    mq_grid_wait();
-                    waited = true;
-                }
                 const int b0 = sb * 8 + 2 * p;
                 const int4* a = reinterpret_cast<const int4*>(aq + b0 * 32);   // blocks b0, b0 + 1: 4 x 16 bytes
                 const int4 a0 = __ldg(a), a1 = __ldg(a + 1), a2 = __ldg(a + 2), a3 = __ldg(a + 3);
@@ -233,8 +230,6 @@ __global__ void __launch_bounds__(32 * kQ6Rows) gemv_q6k_kernel(const uint8_t* _
         const int n = min(kQ6Chunk, S - c * kQ6Chunk);
         return (int)((mis + (uint32_t)n * mq::Q6K_BYTES + 15) >> 4);
     };
-    // Weights do not depend on the previous kernel: the first chunks are requested
-    // before waiting for the plane's producer.
 #pragma unroll
     for (int c = 0; c < kQ6Stages - 1; ++c) {
         if (c < nc)
@@ -242,7 +237,6 @@ __global__ void __launch_bounds__(32 * kQ6Rows) gemv_q6k_kernel(const uint8_t* _
                            last_row && c == nc - 1, wend, lane);
         tc::cp_async_commit();
     }
-    mq_grid_wait();
     const int g = lane >> 3, t = lane & 7;
     const int hh = t >> 2, qq = (t >> 1) & 1, h = t & 1;
     const int g0 = 8 * hh + 2 * qq + h, g1 = g0 + 4;       // 16-element sub-blocks (scale index)
@@ -350,7 +344,7 @@ int take_gemv_device_error(cudaStream_t, unsigned* code) {
 extern "C" int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     int rc = check_gemv(a, w, N, out);
     if (rc != MQ_OK || N == 0) return rc;
-    return mq::launch_pdl(gemv_q4k_kernel, dim3(gemv_grid((N + 1) / 2, gemv_q4k_kernel)), dim3(kThreads), 0, stream,
+    return mq::launch_plain(gemv_q4k_kernel, dim3(gemv_grid((N + 1) / 2, gemv_q4k_kernel)), dim3(kThreads), 0, stream,
                           static_cast<const uint8_t*>(w), a->qs, a->d, a->s, out, N, a->K);
 }
 
@@ -358,7 +352,7 @@ extern "C" int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* ou
     int rc = check_gemv(a, w, N, out);
     if (rc != MQ_OK || N == 0) return rc;
     const int chunks = (a->K / mq::QK_K + kQ6Chunk - 1) / kQ6Chunk;
-    return mq::launch_pdl(chunks <= 3 ? gemv_q6k_kernel<4> : gemv_q6k_kernel<3>, dim3((N + kQ6Rows - 1) / kQ6Rows),
+    return mq::launch_plain(chunks <= 3 ? gemv_q6k_kernel<4> : gemv_q6k_kernel<3>, dim3((N + kQ6Rows - 1) / kQ6Rows),
                           dim3(32 * kQ6Rows), 0, stream,
                           static_cast<const uint8_t*>(w), a->qs, a->d, out, N, a->K);
 }

@@ -59,6 +59,18 @@ int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaS
     return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? MQ_OK : MQ_ERR_LAUNCH;
 }
 
+// Ordinary launch (no overlap with the previous kernel) through the same interface.
+template <typename... KArgs, typename... Args>
+int launch_plain(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? MQ_OK : MQ_ERR_LAUNCH;
+}
+
 // Device-side failure record (bounded waits) -----------------------------------
 // Each translation unit with bounded waits owns one word; these read and clear it.
 int take_gemm_device_error(cudaStream_t stream, unsigned* code);
@@ -74,6 +86,19 @@ __device__ __forceinline__ void mq_grid_wait() { asm volatile("griddepcontrol.wa
 // Let the next kernel on the stream be scheduled once every block of this one has
 // called this (or exited).
 __device__ __forceinline__ void mq_grid_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Loads of data that an earlier kernel on the stream writes (activation planes, producer
+// inputs), made after mq_grid_wait(). A kernel launched with launch_pdl may start while
+// that kernel is still running, so the data is not read-only for this kernel's lifetime
+// and must not be read through the non-coherent path (ld.global.nc, __ldg): a replayed
+// graph then read a stale plane. These are coherent loads that may be cached in L1.
+// Weights, which no kernel in flight writes, may use __ldg; so may a kernel launched
+// with launch_plain, which starts only after the previous kernel has completed.
+__device__ __forceinline__ int4 mq_ld_dep(const int4* p) { return __ldca(p); }
+__device__ __forceinline__ int2 mq_ld_dep(const int2* p) { return __ldca(p); }
+__device__ __forceinline__ float2 mq_ld_dep(const float2* p) { return __ldca(p); }
+__device__ __forceinline__ float4 mq_ld_dep(const float4* p) { return __ldca(p); }
+__device__ __forceinline__ float mq_ld_dep(const float* p) { return __ldca(p); }
 
 __device__ __forceinline__ float mq_f16_to_f32(uint16_t h) {
     float f;

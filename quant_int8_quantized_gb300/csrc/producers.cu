@@ -150,7 +150,7 @@ __device__ __forceinline__ float rms_scale_warp(const float4* __restrict__ xr, i
     const int K4 = K >> 2;
     float ss = 0.0f;
 #pragma unroll 8
-    for (int i = lane; i < K4; i += 32) ss = __fadd_rn(ss, sum_sq4(__ldg(xr + i)));
+    for (int i = lane; i < K4; i += 32) ss = __fadd_rn(ss, sum_sq4(mq_ld_dep(xr + i)));
     return rms_scale_finish(ss, K, eps);
 }
 
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(1024) rms_quant_wide_kernel(const float4* __re
     const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int nrounds = K >> 7;
     const float4* xr = x + (long long)blockIdx.x * (K >> 2);
-    const float4 x0 = __ldg(xr + wid * 32 + lane);   // wid < nrounds by construction of the launch
+    const float4 x0 = mq_ld_dep(xr + wid * 32 + lane);   // wid < nrounds by construction of the launch
     const float4 w0 = __ldg(w4 + wid * 32 + lane);
     if (wid == 0) {
         const float sc = rms_scale_warp(xr, K, eps, lane);
@@ -255,9 +255,9 @@ __global__ void __launch_bounds__(1024) rms_quant_wide_kernel(const float4* __re
     const float scale = s_scale;
     const long long round0 = (long long)blockIdx.x * nrounds;
     rms_quant_one(x0, w0, scale, qs, d, s, qh, round0 + wid, lane);
-#pragma unroll 4
+#pragma unroll 2
     for (int k = wid + nw; k < nrounds; k += nw)
-        rms_quant_one(__ldg(xr + k * 32 + lane), __ldg(w4 + k * 32 + lane), scale, qs, d, s, qh, round0 + k, lane);
+        rms_quant_one(mq_ld_dep(xr + k * 32 + lane), __ldg(w4 + k * 32 + lane), scale, qs, d, s, qh, round0 + k, lane);
 }
 
 // Inputs that would not give every SM two blocks at four rounds a warp (decode

@@ -102,3 +102,57 @@ def test_prefill_gemm_graph_replay_matches_eager():
         torch.cuda.synchronize()
         assert torch.equal(o4, e4) and torch.equal(o6, e6)
     assert mq.mq_device_status() == mq.MQ_OK
+
+
+def test_decode_layer_two_streams_matches_one_stream():
+    """The decode step's schedule: the k|v GEMV on a second stream beside attn_q, joined before
+    the next producer, captured into a graph. Replays equal one-stream eager execution bit for
+    bit, over two layers that reuse the planes."""
+    dev = torch.device("cuda")
+    H, F, KV = 1024, 2048, 256
+    x = synth.normal((1, H), 7, "s.x", device=dev)
+    attn = synth.normal((1, H), 7, "s.attn", device=dev)
+    w_rms = [synth.normal((H,), 7, f"s.rms{l}", 1.0, 0.1, device=dev) for l in range(2)]
+    Wq = [synth.weights("q4k", H, H, 7, f"s.wq{l}", device=dev) for l in range(2)]
+    Wkv = [synth.weights("q6k", 2 * KV, H, 7, f"s.wkv{l}", device=dev) for l in range(2)]
+    Wo = [synth.weights("q4k", H, H, 7, f"s.wo{l}", device=dev) for l in range(2)]
+    ph, pa = mq.Plane.empty(1, H, dev, f16=False), mq.Plane.empty(1, H, dev, f16=False)
+    oq = [torch.empty((H,), device=dev) for _ in range(2)]
+    okv = [torch.empty((2 * KV,), device=dev) for _ in range(2)]
+    oo = [torch.empty((H,), device=dev) for _ in range(2)]
+    side = torch.cuda.Stream()
+    ev_h, ev_kv = torch.cuda.Event(), torch.cuda.Event()
+
+    def layer_two_streams():
+        main = torch.cuda.current_stream()
+        for l in range(2):
+            mq.mq_rms_quant(x, w_rms[l], 1e-6, ph)
+            ev_h.record(main)
+            side.wait_event(ev_h)
+            mq.mq_gemv_q6k(ph, Wkv[l], 2 * KV, okv[l], stream=side)
+            ev_kv.record(side)
+            mq.mq_gemv_q4k(ph, Wq[l], H, oq[l])
+            main.wait_event(ev_kv)
+            mq.mq_quantize_q8(attn, pa)
+            mq.mq_gemv_q4k(pa, Wo[l], H, oo[l])
+
+    def layer_one_stream():
+        for l in range(2):
+            mq.mq_rms_quant(x, w_rms[l], 1e-6, ph)
+            mq.mq_gemv_q4k(ph, Wq[l], H, oq[l])
+            mq.mq_gemv_q6k(ph, Wkv[l], 2 * KV, okv[l])
+            mq.mq_quantize_q8(attn, pa)
+            mq.mq_gemv_q4k(pa, Wo[l], H, oo[l])
+
+    layer_one_stream()
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in oq + okv + oo]
+    graph = _capture(layer_two_streams)
+    for t in oq + okv + oo:
+        t.fill_(float("nan"))
+    for _ in range(3):
+        graph.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(ref, oq + okv + oo):
+            assert torch.equal(a, b)
+    assert mq.mq_device_status() == mq.MQ_OK
