@@ -17,8 +17,9 @@
  *    reduction axis, "id" on the pages), N = output features ("od").
  *  - Every pointer argument that names tensor data is a DEVICE pointer on the
  *    current CUDA device. The caller allocates and owns every buffer. The
- *    library never allocates, frees or synchronizes; it only launches kernels
- *    asynchronously on `stream` (0 = legacy default stream).
+ *    library never allocates, frees or synchronizes; it only enqueues kernels
+ *    (and, for a split GEMM, a memset of part of its output) asynchronously on
+ *    `stream` (0 = legacy default stream).
  *  - Inputs are read only. Outputs (planes, out) are overwritten, never
  *    accumulated into.
  *  - K must be a positive multiple of 256 (one weight super-block; it also
