@@ -37,6 +37,13 @@ class Guarded:
         assert np.all(raw[:GUARD] == POISON), "write before the buffer"
         assert np.all(raw[GUARD + self.nbytes:] == POISON), "write after the buffer"
 
+    def untouched(self):
+        """Number of 4-byte words of the tensor still equal to the poison (never written).
+        For f32 outputs the poison word is -4.3e8, not a value these kernels produce."""
+        words = self.raw[GUARD:GUARD + self.nbytes - self.nbytes % 4].view(torch.int32)
+        poison = int(np.frombuffer(bytes([POISON] * 4), np.int32)[0])
+        return int((words == poison).sum().item())
+
 
 class GuardedPlane:
     def __init__(self, M, K, f16=True):

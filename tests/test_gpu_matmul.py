@@ -115,6 +115,29 @@ def test_gemv_parity(kind, N, K):
     _check(out, p, w, kind, N, K)
 
 
+@pytest.mark.parametrize("kind,N,K", [("q6k", 152064, 3584), ("q4k", 27648, 5120), ("q6k", 5120, 13824),
+                                      ("q6k", 2048, 5120)])
+def test_gemv_full_size_sampled_outputs(kind, N, K):
+    """The bench's decode and lm_head GEMVs at full size (lm_head 152064 x 3584, gate|up and k|v
+    stacked, down); outputs are independent rows, so the oracle checks 512 sampled ones, always
+    the first and the last."""
+    x = synth.normal((1, K), 0, f"fv{K}", device="cuda")
+    w = synth.weights(kind, N, K, 0, f"fvw{kind}{N}", device="cuda")
+    p = mq.Plane.empty(1, K, f16=False)
+    mq.mq_quantize_q8(x, p)
+    g = Guarded((1, N), torch.float32)
+    mq.gemv(kind, p, w, N, g.t)
+    torch.cuda.synchronize()
+    g.check()
+    assert g.untouched() == 0, "unwritten outputs"
+    rows = np.unique(np.r_[np.random.default_rng(N).choice(N, 512, replace=False), 0, N - 1])
+    rt = torch.as_tensor(rows, device="cuda")
+    ref, bound = O.gemm_rows(p.qs.cpu().numpy(), p.d.cpu().numpy(), w[rt].cpu().numpy(), kind, len(rows), K)
+    got = g.t[0, rt].cpu().numpy().astype(np.float64)[None, :]
+    assert np.all(np.abs(got - ref) <= bound)
+    assert mq.mq_device_status() == mq.MQ_OK
+
+
 @pytest.mark.parametrize("N,K", [(33, 1280), (64, 2048), (9, 2304), (17, 8448)])
 def test_gemv_q6k_exact_integer_dots(N, K):
     """Unit super-block scales, sub-block scales of +-1 and integer activations whose every
