@@ -87,18 +87,21 @@ def test_gemm_partial_last_wave_every_element(kind, M, N, K):
 
 @pytest.mark.parametrize("kind,N,K", [("q4k", 18944, 3584), ("q6k", 3584, 18944), ("q4k", 512, 3584)])
 def test_gemm_full_size_sampled_rows(kind, N, K):
-    """7B prefill shapes at M = 3314, oracle on 24 sampled rows (rows are independent)."""
+    """7B prefill shapes at M = 3314, oracle on 24 sampled rows (rows are independent); every
+    output element checked as written (the q6_K shape splits its last wave along K)."""
     M = 3314
     x = synth.normal((M, K), 0, f"fx{K}", device="cuda")
     w = synth.weights(kind, N, K, 0, f"fw{kind}{N}", device="cuda")
     p = mq.Plane.empty(M, K)
     mq.mq_quantize_q8(x, p)
-    out = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    mq.gemm(kind, p, w, N, out)
+    g = Guarded((M, N), torch.float32)
+    mq.gemm(kind, p, w, N, g.t)
     torch.cuda.synchronize()
+    g.check()
+    assert g.untouched() == 0, "unwritten outputs"
     rows = np.sort(np.random.default_rng(1).choice(M, 24, replace=False))
     rows[-1] = M - 1
-    _check(out, p, w, kind, N, K, rows=rows)
+    _check(g.t, p, w, kind, N, K, rows=rows)
     assert mq.mq_device_status() == mq.MQ_OK
 
 
