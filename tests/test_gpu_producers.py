@@ -153,15 +153,17 @@ def test_producers_full_size_sampled_rows():
     rows[-1] = M - 1
     x = synth.normal((M, K), 0, "full.x", device="cuda")
     w = synth.normal((K,), 0, "full.w", mean=1.0, std=0.1, device="cuda")
-    p = mq.Plane.empty(M, K)
+    gp, gpf, gpq = GuardedPlane(M, K), GuardedPlane(M, KF), GuardedPlane(M, KF)
+    p, pf, pq = gp.plane, gpf.plane, gpq.plane
     mq.mq_rms_quant(x, w, 1e-6, p)
     g = synth.normal((M, KF), 0, "full.g", device="cuda")
     u = synth.normal((M, KF), 0, "full.u", device="cuda")
-    pf = mq.Plane.empty(M, KF)
     mq.mq_swiglu_quant(g, u, pf)
-    pq = mq.Plane.empty(M, KF)
     mq.mq_quantize_q8(g, pq)
     torch.cuda.synchronize()
+    for gx in (gp, gpf, gpq):   # every block's d and s written (their poison words are impossible values)
+        gx.check()
+        assert gx.g[1].untouched() == 0 and gx.g[2].untouched() == 0
     idx = torch.from_numpy(rows).cuda()
     sub = lambda pl: (pl.qs[idx].cpu().numpy(), pl.d[idx].cpu().numpy(), pl.s[idx].cpu().numpy())
     xs, ws = x[idx].cpu().numpy(), w.cpu().numpy()
