@@ -188,6 +188,45 @@ def test_quantize_hand_block_ties_to_even():
     assert s[0, 0] == 127 + 2 + 4 - 2 + 0 + 2 + 0 + 127
 
 
+def test_quantize_divides_rather_than_multiplies_by_the_reciprocal():
+    """R4: q = rint(v / d) with the IEEE f32 quotient. The block holds 31 values next to
+    rounding boundaries (n + 1/2) * d where v * f32(1/d) rounds to another integer; the
+    expected quants come from the exact rational v / d, correctly rounded to f32 by exact
+    comparison, then rounded half to even."""
+    f32 = np.float32
+    amax = f32(1.7)
+    d = f32(amax / f32(127))
+    inv = f32(f32(1) / d)
+
+    def exact_quotient_f32(v):
+        t = Fraction(float(v)) / Fraction(float(d))
+        c = f32(float(t))
+        cands = [np.nextafter(c, f32(-np.inf)), c, np.nextafter(c, f32(np.inf))]
+        return min(cands, key=lambda z: (abs(Fraction(float(z)) - t), int(f32(z).view(np.uint32)) & 1))
+
+    vals = []
+    for n in range(126):
+        c = f32((n + 0.5) * float(d))
+        for k in range(-40, 41):
+            v = c
+            for _ in range(abs(k)):
+                v = np.nextafter(v, f32(np.inf) if k > 0 else f32(-np.inf))
+            if np.rint(exact_quotient_f32(v)) != np.rint(f32(v * inv)):
+                vals.append(v)
+                break
+        if len(vals) == 31:
+            break
+    assert len(vals) == 31
+    block = np.array([amax] + vals, np.float32)[None, :]
+    qs, dd, ss = O.quantize_q8(block)
+    assert dd[0, 0] == d
+    expect = np.array([127] + [int(np.rint(exact_quotient_f32(v))) for v in vals])
+    reciprocal = np.array([127] + [int(np.rint(f32(v * inv))) for v in vals])
+    assert np.array_equal(qs[0].astype(int), expect)
+    assert not np.any(expect[1:] == reciprocal[1:])   # every value tells the two rules apart
+    assert ss[0, 0] == expect.sum()
+
+
 def test_quantize_zero_and_single_value_blocks():
     v = np.zeros((1, 64), np.float32)
     v[0, 40] = -0.3
