@@ -183,8 +183,14 @@ def dequant_plane(qs: np.ndarray, d: np.ndarray) -> np.ndarray:
 
 # --------------------------------------------------------------------------- fused producers
 
-def rms_scale(x: np.ndarray, eps: float) -> np.ndarray:
-    """Per-row 1/sqrt(mean(x^2) + eps) in f32, in the R8 order ([r52] §3.2; [D3-7] §2c(i))."""
+def rms_sumsq(x: np.ndarray) -> np.ndarray:
+    """Per-row sum of squares in f32, in the R8 order ([r52] §3.2; [D3-7] §2c(i), Excerpt C).
+
+    Lane l (0..31) keeps a running f32 sum over float4 number l, l+32, l+64, ... of the
+    row, each float4 adding ((x0*x0 + x1*x1) + x2*x2) + x3*x3 with every product and sum
+    rounded separately; the 32 lane sums are then combined by an xor butterfly at
+    offsets 16, 8, 4, 2, 1 (every lane ends with the same value).
+    """
     x = np.asarray(x, np.float32)
     M, K = x.shape
     f4 = x.reshape(M, K // 128, 32, 4)          # float4 number 32*j + lane
@@ -196,7 +202,14 @@ def rms_scale(x: np.ndarray, eps: float) -> np.ndarray:
     idx = np.arange(32)
     for off in (16, 8, 4, 2, 1):                # xor butterfly
         lane = lane + lane[:, idx ^ off]
-    ss = lane[:, 0]
+    return lane[:, 0]
+
+
+def rms_scale(x: np.ndarray, eps: float) -> np.ndarray:
+    """Per-row 1/sqrt(mean(x^2) + eps) in f32 with the R8 sum and correctly rounded ops (R9)."""
+    x = np.asarray(x, np.float32)
+    ss = rms_sumsq(x)
+    K = x.shape[1]
     return (np.float32(1.0) / np.sqrt(ss / np.float32(K) + np.float32(eps))).astype(np.float32)
 
 
