@@ -39,6 +39,11 @@ Readings taken where the pages are silent:
   R11 the GEMM/GEMV error bound is per output element:
       |gpu - oracle| <= 1e-3 * sum_k |a[m,k]| * |w[n,k]|, a the dequantized q8
       activation.
+  R20 the prefill GEMM reads the activations in an operand form derived from
+      the plane (operand_form): each row's super-block of dequantized values
+      d * q, scaled by a power of two and rounded to binary16, with its exact
+      per-block sums and the power of two. The pages' GEMM consumes the int8
+      plane directly; this form is what the f16 tensor pipe multiplies.
 
 Parity pins live in tests/test_oracle.py (closed forms, hand-built blocks,
 invariants, brute force). Parity unpinned: whether R1/R2 match the byte order
@@ -173,6 +178,46 @@ def quantize_q8(v: np.ndarray):
     q = np.where(nz[..., None], q, 0).astype(np.int8)
     s = q.astype(np.int32).sum(axis=-1, dtype=np.int32)
     return q.reshape(M, K), d, s
+
+
+def operand_form(qs: np.ndarray, d: np.ndarray):
+    """The prefill GEMM's activation operand, derived from a q8 plane (R20).
+
+    For every row m and super-block t (8 blocks of 32):
+      D = max_j d[m, 8t + j];  e = 3 - E where D = f * 2^E, f in [1/2, 1) (so that
+      D * 2^e lies in [4, 8)), clamped to [-126, 126]; e = 0 when D == 0;
+      ah[m, k] = f16(f32(d * q) * 2^e)           (the f32 product rounded, then
+                                                  scaled exactly, then rounded to
+                                                  binary16, ties to even);
+      sigma_j = sum of the 32 ah values of block j (exact in f32: they are
+                multiples of the smallest one's ulp and stay below 2^15);
+      ax[m, t, j] = f16(sigma_j), ax[m, t, 8 + j] = f16(sigma_j - ax[m, t, j]);
+      af[t, m] = 2^-e (f32).
+    Then 2^-e * ah is the dequantized activation d * q to within 2^-11 relative
+    (binary16 normal range), and 2^-e * (ax_hi + ax_lo) the block sums of those
+    values to within 2^-22 relative.
+    Returns ah f16 [M, K], ax f16 [M, K/256, 16], af f32 [K/256, M].
+    """
+    qs = np.asarray(qs)
+    d = np.asarray(d, np.float32)
+    M, K = qs.shape
+    S = K // QK_K
+    D = d.reshape(M, S, 8).max(axis=-1)
+    _, E = np.frexp(D)
+    e = np.clip(3 - E, -126, 126)
+    e = np.where(D == 0, 0, e).astype(np.int64)
+    scale = np.ldexp(np.float32(1.0), e.astype(np.int32)).astype(np.float32)          # [M, S]
+    dq = (np.repeat(d, QK, axis=1) * qs.astype(np.float32)).astype(np.float32)       # f32(d * q)
+    t = (dq.reshape(M, S, QK_K) * scale[..., None]).astype(np.float32)              # exact scaling
+    ah = t.astype(np.float16).reshape(M, K)
+    sig = ah.astype(np.float32).reshape(M, S, 8, QK).astype(np.float64).sum(axis=-1)
+    sig32 = sig.astype(np.float32)
+    assert np.all(sig32.astype(np.float64) == sig), "block sum of ah not exact in f32"
+    hi = sig32.astype(np.float16)
+    lo = (sig32 - hi.astype(np.float32)).astype(np.float32).astype(np.float16)
+    ax = np.concatenate([hi, lo], axis=-1)
+    af = np.ldexp(np.float32(1.0), (-e).astype(np.int32)).astype(np.float32).T.copy()
+    return ah, ax, af
 
 
 def dequant_plane(qs: np.ndarray, d: np.ndarray) -> np.ndarray:
