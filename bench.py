@@ -85,15 +85,20 @@ def wbytes(kind, N, K):
     return N * (K // 256) * BYTES_PER_SB[kind]
 
 
-def plane_bytes(M, K, f16=False):
-    """Bytes of a q8 plane: qs (1 B/elem), d and s (4 B per 32-block each), and, with f16,
-    the binary16 copy of the quants (2 B/elem) that the prefill producers also write."""
-    return M * K + M * (K // 32) * 8 + (2 * M * K if f16 else 0)
+def plane_bytes(M, K, q8=True, op=False):
+    """Bytes of a plane: the q8 arrays qs (1 B/elem), d and s (4 B per 32-block each), and the
+    GEMM operand arrays ah (2 B/elem), ax (32 B per super-block) and af (4 B per super-block)."""
+    n = 0
+    if q8:
+        n += M * K + M * (K // 32) * 8
+    if op:
+        n += 2 * M * K + M * (K // 256) * 36
+    return n
 
 
 def gemm_act_bytes(kind, M, K):
-    """Activation bytes a GEMM reads: the f16 quant copy and d (and s for q4_K's min term)."""
-    return 2 * M * K + M * (K // 32) * (8 if kind == "q4k" else 4)
+    """Activation bytes a GEMM reads: the operand arrays ah, af and (q4_K's min term) ax."""
+    return 2 * M * K + M * (K // 256) * (36 if kind == "q4k" else 4)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -173,11 +178,12 @@ class Stack:
         self.lm_head = S.q6k_weights(VOCAB, HID, seed, "lm_head", device=dev)
         f32 = dict(dtype=torch.float32, device=dev)
         self.out = {n: torch.empty((M_TOK, N), **f32) for n, _, N, _, _ in PREFILL_MATS}
-        self.p_rms = mq.Plane.empty(M_TOK, HID, dev)
-        self.p_rms2 = mq.Plane.empty(M_TOK, HID, dev)
-        self.p_attn = mq.Plane.empty(M_TOK, HID, dev)
-        self.p_ffn = mq.Plane.empty(M_TOK, FFN, dev)
-        self.p_last = mq.Plane.empty(1, HID, dev, f16=False)
+        # prefill planes feed only GEMMs: the producers write the operand arrays alone
+        self.p_rms = mq.Plane.empty(M_TOK, HID, dev, q8=False)
+        self.p_rms2 = mq.Plane.empty(M_TOK, HID, dev, q8=False)
+        self.p_attn = mq.Plane.empty(M_TOK, HID, dev, q8=False)
+        self.p_ffn = mq.Plane.empty(M_TOK, FFN, dev, q8=False)
+        self.p_last = mq.Plane.empty(1, HID, dev, op=False)
         self.logits = torch.empty((VOCAB,), **f32)
         self.q4_events = []
         if decode:
@@ -195,9 +201,9 @@ class Stack:
             self.DW = [{n: S.weights(kind, N, K, seed, f"D{l}.{n}", device=dev)
                         for n, (kind, N, K) in self.dstack.items()} for l in range(D_LAYERS)]
             self.dout = {n: torch.empty((N,), **f32) for n, (_, N, _) in self.dstack.items()}
-            self.dp_h = mq.Plane.empty(1, D_HID, dev, f16=False)
-            self.dp_a = mq.Plane.empty(1, D_HID, dev, f16=False)
-            self.dp_f = mq.Plane.empty(1, D_FFN, dev, f16=False)
+            self.dp_h = mq.Plane.empty(1, D_HID, dev, op=False)
+            self.dp_a = mq.Plane.empty(1, D_HID, dev, op=False)
+            self.dp_f = mq.Plane.empty(1, D_FFN, dev, op=False)
             # q and k|v only read the rms plane: k|v runs on a second stream, joined before the
             # attention stand-in, so the two GEMVs overlap (inside the captured graph too)
             self.side = torch.cuda.Stream(device=dev)
@@ -418,7 +424,7 @@ def run_sweep(steps: int, warmup: int):
             w = S.weights(kind, N, K, 0, f"sweep.{kind}.{N}x{K}", device=dev)
             for M in SWEEP_M:
                 x = S.with_outliers(S.normal((M, K), 0, f"sweep.x.{M}x{K}", device=dev), 0, f"sweep.o.{M}x{K}")
-                p = mq.Plane.empty(M, K, dev, f16=M > 1)
+                p = mq.Plane.empty(M, K, dev, op=M > 1)
                 mq.mq_quantize_q8(x, p)
                 out = torch.empty((M, N), dtype=torch.float32, device=dev)
                 if M == 1:
@@ -485,15 +491,15 @@ def run_case(spec: str, steps: int, warmup: int):
         flops = 0.0
         if kind == "quantize":
             fn = lambda: mq.mq_quantize_q8(x, p)
-            nbytes = 4 * M * K + plane_bytes(M, K, f16=True)
+            nbytes = 4 * M * K + plane_bytes(M, K, op=True)
         elif kind == "rms":
             w = S.normal((K,), 0, "case.rmsw", 1.0, 0.1, device=dev)
             fn = lambda: mq.mq_rms_quant(x, w, EPS, p)
-            nbytes = 4 * M * K + 4 * K + plane_bytes(M, K, f16=True)
+            nbytes = 4 * M * K + 4 * K + plane_bytes(M, K, op=True)
         elif kind == "swiglu":
             u = S.normal((M, K), 0, "case.u", device=dev)
             fn = lambda: mq.mq_swiglu_quant(x, u, p)
-            nbytes = 8 * M * K + plane_bytes(M, K, f16=True)
+            nbytes = 8 * M * K + plane_bytes(M, K, op=True)
         else:
             raise ValueError(kind)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 256 MB > L2
@@ -625,7 +631,7 @@ def main():
             "metric": METRIC, "value": job_tok_s(ws, t_ms), "unit": "tok/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": "int8 activations x 4/6-bit weights, exact on the f16 tensor pipe, f32 accumulate",
+            "dtype": "q8 activations as binary16 operands (2^-11) x exact 4/6-bit weight operands, f16 tensor pipe, f32 accumulate",
             "data": "synthetic",
             "config": {"workload": "7B-shaped matmul stack prefill (28 layers + lm_head), M=3314",
                        "hidden": HID, "ffn": FFN, "kv": KVD, "vocab": VOCAB, "layers": LAYERS,

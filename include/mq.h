@@ -59,28 +59,43 @@ enum {
  *     qs : int8     [M][K]      row-major, row stride K bytes
  *     d  : float    [M][K/32]   row-major
  *     s  : int32_t  [M][K/32]   row-major
- *     qh : uint16_t [M][K]      optional: the same quants as IEEE binary16 bit
- *                               patterns (exact: |q| <= 127), the operand form
- *                               the f16 tensor cores read. NULL = absent.
- * Producers write qh in the same pass when it is non-NULL; the GEMM requires
- * it (the GEMV does not read it). The plane is a pure function of the f32
- * values it quantizes, so one plane may feed several GEMMs (Q/K/V, gate/up).
- * The library reads only rows < M; the GEMM supplies the zero rows of a
- * partial 128-row tile itself. The struct lives in host memory; only its
- * pointers are device pointers.
+ * The prefill GEMM multiplies on the f16 tensor pipe and reads the activations
+ * in an operand form derived from the same quants (the library's reading; the
+ * pages' GEMM reads the int8 plane). Per row m and super-block t of 256
+ * (blocks 8t .. 8t+7), with D = the largest of the 8 block scales and
+ * e = 3 - E where D = f * 2^E, f in [1/2, 1) (so D * 2^e lies in [4, 8); e is
+ * clamped to [-126, 126], and e = 0 when D == 0):
+ *     ah : uint16_t [M][K]        binary16 bit patterns of f16(f32(d * q) * 2^e)
+ *                                 (|ah| < 1016);
+ *     ax : uint16_t [M][K/256][16] binary16: for block j of the super-block,
+ *                                 slot j = f16(sigma_j) and slot 8+j =
+ *                                 f16(sigma_j - slot j), sigma_j the exact f32
+ *                                 sum of the block's 32 ah values;
+ *     af : float    [K/256][Mp]   2^-e, Mp = M rounded up to a multiple of 4
+ *                                 (entries of rows >= M are not written).
+ * 2^-e * ah equals d * q to within 2^-11 relative (binary16 normal range).
+ * A plane holds the q8 arrays (qs, d, s), the operand arrays (ah, ax, af), or
+ * both; each group is all present or all NULL. Producers write every array
+ * that is present. The GEMV reads the q8 arrays, the GEMM the operand arrays.
+ * The plane is a pure function of the f32 values it quantizes, so one plane
+ * may feed several GEMMs (Q/K/V, gate/up). The library reads only rows < M.
+ * The struct lives in host memory; only its pointers are device pointers.
  */
 typedef struct mq_q8_plane {
     int8_t*   qs;
     float*    d;
     int32_t*  s;
-    uint16_t* qh;
+    uint16_t* ah;
+    uint16_t* ax;
+    float*    af;
     int M;
     int K;
 } mq_q8_plane;
 
-/* Bytes of each plane array for an M x K activation (qh, when used, takes 2*M*K
- * bytes more). Returns qs + d + s bytes. Pure host helper. */
-size_t mq_plane_bytes(int M, int K, size_t* qs_bytes, size_t* d_bytes, size_t* s_bytes);
+/* Bytes of each plane array for an M x K activation (any output pointer may be
+ * NULL). Returns the sum of all six. Pure host helper. */
+size_t mq_plane_bytes(int M, int K, size_t* qs_bytes, size_t* d_bytes, size_t* s_bytes,
+                      size_t* ah_bytes, size_t* ax_bytes, size_t* af_bytes);
 
 /*
  * Bytes of one weight row (K/256 super-blocks):
@@ -102,7 +117,8 @@ size_t mq_q6k_row_bytes(int K);
  *     amax = max|v|; d = amax / 127 (f32); q = rint(v / d) (IEEE f32 divide,
  *     ties to even) clamped to [-127, 127]; s = sum q; an all-zero block gives
  *     d = 0, q = 0, s = 0.
- * Every producer also writes out->qh when it is non-NULL.
+ * Every producer writes whichever of the plane's array groups are present
+ * (the q8 arrays, the operand arrays, or both).
  * out->M, out->K must equal M, K. Input values must be finite.
  */
 int mq_quantize_q8(const float* x, int M, int K, const mq_q8_plane* out, cudaStream_t stream);
@@ -137,22 +153,26 @@ int mq_swiglu_quant(const float* g, const float* u, int M, int K,
                     const mq_q8_plane* out, cudaStream_t stream);
 
 /*
- * mq_gemm_q4k / mq_gemm_q6k — prefill matmul of a q8 plane by super-block
- * weights ([r60] §3.1 and §3.2, the MMQ dispatch for nt >= 16; q6_K "runs as
- * k32 chunks with dual 16-sub rescale"):
+ * mq_gemm_q4k / mq_gemm_q6k — prefill matmul of a plane by super-block weights
+ * ([r60] §3.1 and §3.2, the MMQ dispatch for nt >= 16; q6_K runs each 32-wide
+ * chunk as two 16-element halves with their own int8 scales):
  *     out[m][n] = sum_k (d_a[m][k/32] * q_a[m][k]) * w[n][k]
  * with w the dequantized weight (q4_K: d*sc*q - dmin*m per 32; q6_K:
- * d*sc*(q-32) per 16). a: plane with a->M >= 1 rows, a->K = K and a->qh set
- * (MQ_ERR_NULL otherwise); w: N rows of super-blocks; out: f32 [a->M][N]
- * row-major, overwritten. Any M >= 1 is accepted (the kernel is built for
- * M >= 16). Accuracy: within 1e-3 * sum_k |a||w| per element.
- * When the output has fewer 128 x 128 tiles than the GPU has SMs (small M or
- * N), the K axis is split across several thread blocks, `out` is zeroed on
- * `stream` and the partial sums are added with f32 atomics: the result is then
- * within the same bound, but its last bits may differ from run to run. The
- * q6_K GEMM does the same for the tiles of its last, partial wave when the
- * tile count is not a multiple of the SM count: only the output columns
- * holding those tiles are zeroed, and only those tiles' last bits may vary.
+ * d*sc*(q-32) per 16). a: plane with a->M >= 1 rows, a->K = K and its operand
+ * arrays (ah, ax, af; MQ_ERR_NULL otherwise); w: N rows of super-blocks in the
+ * layout above (q6_K rows need only 2-byte alignment within the buffer); out:
+ * f32 [a->M][N] row-major, overwritten. Any M >= 1 is accepted (the kernel is
+ * built for M >= 16).
+ * Arithmetic: per 256-wide super-block, the f16 tensor pipe multiplies the
+ * binary16 activations ah by the exact integer weight operands (q4_K sc*q,
+ * q6_K sc*(q-32) in two parts) and, for q4_K, the min term's exact block sums
+ * by -dmin/d*m in hi + lo parts, accumulating in f32; the result is scaled by
+ * d * 2^-e. Accuracy: within 1e-3 * sum_k |a||w| per element (the binary16
+ * activation contributes at most 2^-11 of it).
+ * When the output has fewer 192-token x 128-row tiles than the GPU has SMs
+ * (small M or N), the K axis is split across several thread blocks, `out` is
+ * zeroed on `stream` and the partial sums are added with f32 atomics: the result
+ * is then within the same bound, but its last bits may differ from run to run.
  */
 int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);

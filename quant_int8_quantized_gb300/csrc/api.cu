@@ -43,13 +43,19 @@ int num_sms() {
 
 }  // namespace mq
 
-extern "C" size_t mq_plane_bytes(int M, int K, size_t* qs_bytes, size_t* d_bytes, size_t* s_bytes) {
+extern "C" size_t mq_plane_bytes(int M, int K, size_t* qs_bytes, size_t* d_bytes, size_t* s_bytes,
+                                 size_t* ah_bytes, size_t* ax_bytes, size_t* af_bytes) {
     const size_t m = M > 0 ? (size_t)M : 0, k = K > 0 ? (size_t)K : 0;
     const size_t qs = m * k, d = m * (k / mq::QK) * sizeof(float), s = m * (k / mq::QK) * sizeof(int32_t);
+    const size_t ah = m * k * sizeof(uint16_t), ax = m * (k / mq::QK_K) * 16 * sizeof(uint16_t);
+    const size_t af = (k / mq::QK_K) * ((m + 3) & ~(size_t)3) * sizeof(float);
     if (qs_bytes) *qs_bytes = qs;
     if (d_bytes) *d_bytes = d;
     if (s_bytes) *s_bytes = s;
-    return qs + d + s;
+    if (ah_bytes) *ah_bytes = ah;
+    if (ax_bytes) *ax_bytes = ax;
+    if (af_bytes) *af_bytes = af;
+    return qs + d + s + ah + ax + af;
 }
 
 extern "C" size_t mq_q4k_row_bytes(int K) { return K > 0 ? (size_t)(K / mq::QK_K) * mq::Q4K_BYTES : 0; }

@@ -1,41 +1,53 @@
-// Prefill GEMM: q8 activation plane x q4_K / q6_K super-block weights -> f32.
+// Prefill GEMM: activation operand form x q4_K / q6_K super-block weights -> f32.
 //
-// "64 · r60 — the coronation", §3.1-§3.2: for nt >= 16 tokens the matmul runs
-// as integer dot products of int8 activation blocks (32 wide, scale d_a) with
-// the weight quants, rescaled per block; q6_K runs as k32 chunks whose two
-// 16-element halves carry their own int8 scales.
+// "64 · r60 — the coronation", §3.1-§3.2: for nt >= 16 tokens the matmul runs as
+// block dot products of quantized activations with the weight quants, rescaled
+// per block; q6_K runs its 32-wide chunks as two 16-element halves, each with
+// its own int8 scale.
 //
-// sm_103a has no int8 tcgen05 MMA, so the integer products run on the f16
-// tensor pipe with f32 accumulation, on operands that are small integers and
-// therefore exact in f16:
-//   A (activations): q_a in [-127, 127] — the plane's binary16 copy (qh),
-//                    loaded by TMA straight into the MMA operand layout.
-//   B (q4_K):        sc * q with sc in 0..63, q in 0..15 (at most 945).
-//   B (q6_K):        sc * (q - 32) = sc*lo + 16*sc*(hi - 2) with q = lo + 16*hi,
-//                    two exact operands (|.| <= 1920, and a multiple of 16 with
-//                    |.| <= 4096), accumulated into the same block sum.
-// Per 32-wide activation block one MMA group yields the exact integer block dot
-// I (partial sums are integers below 2^24) in a TMEM slot. The epilogue applies
-// the scales: per block acc += d_a * I (one packed FMA per two outputs), per
-// super-block out += d * acc, and for q4_K out -= dmin * MS where
-// MS = sum_j m_j * (d_a,j * s_j) comes from two small tf32 MMAs (the f32 factor
-// d_a*s split into two tf32 parts; m_j is exact).
+// sm_103a has no int8 tcgen05 MMA, and GB300's int8 rate is far below its f16
+// rate, so the products run on the f16 tensor pipe with f32 accumulation. One
+// accumulation covers a whole 256-wide super-block; the epilogue rescales once
+// per super-block:
+//   activations (B operand, smem, TMA, 128-byte swizzle): the plane's operand
+//       form ah = f16(2^e * d_a * q_a), one power of two e per row and
+//       super-block, so 2^-e * ah = d_a * q_a within 2^-11;
+//   weights (A operand, tensor memory, written by converter warps):
+//       q4_K  sc * q * 2^-k, exact in f16 (sc <= 63, q <= 15; k below);
+//       q6_K  sc * (q - 32) as two exact parts sc * lo and 16 * sc * (hi - 2)
+//             (q = lo + 16 hi), two MMAs per K step into the same accumulator.
+//   q4_K min term: -dmin * sum_j m_j * sum_{k in block j} a_k is folded into the
+//       same accumulator by two more K = 16 MMAs per super-block: A (shared memory)
+//       = the exact hi + lo binary16 parts of -(dmin / (d 2^k)) m_j, B = the
+//       plane's exact block sums of ah as hi + lo parts. k >= 0 is the least power of two with
+//       |d| 2^k >= |dmin|, so the ratio is at most 1 (d = 0: the main operand
+//       is 0 and the ratio 1).
+//   epilogue: out[tok][n] += (c_n * 2^-e_tok) * S[n][tok], c = d 2^k (q4_K; dmin
+//       when d = 0) or d (q6_K).
+// The error is at most 2^-11 * sum_k |a||w| from the activation rounding plus
+// f32 accumulation and 2^-21-relative terms of the min-term ratio.
 //
-// Kernel structure (one persistent CTA per SM, 5 warpgroups, 640 threads):
-//   warp 0      TMA producer: activation f16 quants (2-D map, 64-byte swizzle,
-//               one 32-block per operand slot), activation d and s planes
-//               (2-D, one super-block per stage), weight rows (1-D bulk
-//               copies, one super-block per stage);
-//   warp 1      MMA issuer (tcgen05.mma, one thread);
+// Tile: 128 weight rows (MMA M, TMEM lanes) x 192 tokens (MMA N): at N = 192 an
+// M = 128, K = 16 MMA with A in tensor memory keeps the tensor pipe ~92% busy
+// (N = 128: 67%; A from shared memory: at most 80%).
+// Tensor memory (512 columns): two 192-column super-block accumulators (the
+// epilogue drains one while the MMAs fill the other), the weight operand slots
+// (q4_K: 4 slots of K = 64, 32 columns each; q6_K: 2 slots of K = 64 with both
+// parts, 64 columns each).
+//
+// One persistent CTA per SM, 640 threads:
+//   warp 0      TMA producer: activation slots (K = 64 x 192 tokens), the block-sum
+//               record and 2^-e row of each super-block, q4_K weight rows;
+//   warp 1      MMA issuer;
 //   warp 2      TMEM allocator;
-//   warps 4-11  B converters: 4/6-bit quants (+ sub-block scales) -> f16
-//               operand tiles, per-row super-block scales, q4_K min operand;
-//   warps 12-19 epilogue: TMEM -> registers, scale, accumulate (each warp one
-//               TMEM lane quarter x 64 columns); the running output tile lives
-//               in TMEM columns [0, 128); q4_K min-term activation operand.
-// Weight operand tiles use the no-swizzle K-major layout (8 rows x 16 B core
-// matrices). Every mbarrier wait is bounded; on timeout the kernel records an
-// error, stops, drains its own copies and MMAs, frees TMEM and returns.
+//   warps 4-11  weight converters, thread = weight row, two warps per TMEM lane
+//               quarter, each half of a super-block's K; they also stage q6_K rows
+//               (2-byte aligned) with one 224-byte bulk copy per row;
+//   warps 12-19 epilogue, thread = weight row, two warps per lane quarter, 96
+//               token columns each, accumulators in registers across the
+//               super-blocks of a work unit.
+// Every mbarrier wait is bounded; on timeout the kernel records an error, stops,
+// drains its own copies and MMAs, frees TMEM and returns.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -50,106 +62,69 @@ namespace {
 
 __device__ unsigned int g_gemm_error;   // bit 0: a bounded wait gave up
 
-constexpr int BM = 128;                 // activation rows per tile (MMA M)
-constexpr int BN = 128;                 // weight rows per tile (MMA N)
-constexpr int RB = 2;                   // weight stages (one super-block each)
-constexpr int RD = 2;                   // d/s plane stages (one super-block each)
-constexpr int RM = 2;                   // q4_K min-term operand slots
-constexpr int RS = 2;                   // per-row super-block scale slots
-constexpr int RT = 3;                   // TMEM accumulator slots (128 columns each)
+constexpr int BW = 128;                 // weight rows per tile (MMA M)
+constexpr int BT = 192;                 // tokens per tile (MMA N)
+constexpr int KS = 64;                  // K per activation slot and weight-operand slot
+constexpr int RA = 5;                   // activation slots
+constexpr int RX = 3;                   // per-super-block stages (block sums, 2^-e, weight scales c)
+constexpr int kActBytes = BT * KS * 2;  // 24576
+constexpr int kAxBytes = BT * 32;       // 16 binary16 block-sum parts per token
+constexpr int kAfBytes = BT * 4;
 constexpr int kConvWarps = 8;
-constexpr int kConvRows = BN / (8 * kConvWarps);   // weight rows per converter thread
-constexpr int kEpiWarps = 8;            // 2 per TMEM lane quarter, 64 columns each
+constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + 32 * kConvWarps + 32 * kEpiWarps;
 constexpr int kLaunchRegs = 96;         // 65536 / 640, rounded down to the allocation unit
-#ifndef MQ_REGS_OVERRIDE
-constexpr int kRegsWG0 = 48, kRegsConv = 64, kRegsEpi = 152;   // measured best of the splits that fit
-#else
-constexpr int kRegsWG0 = MQ_R0, kRegsConv = MQ_RC, kRegsEpi = MQ_RE;
-#endif
+constexpr int kRegsWG0 = 32, kRegsConv = 64, kRegsEpi = 160;
 static_assert(128 * kRegsWG0 + 32 * kConvWarps * kRegsConv + 32 * kEpiWarps * kRegsEpi <= kThreads * kLaunchRegs,
               "register split");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr uint32_t kLBO = 128;          // K-adjacent core matrices (no-swizzle tiles)
-constexpr uint32_t kSBO = 512;          // 8-row groups
-constexpr int kTile = 8192;             // 128 rows x 32 f16 (or 16 tf32)
-constexpr int kDRaw = BM * 8 * 4;       // one super-block of d (or s)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOutCol = 0, kSlotCol0 = 128;
+constexpr uint32_t kSCol0 = 0, kSCol1 = BT, kACol = 2 * BT;   // accumulators, then the weight ring
+constexpr int kMTile = BW * 16 * 2;                           // q4_K min-term operand: 128 rows x K 16, f16
+static_assert(kACol + 128 <= kTmemCols, "tensor memory");
 
 template <bool Q6>
 struct Cfg {
     static constexpr int kSB = Q6 ? mq::Q6K_BYTES : mq::Q4K_BYTES;
-    static constexpr int kBStride = Q6 ? 240 : 144;       // bytes per weight row in a stage (8 rows: distinct banks)
-    static constexpr int kBRaw = BN * kBStride;
-    static constexpr int kBTiles = Q6 ? 2 : 1;
-    static constexpr int kFSlot = kTile * (1 + kBTiles);  // A tile, then B tile(s)
-    static constexpr int RF = Q6 ? 5 : 6;                 // operand slots (one 32-block each)
-    static constexpr int kMS = Q6 ? 1 : RM;
+    static constexpr int kRowBytes = Q6 ? 224 : 144;   // staged bytes per weight row (q6_K: its aligned window)
+    static constexpr int kStage = BW * kRowBytes;
+    static constexpr int kRB = Q6 ? 2 : 3;             // weight stages
+    // Weight-operand slots in tensor memory. q4_K: slot j holds K chunk j of every super-block
+    // and is written by one converter half only. q6_K: slot j & 1, written alternately by the
+    // two halves, each waiting on its own "empty" barrier: every waiter then waits for
+    // consecutive phases of its barrier, which a parity wait tells apart.
+    static constexpr int kRF = Q6 ? 2 : 4;
+    static constexpr uint32_t kFCols = Q6 ? 64 : 32;   // tensor-memory columns per weight-operand slot
 };
 
 template <bool Q6>
 struct Smem {
-    uint8_t f16[Cfg<Q6>::RF][Cfg<Q6>::kFSlot];
-    uint8_t ms[Cfg<Q6>::kMS][Q6 ? 1024 : 2 * kTile];      // q4_K: A_ms tile, B_ms tile
-    uint8_t draw[RD][2 * kDRaw];                           // d tile, then s tile
-    uint8_t braw[RB][Cfg<Q6>::kBRaw];
-    uint2 scpack[Q6 ? 1 : BN][8];                          // q4_K: per row and sub-block {sc x2, -1024 sc x2} as f16
-    float wd[RS][BN];
-    float wdmin[RS][BN];
-    uint64_t fullB[RB], emptyB[RB], fullD[RD], emptyD[RD];
-    uint64_t fullF[Cfg<Q6>::RF], emptyF[Cfg<Q6>::RF], fullM[RM], emptyM[RM], fullS[RS], emptyS[RS];
-    uint64_t tfull[RT], tempty[RT], mma_done;
+    alignas(1024) uint8_t act[RA][kActBytes];
+    alignas(256) uint8_t ax[RX][kAxBytes];
+    alignas(16) float af[RX][BT];
+    float cvec[RX][BW];
+    alignas(128) uint8_t braw[Cfg<Q6>::kRB][Cfg<Q6>::kStage];
+    alignas(128) uint8_t mop[2][Q6 ? 16 : 2 * kMTile];   // q4_K min-term operand (hi part, lo part)
+    uint64_t act_full[RA], act_empty[RA], ax_full[RX], ax_empty[RX], c_full[RX], c_empty[RX];
+    uint64_t b_full[Cfg<Q6>::kRB], b_empty[Cfg<Q6>::kRB];
+    uint64_t a_full[Cfg<Q6>::kRF], a_empty[Cfg<Q6>::kRF][2], m_full[2], m_empty[2];
+    uint64_t t_full[2], t_empty[2], mma_done;
     uint32_t tmem;
     int abort;
 };
 
-struct Ring {
-    int i = 0;
-    uint32_t ph = 0;
-    __device__ __forceinline__ void next(int n) {
-        if (++i == n) {
-            i = 0;
-            ph ^= 1u;
-        }
-    }
-};
-
-// A work unit: one output tile and one slice [sb0, sb1) of its super-blocks. Tiles
-// are numbered m-fastest; units that share a tile add their partial sums into the
-// output, which the host zeroed beforehand.
-//   q4_K: every tile is split into `splits` slices (1 unless there are fewer tiles
-//         than SMs); unit u is slice u % splits of tile u / splits.
-//   q6_K: the first `whole` units are whole tiles (full waves over the CTAs); each
-//         tile of the last, partial wave is split into `splits` slices.
-// (The q4_K kernel keeps the plain mapping: the same hybrid there measured slower
-// through the code it makes, not through its schedule.)
+// A work unit: one output tile (token tile fastest) and a slice [sb0, sb1) of its
+// super-blocks; units that share a tile add their partial sums into the output,
+// which the host zeroed beforehand.
 struct Work {
     int m0, n0, sb0, sb1;
 };
-template <bool Q6>
-__device__ __forceinline__ Work work_of(int u, int whole, int splits, int num_mt, int S) {
-    if constexpr (!Q6) {
-        const int t = u / splits, sp = u - t * splits;
-        return Work{(t % num_mt) * BM, (t / num_mt) * BN, (sp * S) / splits, ((sp + 1) * S) / splits};
-    } else {
-        int t = u, sp = 0, ns = 1;
-        if (u >= whole) {
-            const int v = u - whole;
-            t = whole + v / splits;
-            sp = v - (t - whole) * splits;
-            ns = splits;
-        }
-        return Work{(t % num_mt) * BM, (t / num_mt) * BN, (sp * S) / ns, ((sp + 1) * S) / ns};
-    }
+__device__ __forceinline__ Work work_of(int u, int splits, int num_mt, int S) {
+    const int t = u / splits, sp = u - t * splits;
+    return Work{(t % num_mt) * BT, (t / num_mt) * BW, (sp * S) / splits, ((sp + 1) * S) / splits};
 }
 
-__device__ __forceinline__ uint32_t tile_off(int r, int kg) {
-    return (uint32_t)((r >> 3) * kSBO + kg * kLBO + (r & 7) * 16);
-}
-
-// Non-suspending test of a phase (acquire semantics, like the waits). A phase that
-// has already completed is seen sooner this way than by a suspending try_wait.
+// Non-suspending test of a phase (acquire semantics, like the waits).
 __device__ __forceinline__ bool mbar_ready(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile("{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
@@ -160,7 +135,7 @@ __device__ __forceinline__ bool mbar_ready(uint64_t* bar, uint32_t parity) {
 }
 
 template <bool Q6>
-__device__ __forceinline__ bool wait_or_abort(Smem<Q6>& sm, uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool wait1(Smem<Q6>& sm, uint64_t* bar, uint32_t parity) {
     if (mbar_ready(bar, parity) || tc::mbar_wait(bar, parity, kWaitLimitNs)) return true;
     atomicOr(&g_gemm_error, 1u);
     *(volatile int*)&sm.abort = 1;
@@ -172,8 +147,8 @@ __device__ __forceinline__ bool aborted(Smem<Q6>& sm) {
     return *(volatile int*)&sm.abort != 0;
 }
 
-// Whole-warp variants: every lane waits, and the outcome is made warp-uniform
-// so that the warp never diverges in front of a warp-collective operation.
+// Whole-warp variants: every lane waits, and the outcome is made warp-uniform so
+// that the warp never diverges in front of a warp-collective operation.
 template <bool Q6>
 __device__ __forceinline__ bool wwait(Smem<Q6>& sm, uint64_t* bar, uint32_t parity) {
     const bool ok = __all_sync(0xffffffffu, mbar_ready(bar, parity) || tc::mbar_wait(bar, parity, kWaitLimitNs));
@@ -189,101 +164,90 @@ __device__ __forceinline__ bool waborted(Smem<Q6>& sm) {
     return __any_sync(0xffffffffu, aborted(sm));
 }
 
-// f16 bit pattern of a small integer (|v| <= 2048, exact), replicated in both halves.
-__device__ __forceinline__ uint32_t h2_of_int(int v) {
-    const uint32_t h = (uint32_t)__half_as_ushort(__int2half_rn(v));
+// f16 bit pattern of a value exactly representable in binary16, in both halves.
+__device__ __forceinline__ uint32_t h2_of(float v) {
+    const uint32_t h = (uint32_t)__half_as_ushort(__float2half_rn(v));
     return h | (h << 16);
 }
+__device__ __forceinline__ uint32_t h2_pack(float lo, float hi) {
+    return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+}
 
-// Four 4-bit values in the low nibble of each byte of `x` (byte i = K position
-// i) -> f16 pairs (0, 1), (2, 3) of mul * v + add. The value v is placed in the
-// mantissa of 1024.0 (1024 + v), so mul * v + add with add = -1024 * mul gives
-// mul * v exactly for the q4_K range (|1024 * sc| <= 64512 fits in f16).
-__device__ __forceinline__ void nib4_to_f16_1024(uint32_t x, uint32_t mul2, uint32_t add2, uint32_t& p01,
-                                                 uint32_t& p23) {
+// Four 4-bit values in the low nibble of each byte of `x` (byte i = K position i)
+// -> f16 pairs (0, 1), (2, 3) of mul * v. The value is placed in the mantissa of
+// 1024 (1024 + v); with add = -1024 * mul the fused multiply-add gives mul * v
+// exactly (q4_K: mul = sc * 2^-k, |1024 * mul| <= 64512).
+__device__ __forceinline__ void nib4_1024(uint32_t x, uint32_t mul2, uint32_t add2, uint32_t& p01, uint32_t& p23) {
     p01 = tc::hfma2(tc::prmt(x, 0x64u, 0x4140u), mul2, add2);
     p23 = tc::hfma2(tc::prmt(x, 0x64u, 0x4342u), mul2, add2);
 }
 
-// Same for q6_K, where the multipliers reach 16 * 128: v (0..15) is placed as
-// 1 + v/16, and mul16 = 16 * mul, add = -16 * mul + offset never overflow f16.
-__device__ __forceinline__ void nib4_to_f16_one(uint32_t x, uint32_t mul16, uint32_t add2, uint32_t& p01,
-                                                uint32_t& p23) {
+// Same for q6_K, where the multipliers reach 256 * 128: v (0..15) is placed as
+// 1 + v/16 and mul16 = 16 * mul, add = -16 * mul + offset stay inside f16.
+__device__ __forceinline__ void nib4_one(uint32_t x, uint32_t mul16, uint32_t add2, uint32_t& p01, uint32_t& p23) {
     const uint32_t t01 = (tc::prmt(x, 0u, 0x4140u) << 6) | 0x3C003C00u;
     const uint32_t t23 = (tc::prmt(x, 0u, 0x4342u) << 6) | 0x3C003C00u;
     p01 = tc::hfma2(t01, mul16, add2);
     p23 = tc::hfma2(t23, mul16, add2);
 }
 
-// Two little-endian words starting at a 2-byte aligned shared-memory address.
-__device__ __forceinline__ void lds8_unaligned(const uint8_t* p, uint32_t& w0, uint32_t& w1) {
+__device__ __forceinline__ uint32_t byte_of(uint32_t y, uint32_t z, uint32_t w, int i) {
+    const uint32_t v = (i < 4) ? y : (i < 8 ? z : w);
+    return (v >> (8 * (i & 3))) & 0xffu;
+}
+
+// Eight little-endian words starting at a 2-byte aligned shared-memory address.
+__device__ __forceinline__ void lds32x8_unaligned(const uint8_t* p, uint32_t (&w)[8]) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~(uintptr_t)3);
+    const uint32_t* b = reinterpret_cast<const uint32_t*>(a & ~(uintptr_t)3);
     const uint32_t sh = (uint32_t)(a & 3) * 8;
-    const uint32_t v0 = w[0], v1 = w[1], v2 = w[2];
-    w0 = __funnelshift_r(v0, v1, sh);
-    w1 = __funnelshift_r(v1, v2, sh);
-}
-
-__device__ __forceinline__ uint32_t byte_at(uint32_t w0, uint32_t w1, uint32_t w2, int i) {
-    const uint32_t w = (i < 4) ? w0 : (i < 8 ? w1 : w2);
-    return (w >> (8 * (i & 3))) & 0xffu;
-}
-
-// q6_K weight rows are only 2-byte aligned, so they are staged by the converter
-// threads themselves: for each of its rows, part c of the 4 threads sharing a
-// row copies 16-byte chunks c, c+4, ... of the aligned window that holds the
-// row's 210-byte super-block (chunk copies never cross the last 16-byte
-// boundary of the buffer; the few bytes past it are copied one by one).
-// The copies form one commit group per super-block.
-__device__ __forceinline__ void q6_fetch(uint8_t* stage, const uint8_t* __restrict__ W, int n0, int sb, int N,
-                                         unsigned long long wstride, unsigned long long wtotal, int rbase, int c) {
-    const unsigned long long wend16 = wtotal & ~15ull;
+    uint32_t v[9];
 #pragma unroll
-    for (int k = 0; k < kConvRows; ++k) {
-        const int r = 8 * kConvWarps * k + rbase, n = n0 + r;
-        if (n < N) {
-            const unsigned long long start = (unsigned long long)n * wstride + (unsigned long long)sb * mq::Q6K_BYTES;
-            const unsigned long long a0 = start & ~15ull, end = start + mq::Q6K_BYTES;
-            uint8_t* dst = stage + r * Cfg<true>::kBStride;
-            for (int ch = c; ch < 14; ch += 4) {
-                const unsigned long long src = a0 + 16ull * ch;
-                if (src >= end) break;
-                if (src + 16 <= wend16) {
-                    tc::cp_async16(dst + 16 * ch, W + src);
-                } else {
-                    for (unsigned long long b = src; b < end; ++b) dst[b - a0] = W[b];
-                }
-            }
-        }
-    }
-    tc::cp_async_commit();
+    for (int i = 0; i < 9; ++i) v[i] = b[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = __funnelshift_r(v[i], v[i + 1], sh);
 }
 
 template <bool Q6>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                                                           const __grid_constant__ CUtensorMap tmD,
-                                                           const __grid_constant__ CUtensorMap tmS,
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmAct,
+                                                           const __grid_constant__ CUtensorMap tmAx,
+                                                           const __grid_constant__ CUtensorMap tmAf,
                                                            const __grid_constant__ CUtensorMap tmW,
                                                            const uint8_t* __restrict__ W, float* __restrict__ out,
-                                                           int M, int N, int K, int whole, int splits,
+                                                           int M, int N, int K, int splits,
                                                            unsigned long long wstride, unsigned long long wtotal) {
     using C = Cfg<Q6>;
-    constexpr int RF = C::RF;
+    constexpr int kRB = C::kRB, kRF = C::kRF;
     extern __shared__ uint8_t smem_raw[];
     Smem<Q6>& sm = *reinterpret_cast<Smem<Q6>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = K / mq::QK_K;
-    const int num_mt = (M + BM - 1) / BM, num_nt = (N + BN - 1) / BN;
-    const int units = Q6 ? whole + (num_mt * num_nt - whole) * splits : num_mt * num_nt * splits;
+    const int num_mt = (M + BT - 1) / BT, num_nt = (N + BW - 1) / BW;
+    const int units = num_mt * num_nt * splits;
 
     if (tid == 0) {
-        for (int i = 0; i < RB; ++i) { tc::mbar_init(&sm.fullB[i], 1); tc::mbar_init(&sm.emptyB[i], kConvWarps); }
-        for (int i = 0; i < RD; ++i) { tc::mbar_init(&sm.fullD[i], 1); tc::mbar_init(&sm.emptyD[i], kEpiWarps); }
-        for (int i = 0; i < RF; ++i) { tc::mbar_init(&sm.fullF[i], 1 + kConvWarps); tc::mbar_init(&sm.emptyF[i], 1); }
-        for (int i = 0; i < RM; ++i) { tc::mbar_init(&sm.fullM[i], 4 + kConvWarps); tc::mbar_init(&sm.emptyM[i], 1); }
-        for (int i = 0; i < RS; ++i) { tc::mbar_init(&sm.fullS[i], kConvWarps); tc::mbar_init(&sm.emptyS[i], kEpiWarps); }
-        for (int i = 0; i < RT; ++i) { tc::mbar_init(&sm.tfull[i], 1); tc::mbar_init(&sm.tempty[i], kEpiWarps); }
+        for (int i = 0; i < RA; ++i) { tc::mbar_init(&sm.act_full[i], 1); tc::mbar_init(&sm.act_empty[i], 1); }
+        for (int i = 0; i < RX; ++i) {
+            tc::mbar_init(&sm.ax_full[i], 1);
+            tc::mbar_init(&sm.ax_empty[i], 1 + kEpiWarps);   // the MMAs (block sums) and the epilogue (2^-e)
+            tc::mbar_init(&sm.c_full[i], 4);
+            tc::mbar_init(&sm.c_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < kRB; ++i) {
+            tc::mbar_init(&sm.b_full[i], Q6 ? BW : 1);       // q6_K: one bulk copy per row
+            tc::mbar_init(&sm.b_empty[i], kConvWarps);
+        }
+        for (int i = 0; i < kRF; ++i) {
+            tc::mbar_init(&sm.a_full[i], 4);
+            tc::mbar_init(&sm.a_empty[i][0], 1);
+            tc::mbar_init(&sm.a_empty[i][1], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&sm.m_full[i], 4);
+            tc::mbar_init(&sm.m_empty[i], 1);
+            tc::mbar_init(&sm.t_full[i], 1);
+            tc::mbar_init(&sm.t_empty[i], kEpiWarps);
+        }
         tc::mbar_init(&sm.mma_done, 1);
         sm.abort = 0;
         tc::fence_mbar_init();
@@ -296,444 +260,361 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (warp < 4) {
         // ============================================================ warpgroup 0
         tc::setmaxnreg_dec<kRegsWG0>();
-        if (warp == 0) {
+        if (warp == 0 && lane == 0) {
             // ---------------------------------------------------- TMA producer
-            Ring rb, rd, rf;
-            uint32_t issB = 0, issD = 0, issF = 0;        // bit i: stage i has a copy in flight
-            uint32_t phB = 0, phD = 0, phF = 0;           // bit i: parity of that copy
-            for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-                const Work wk = work_of<Q6>(u, whole, splits, num_mt, S);
-                const int m0 = wk.m0, n0 = wk.n0;
-                for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
-                    // activation d and s of this super-block
-                    if (lane == 0 && wait_or_abort(sm, &sm.emptyD[rd.i], rd.ph ^ 1u)) {
-                        tc::mbar_arrive_expect_tx(&sm.fullD[rd.i], 2 * kDRaw);
-                        tc::tma_load_2d(sm.draw[rd.i], &tmD, sb * 8, m0, &sm.fullD[rd.i]);
-                        tc::tma_load_2d(sm.draw[rd.i] + kDRaw, &tmS, sb * 8, m0, &sm.fullD[rd.i]);
-                        issD |= 1u << rd.i;
-                        phD = (phD & ~(1u << rd.i)) | (rd.ph << rd.i);
-                    }
-                    rd.next(RD);
-                    // q4_K weight rows n0..n0+127 of this super-block: one 2-D copy (rows >= N read as zeros).
-                    // q6_K rows are only 2-byte aligned; the converters fetch them themselves.
+            uint32_t issA = 0, phA = 0, issX = 0, phX = 0, issB = 0, phB = 0;   // copies in flight (for an abort)
+            int sbc = 0, ga = 0;
+            for (int u = blockIdx.x; u < units && !aborted(sm); u += gridDim.x) {
+                const Work wk = work_of(u, splits, num_mt, S);
+                for (int sb = wk.sb0; sb < wk.sb1 && !aborted(sm); ++sb, ++sbc) {
+                    const int x = sbc % RX;
+                    if (!wait1(sm, &sm.ax_empty[x], ((sbc / RX) & 1) ^ 1)) break;
+                    tc::mbar_arrive_expect_tx(&sm.ax_full[x], kAxBytes + kAfBytes);
+                    tc::tma_load_2d(sm.ax[x], &tmAx, 16 * sb, wk.m0, &sm.ax_full[x]);
+                    tc::tma_load_2d(sm.af[x], &tmAf, wk.m0, sb, &sm.ax_full[x]);
+                    issX |= 1u << x;
+                    phX = (phX & ~(1u << x)) | (((sbc / RX) & 1) << x);
                     if constexpr (!Q6) {
-                        if (lane == 0 && wait_or_abort(sm, &sm.emptyB[rb.i], rb.ph ^ 1u)) {
-                            tc::mbar_arrive_expect_tx(&sm.fullB[rb.i], C::kBRaw);
-                            tc::tma_load_2d(sm.braw[rb.i], &tmW, sb * C::kSB, n0, &sm.fullB[rb.i]);
-                            issB |= 1u << rb.i;
-                            phB = (phB & ~(1u << rb.i)) | (rb.ph << rb.i);
-                        }
-                        rb.next(RB);
+                        const int b = sbc % kRB;
+                        if (!wait1(sm, &sm.b_empty[b], ((sbc / kRB) & 1) ^ 1)) break;
+                        tc::mbar_arrive_expect_tx(&sm.b_full[b], C::kStage);
+                        tc::tma_load_2d(sm.braw[b], &tmW, sb * C::kSB, wk.n0, &sm.b_full[b]);
+                        issB |= 1u << b;
+                        phB = (phB & ~(1u << b)) | (((sbc / kRB) & 1) << b);
                     }
-                    // activation f16 quants: one 32-block per operand slot
-                    for (int j = 0; j < 8; ++j) {
-                        if (lane == 0 && wait_or_abort(sm, &sm.emptyF[rf.i], rf.ph ^ 1u)) {
-                            tc::mbar_arrive_expect_tx(&sm.fullF[rf.i], kTile);
-                            tc::tma_load_2d(sm.f16[rf.i], &tmA, sb * 256 + 32 * j, m0, &sm.fullF[rf.i]);
-                            issF |= 1u << rf.i;
-                            phF = (phF & ~(1u << rf.i)) | (rf.ph << rf.i);
-                        }
-                        rf.next(RF);
+                    bool ok = true;
+                    for (int j = 0; j < 4; ++j, ++ga) {
+                        const int a = ga % RA;
+                        if (!wait1(sm, &sm.act_empty[a], ((ga / RA) & 1) ^ 1)) { ok = false; break; }
+                        tc::mbar_arrive_expect_tx(&sm.act_full[a], kActBytes);
+                        tc::tma_load_2d(sm.act[a], &tmAct, sb * 256 + KS * j, wk.m0, &sm.act_full[a]);
+                        issA |= 1u << a;
+                        phA = (phA & ~(1u << a)) | (((ga / RA) & 1) << a);
                     }
+                    if (!ok) break;
                 }
             }
-            if (aborted(sm) && lane == 0) {   // let every copy already issued land before the CTA exits
-                for (int i = 0; i < RF; ++i) if (issF >> i & 1u) tc::mbar_wait(&sm.fullF[i], phF >> i & 1u, kWaitLimitNs);
-                for (int i = 0; i < RB; ++i) if (issB >> i & 1u) tc::mbar_wait(&sm.fullB[i], phB >> i & 1u, kWaitLimitNs);
-                for (int i = 0; i < RD; ++i) if (issD >> i & 1u) tc::mbar_wait(&sm.fullD[i], phD >> i & 1u, kWaitLimitNs);
+            if (aborted(sm)) {   // let every copy already issued land before the CTA exits
+                for (int i = 0; i < RA; ++i) if (issA >> i & 1u) tc::mbar_wait(&sm.act_full[i], phA >> i & 1u, kWaitLimitNs);
+                for (int i = 0; i < RX; ++i) if (issX >> i & 1u) tc::mbar_wait(&sm.ax_full[i], phX >> i & 1u, kWaitLimitNs);
+                for (int i = 0; i < kRB; ++i) if (issB >> i & 1u) tc::mbar_wait(&sm.b_full[i], phB >> i & 1u, kWaitLimitNs);
             }
-        } else if (warp == 1) {
+        } else if (warp == 1 && lane == 0) {
             // ---------------------------------------------------- MMA issuer
-            // The whole warp runs the loop and waits; lane 0 issues. (A warp whose other 31
-            // lanes stay parked while one lane runs the kernel-long loop slows every warp of
-            // its SM sub-partition.)
-            Ring rf, rm, rt;
-            const uint32_t idesc = tc::instr_desc(BM, BN, 0);
-            const uint32_t idesc32 = tc::instr_desc(BM, BN, 2);
+            const uint32_t idesc = tc::instr_desc(BW, BT, 0);
             bool issued = false;
-            for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-                const Work wk = work_of<Q6>(u, whole, splits, num_mt, S);
-                for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
-                    for (int j = 0; j < 8; ++j) {
-                        if (!wwait(sm, &sm.fullF[rf.i], rf.ph)) break;
-                        if (!wwait(sm, &sm.tempty[rt.i], rt.ph ^ 1u)) break;
-                        tc::tc_fence_after();
-                        if (lane == 0) {
-                            const uint32_t d = tbase + kSlotCol0 + 128u * rt.i;
-                            const uint32_t sa = tc::smem_u32(sm.f16[rf.i]);
-#pragma unroll
-                            for (int part = 0; part < C::kBTiles; ++part) {
-                                const uint32_t sbb = sa + kTile * (1 + part);
-#pragma unroll
-                                for (int k = 0; k < 2; ++k)
-                                    tc::mma_f16(d, tc::smem_desc_sw64(sa + 32 * k, 512),
-                                                tc::smem_desc_noswizzle(sbb + k * 2 * kLBO, kLBO, kSBO), idesc,
-                                                (part | k) ? 1u : 0u);
-                            }
-                            tc::mma_commit(&sm.emptyF[rf.i]);
-                            tc::mma_commit(&sm.tfull[rt.i]);
+            int sbc = 0, ga = 0;
+            for (int u = blockIdx.x; u < units && !aborted(sm); u += gridDim.x) {
+                const Work wk = work_of(u, splits, num_mt, S);
+                for (int sb = wk.sb0; sb < wk.sb1 && !aborted(sm); ++sb, ++sbc) {
+                    const int s = sbc & 1;
+                    const uint32_t dcol = tbase + (s ? kSCol1 : kSCol0);
+                    if (!wait1(sm, &sm.t_empty[s], ((sbc >> 1) & 1) ^ 1)) break;
+                    bool ok = true;
+                    for (int j = 0; j < 4; ++j, ++ga) {
+                        // slot f; its use number u (q4_K: one use a super-block; q6_K: two)
+                        const int a = ga % RA, f = Q6 ? (j & 1) : j, u = Q6 ? 2 * sbc + (j >> 1) : sbc;
+                        if (!wait1(sm, &sm.act_full[a], (ga / RA) & 1) || !wait1(sm, &sm.a_full[f], u & 1)) {
+                            ok = false;
+                            break;
                         }
-                        __syncwarp();
+                        tc::tc_fence_after();
+                        const uint32_t sa = tc::smem_u32(sm.act[a]);
+                        const uint32_t fa = tbase + kACol + C::kFCols * f;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t bd = tc::smem_desc_sw128(sa + 32 * k);
+                            tc::mma_f16_ts(dcol, fa + 8 * k, bd, idesc, (j | k) ? 1u : 0u);
+                            if constexpr (Q6) tc::mma_f16_ts(dcol, fa + 32 + 8 * k, bd, idesc, 1u);
+                        }
+                        tc::mma_commit(&sm.act_empty[a]);
+                        // q6_K: the next writer of slot f is the other half
+                        tc::mma_commit(&sm.a_empty[f][Q6 ? 1 - (j >> 1) : 0]);
                         issued = true;
-                        rf.next(RF);
-                        rt.next(RT);
                     }
+                    if (!ok) break;
+                    const int x = sbc % RX;
+                    if (!wait1(sm, &sm.ax_full[x], (sbc / RX) & 1)) break;
                     if constexpr (!Q6) {
-                        if (waborted(sm)) break;
-                        if (!wwait(sm, &sm.fullM[rm.i], rm.ph)) break;
-                        if (!wwait(sm, &sm.tempty[rt.i], rt.ph ^ 1u)) break;
+                        const int m = sbc & 1;
+                        if (!wait1(sm, &sm.m_full[m], (sbc >> 1) & 1)) break;
                         tc::tc_fence_after();
-                        if (lane == 0) {
-                            const uint32_t d = tbase + kSlotCol0 + 128u * rt.i;
-                            const uint32_t sa = tc::smem_u32(sm.ms[rm.i]);
-#pragma unroll
-                            for (int k = 0; k < 2; ++k)
-                                tc::mma_tf32(d, tc::smem_desc_noswizzle(sa + k * 2 * kLBO, kLBO, kSBO),
-                                             tc::smem_desc_noswizzle(sa + kTile + k * 2 * kLBO, kLBO, kSBO), idesc32,
-                                             k ? 1u : 0u);
-                            tc::mma_commit(&sm.emptyM[rm.i]);
-                            tc::mma_commit(&sm.tfull[rt.i]);
-                        }
-                        __syncwarp();
-                        rm.next(RM);
-                        rt.next(RT);
+                        const uint64_t bd = tc::smem_desc_sw32(tc::smem_u32(sm.ax[x]));
+                        const uint32_t ma = tc::smem_u32(sm.mop[m]);
+                        tc::mma_f16(dcol, tc::smem_desc_noswizzle(ma, 128, 256), bd, idesc, 1u);
+                        tc::mma_f16(dcol, tc::smem_desc_noswizzle(ma + kMTile, 128, 256), bd, idesc, 1u);
+                        tc::mma_commit(&sm.m_empty[m]);
                     }
+                    tc::mma_commit(&sm.ax_empty[x]);
+                    tc::mma_commit(&sm.t_full[s]);
                 }
             }
-            if (lane == 0 && issued) {   // every MMA of this CTA has completed before TMEM is freed
+            if (issued) {   // every MMA of this CTA has completed before TMEM is freed
                 tc::mma_commit(&sm.mma_done);
                 tc::mbar_wait(&sm.mma_done, 0, kWaitLimitNs);
             }
             tc::tc_fence_before();
-            __syncwarp();
         }
+        __syncwarp();
     } else if (warp < 4 + kConvWarps) {
-        // ============================================================ B converters
+        // ============================================================ weight converters
         tc::setmaxnreg_dec<kRegsConv>();
-        const int c = lane >> 3;                       // 8-position part of a 32-block
-        const int rbase = 8 * (warp - 4) + (lane & 7); // rows rbase + 64k: a quarter-warp covers 8 consecutive rows
-        Ring rb, rf, rm, rs;
-        if constexpr (Q6) {   // the first super-block of the first tile
-            if (blockIdx.x < units) {
-                const Work w0 = work_of<Q6>(blockIdx.x, whole, splits, num_mt, S);
-                q6_fetch(sm.braw[0], W, w0.n0, w0.sb0, N, wstride, wtotal, rbase, c);
+        const int q = warp & 3, h = (warp - 4) >> 2;
+        const int r = 32 * q + lane;                            // weight row within the tile
+        const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
+        int sbc = 0;
+        uint32_t issB = 0, phB = 0;                             // q6_K copies in flight (for an abort)
+        // q6_K: threads of the h == 0 warps stage their row's super-block window, one stage ahead
+        auto q6_issue = [&](int sbc_i, const Work& wk_i, int sb_i) {
+            const int b = sbc_i % kRB;
+            if (!wwait(sm, &sm.b_empty[b], ((sbc_i / kRB) & 1) ^ 1)) return false;
+            const int n = wk_i.n0 + r;
+            uint8_t* dst = sm.braw[b] + r * C::kRowBytes;
+            uint32_t bytes = 0;
+            const unsigned long long a0 =
+                n < N ? (((unsigned long long)n * wstride + (unsigned long long)sb_i * C::kSB) & ~15ull) : 0;
+            if (n < N) {
+                bytes = C::kRowBytes;
+                if (a0 + C::kRowBytes > wtotal) {   // the matrix's last super-block: copy its tail by hand
+                    bytes = (uint32_t)((wtotal - a0) & ~15ull);
+                    for (unsigned long long p = a0 + bytes; p < wtotal; ++p) dst[p - a0] = W[p];
+                }
+            }
+            tc::mbar_arrive_expect_tx(&sm.b_full[b], bytes);
+            if (bytes) tc::bulk_load(dst, W + a0, bytes, &sm.b_full[b]);
+            issB |= 1u << b;
+            phB = (phB & ~(1u << b)) | (((sbc_i / kRB) & 1) << b);
+            return true;
+        };
+        if constexpr (Q6) {
+            if (h == 0 && blockIdx.x < units) {
+                const Work w0 = work_of(blockIdx.x, splits, num_mt, S);
+                q6_issue(0, w0, w0.sb0);
             }
         }
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of<Q6>(u, whole, splits, num_mt, S);
-            const int n0 = wk.n0;
-            for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
+            const Work wk = work_of(u, splits, num_mt, S);
+            const int n = wk.n0 + r;
+            for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb, ++sbc) {
+                const int b = sbc % kRB, x = sbc % RX;
                 if constexpr (Q6) {
-                    // prefetch the next super-block into the other stage, then wait for this one
-                    const int nu = (sb + 1 < wk.sb1) ? u : u + (int)gridDim.x;
-                    if (nu < units) {
-                        const Work nw = (nu == u) ? wk : work_of<Q6>(nu, whole, splits, num_mt, S);
-                        q6_fetch(sm.braw[rb.i ^ 1], W, nw.n0, (nu == u) ? sb + 1 : nw.sb0, N, wstride, wtotal, rbase, c);
-                    }
-                    else tc::cp_async_commit();
-                    tc::cp_async_wait<1>();
-                    __syncwarp();
-                } else {
-                    if (!wwait(sm, &sm.fullB[rb.i], rb.ph)) break;
-                }
-                if (!wwait(sm, &sm.emptyS[rs.i], rs.ph ^ 1u)) break;
-                if constexpr (!Q6) {
-                    if (!wwait(sm, &sm.emptyM[rm.i], rm.ph ^ 1u)) break;
-                }
-                const uint8_t* stage = sm.braw[rb.i];
-                // ---- per-row super-block scales
-#pragma unroll
-                for (int k = 0; k < kConvRows; ++k) {
-                    const int r = 8 * kConvWarps * k + rbase, n = n0 + r;
-                    const bool valid = n < N;
-                    if constexpr (Q6) {
-                        const int delta = (int)(((unsigned long long)n * wstride + (unsigned long long)sb * C::kSB) & 15ull);
-                        if (c == 0)
-                            sm.wd[rs.i][r] = valid ? __half2float(__ushort_as_half(
-                                                         *reinterpret_cast<const unsigned short*>(stage + r * C::kBStride + delta + 208)))
-                                                   : 0.0f;
-                    } else {
-                        uint4 hdr = make_uint4(0, 0, 0, 0);
-                        if (valid) hdr = *reinterpret_cast<const uint4*>(stage + r * C::kBStride);
-                        if (c == 0) {
-                            sm.wd[rs.i][r] = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
-                            sm.wdmin[rs.i][r] = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+                    if (h == 0) {   // stage the next super-block (of this unit or the next one)
+                        const int nu = (sb + 1 < wk.sb1) ? u : u + (int)gridDim.x;
+                        if (nu < units) {
+                            const Work nw = (nu == u) ? wk : work_of(nu, splits, num_mt, S);
+                            if (!q6_issue(sbc + 1, nw, nu == u ? sb + 1 : nw.sb0)) break;
                         }
-                        // part c decodes sub-blocks 2c, 2c+1: f16 {sc, sc}, {-1024 sc, -1024 sc}, and the mins
-                        float mv[2];
+                    }
+                }
+                if (!wwait(sm, &sm.b_full[b], (sbc / kRB) & 1)) break;
+                const uint8_t* row = sm.braw[b] + r * C::kRowBytes;
+                if constexpr (!Q6) {
+                    // ---- q4_K: scales and the power of two k; the main operand, then (h == 0) the
+                    //      min-term operand and the epilogue's scale c
+                    const uint4 hdr = *reinterpret_cast<const uint4*>(row);
+                    const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
+                    const float dmin = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+                    int k = 0;
+                    float c = dmin, rr = 1.0f;
+                    if (d != 0.0f) {
+                        float t = fabsf(d);
+                        while (t < fabsf(dmin) && k < 24) {
+                            t *= 2.0f;
+                            ++k;
+                        }
+                        c = ldexpf(d, k);
+                        rr = __fdiv_rn(dmin, c);
+                    }
+                    // ---- the main operand: slots j = 2h, 2h + 1 (sub-blocks 2j, 2j + 1)
+                    bool ok = true;
 #pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int j = 2 * c + u;
-                            int sc, mn;
-                            if (j < 4) {
-                                sc = (int)(byte_at(hdr.y, hdr.z, hdr.w, j) & 63u);
-                                mn = (int)(byte_at(hdr.y, hdr.z, hdr.w, j + 4) & 63u);
-                            } else {
-                                const uint32_t b = byte_at(hdr.y, hdr.z, hdr.w, j + 4);
-                                sc = (int)((b & 15u) | ((byte_at(hdr.y, hdr.z, hdr.w, j - 4) >> 6) << 4));
-                                mn = (int)((b >> 4) | ((byte_at(hdr.y, hdr.z, hdr.w, j) >> 6) << 4));
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * h + jj, f = j;   // slot j: this half's own, one use a super-block
+                        if (!wwait(sm, &sm.a_empty[f][0], (sbc & 1) ^ 1)) { ok = false; break; }
+                        tc::tc_fence_after();   // the stores below come after the MMAs that read the slot
+                        const int s0 = j < 2 ? (int)(byte_of(hdr.y, hdr.z, hdr.w, 2 * j) & 63u)
+                                             : (int)((byte_of(hdr.y, hdr.z, hdr.w, 2 * j + 4) & 15u) |
+                                                     ((byte_of(hdr.y, hdr.z, hdr.w, 2 * j - 4) >> 6) << 4));
+                        const int s1 = j < 2 ? (int)(byte_of(hdr.y, hdr.z, hdr.w, 2 * j + 1) & 63u)
+                                             : (int)((byte_of(hdr.y, hdr.z, hdr.w, 2 * j + 5) & 15u) |
+                                                     ((byte_of(hdr.y, hdr.z, hdr.w, 2 * j - 3) >> 6) << 4));
+                        const float m0f = d != 0.0f ? ldexpf((float)s0, -k) : 0.0f;
+                        const float m1f = d != 0.0f ? ldexpf((float)s1, -k) : 0.0f;
+                        const uint32_t mul0 = h2_of(m0f), add0 = h2_of(-1024.0f * m0f);
+                        const uint32_t mul1 = h2_of(m1f), add1 = h2_of(-1024.0f * m1f);
+                        const uint4 qa = *reinterpret_cast<const uint4*>(row + 16 + 32 * j);
+                        const uint4 qb = *reinterpret_cast<const uint4*>(row + 32 + 32 * j);
+                        const uint32_t wv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+                        uint32_t o[32];
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            nib4_1024(wv[w] & 0x0F0F0F0Fu, mul0, add0, o[2 * w], o[2 * w + 1]);
+                            nib4_1024((wv[w] >> 4) & 0x0F0F0F0Fu, mul1, add1, o[16 + 2 * w], o[16 + 2 * w + 1]);
+                        }
+                        tc::tmem_st32(tbase + lane_bits + kACol + C::kFCols * f, o);
+                        tc::tmem_st_wait();
+                        tc::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&sm.a_full[f]);
+                    }
+                    if (!ok) break;
+                    if (h == 0) {
+                        const int mslot = sbc & 1;
+                        if (!wwait(sm, &sm.m_empty[mslot], ((sbc >> 1) & 1) ^ 1)) break;
+                        uint32_t mh[8];
+#pragma unroll
+                        for (int j = 0; j < 8; j += 2) {
+                            float v[2];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int jj = j + e;
+                                const uint32_t mn = jj < 4 ? (byte_of(hdr.y, hdr.z, hdr.w, jj + 4) & 63u)
+                                                           : ((byte_of(hdr.y, hdr.z, hdr.w, jj + 4) >> 4) |
+                                                              ((byte_of(hdr.y, hdr.z, hdr.w, jj) >> 6) << 4));
+                                v[e] = -__fmul_rn(rr, (float)mn);
                             }
-                            sm.scpack[r][j] = make_uint2(h2_of_int(sc), h2_of_int(-1024 * sc));
-                            mv[u] = (float)mn;
+                            const float hi0 = __half2float(__float2half_rn(v[0])), hi1 = __half2float(__float2half_rn(v[1]));
+                            mh[j / 2] = h2_pack(v[0], v[1]);
+                            mh[4 + j / 2] = h2_pack(__fsub_rn(v[0], hi0), __fsub_rn(v[1], hi1));
                         }
-                        // B_ms row r: K' = j and 8 + j both hold m_j; part c writes K' 2c, 2c+1 and 8+2c, 9+2c
-                        *reinterpret_cast<float2*>(sm.ms[rm.i] + kTile + tile_off(r, c >> 1) + 8 * (c & 1)) =
-                            make_float2(mv[0], mv[1]);
-                        *reinterpret_cast<float2*>(sm.ms[rm.i] + kTile + tile_off(r, 2 + (c >> 1)) + 8 * (c & 1)) =
-                            make_float2(mv[0], mv[1]);
+                        // row r of the hi tile [hi_0..hi_7, hi_0..hi_7] and of the lo tile, K-major
+                        // without swizzle: core matrices of 8 rows x 16 B, K-adjacent ones 128 B apart
+                        uint8_t* mt = sm.mop[mslot] + (r >> 3) * 256 + (r & 7) * 16;
+                        const uint4 vh = make_uint4(mh[0], mh[1], mh[2], mh[3]), vl = make_uint4(mh[4], mh[5], mh[6], mh[7]);
+                        *reinterpret_cast<uint4*>(mt) = vh;
+                        *reinterpret_cast<uint4*>(mt + 128) = vh;
+                        *reinterpret_cast<uint4*>(mt + kMTile) = vl;
+                        *reinterpret_cast<uint4*>(mt + kMTile + 128) = vl;
+                        tc::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&sm.m_full[mslot]);
+                        if (!wwait(sm, &sm.c_empty[x], ((sbc / RX) & 1) ^ 1)) break;
+                        sm.cvec[x][r] = n < N ? c : 0.0f;
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&sm.c_full[x]);
                     }
-                }
-                if constexpr (!Q6) tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tc::mbar_arrive(&sm.fullS[rs.i]);
-                    if constexpr (!Q6) tc::mbar_arrive(&sm.fullM[rm.i]);
-                }
-                rs.next(RS);
-                if constexpr (!Q6) rm.next(RM);
-
-                // ---- operand tiles, two 32-blocks per step
+                } else {
+                    // ---- q6_K: the row's super-block sits at offset o of its aligned window
+                    const int o = n < N ? (int)(((unsigned long long)n * wstride + (unsigned long long)sb * C::kSB) & 15ull)
+                                        : 0;
+                    const uint8_t* blk = row + o;
+                    bool ok = true;
+                    // slot j = 2h + jj covers half h, quarters 2jj and 2jj + 1
+                    uint32_t qh[8];
+                    lds32x8_unaligned(blk + 128 + 32 * h, qh);
 #pragma unroll
-                for (int P = 0; P < 4; ++P) {
-                    const int f0 = rf.i;
-                    if (!wwait(sm, &sm.emptyF[rf.i], rf.ph ^ 1u)) break;
-                    rf.next(RF);
-                    const int f1 = rf.i;
-                    if (!wwait(sm, &sm.emptyF[rf.i], rf.ph ^ 1u)) break;
-                    rf.next(RF);
-                    uint8_t* b0 = sm.f16[f0] + kTile;
-                    uint8_t* b1 = sm.f16[f1] + kTile;
-                    // Rows >= N convert to zeros (q4_K: the copy zero-filled them, so their scales
-                    // are 0; q6_K: their scale is taken as 0). For q6_K all shared-memory loads of
-                    // the thread's rows come before any store: a store may alias a later load as
-                    // far as the compiler knows, which would serialise the rows.
-                    if constexpr (!Q6) {
-                        // sub-blocks 2P (low nibbles) and 2P+1 (high nibbles), positions 8c .. 8c+7. (Here
-                        // the per-row order measured faster than loads first: fewer live registers.)
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int j = 2 * h + jj, f = jj;
+                        // slot jj alternates between the halves: half 0 waits for the previous
+                        // super-block's half-1 use to be read, half 1 for this super-block's half-0 use
+                        if (!wwait(sm, &sm.a_empty[f][h], h ? (sbc & 1) : ((sbc & 1) ^ 1))) { ok = false; break; }
+                        tc::tc_fence_after();   // the stores below come after the MMAs that read the slot
+                        const uint32_t fa = tbase + lane_bits + kACol + C::kFCols * f;
+                        const uint32_t scw = (uint32_t)blk[192 + 8 * h + 4 * jj] | ((uint32_t)blk[193 + 8 * h + 4 * jj] << 8) |
+                                             ((uint32_t)blk[194 + 8 * h + 4 * jj] << 16) |
+                                             ((uint32_t)blk[195 + 8 * h + 4 * jj] << 24);
 #pragma unroll
-                        for (int k = 0; k < kConvRows; ++k) {
-                            const int r = 8 * kConvWarps * k + rbase;
-                            const uint4 sp = *reinterpret_cast<const uint4*>(&sm.scpack[r][2 * P]);
-                            const uint2 q = *reinterpret_cast<const uint2*>(stage + r * C::kBStride + 16 + 32 * P + 8 * c);
-                            const uint32_t m4 = 0x0F0F0F0Fu;
-                            uint4 o0, o1;
-                            nib4_to_f16_1024(q.x & m4, sp.x, sp.y, o0.x, o0.y);
-                            nib4_to_f16_1024(q.y & m4, sp.x, sp.y, o0.z, o0.w);
-                            nib4_to_f16_1024((q.x >> 4) & m4, sp.z, sp.w, o1.x, o1.y);
-                            nib4_to_f16_1024((q.y >> 4) & m4, sp.z, sp.w, o1.z, o1.w);
-                            *reinterpret_cast<uint4*>(b0 + tile_off(r, c)) = o0;
-                            *reinterpret_cast<uint4*>(b1 + tile_off(r, c)) = o1;
+                        for (int i = 0; i < 2; ++i) {          // quarter t = 2 jj + i
+                            uint32_t ql[8];
+                            lds32x8_unaligned(blk + 64 * h + 32 * i, ql);
+                            const int nsh = jj ? 4 : 0, hsh = 2 * (2 * jj + i);
+                            uint32_t p1[16], p2[16];
+#pragma unroll
+                            for (int w = 0; w < 8; ++w) {
+                                const float sc = (float)(int)(int8_t)(scw >> (8 * (2 * i + (w >> 2))));
+                                nib4_one((ql[w] >> nsh) & 0x0F0F0F0Fu, h2_of(16.0f * sc), h2_of(-16.0f * sc), p1[2 * w],
+                                         p1[2 * w + 1]);
+                                nib4_one((qh[w] >> hsh) & 0x03030303u, h2_of(256.0f * sc), h2_of(-288.0f * sc), p2[2 * w],
+                                         p2[2 * w + 1]);
+                            }
+                            tc::tmem_st16(fa + 16 * i, p1);
+                            tc::tmem_st16(fa + 32 + 16 * i, p2);
                         }
-                    } else {
-                        // blocks 2P, 2P+1: half h, quarters tq0 = 2(P&1), tq0+1
-                        const int h = P >> 1, tq0 = 2 * (P & 1), nsh = (P & 1) ? 4 : 0;
-                        uint32_t l0a[kConvRows], l0b[kConvRows], l1a[kConvRows], l1b[kConvRows], qa[kConvRows],
-                            qb[kConvRows];
-                        int sc0[kConvRows], sc1[kConvRows];
-#pragma unroll
-                        for (int k = 0; k < kConvRows; ++k) {
-                            const int r = 8 * kConvWarps * k + rbase, n = n0 + r;
-                            const int delta = (int)(((unsigned long long)n * wstride + (unsigned long long)sb * C::kSB) & 15ull);
-                            const uint8_t* blk = stage + r * C::kBStride + delta;
-                            lds8_unaligned(blk + 64 * h + 8 * c, l0a[k], l0b[k]);
-                            lds8_unaligned(blk + 64 * h + 32 + 8 * c, l1a[k], l1b[k]);
-                            lds8_unaligned(blk + 128 + 32 * h + 8 * c, qa[k], qb[k]);
-                            sc0[k] = (n < N) ? (int)(int8_t)blk[192 + 4 * P + (c >> 1)] : 0;
-                            sc1[k] = (n < N) ? (int)(int8_t)blk[192 + 4 * P + 2 + (c >> 1)] : 0;
-                        }
-#pragma unroll
-                        for (int k = 0; k < kConvRows; ++k) {
-                            const int r = 8 * kConvWarps * k + rbase;
-                            const uint32_t m0 = h2_of_int(16 * sc0[k]), a0 = h2_of_int(-16 * sc0[k]);
-                            const uint32_t m1 = h2_of_int(16 * sc1[k]), a1 = h2_of_int(-16 * sc1[k]);
-                            const uint32_t hm0 = h2_of_int(256 * sc0[k]), ha0 = h2_of_int(-288 * sc0[k]);
-                            const uint32_t hm1 = h2_of_int(256 * sc1[k]), ha1 = h2_of_int(-288 * sc1[k]);
-                            const uint32_t m4 = 0x0F0F0F0Fu, m2 = 0x03030303u;
-                            uint4 o0, o1, o2, o3;
-                            // block 2P: B1 = sc*lo -> o0, B2 = 16 sc (hi - 2) -> o1
-                            nib4_to_f16_one((l0a[k] >> nsh) & m4, m0, a0, o0.x, o0.y);
-                            nib4_to_f16_one((l0b[k] >> nsh) & m4, m0, a0, o0.z, o0.w);
-                            nib4_to_f16_one((qa[k] >> (2 * tq0)) & m2, hm0, ha0, o1.x, o1.y);
-                            nib4_to_f16_one((qb[k] >> (2 * tq0)) & m2, hm0, ha0, o1.z, o1.w);
-                            // block 2P+1 -> o2, o3
-                            nib4_to_f16_one((l1a[k] >> nsh) & m4, m1, a1, o2.x, o2.y);
-                            nib4_to_f16_one((l1b[k] >> nsh) & m4, m1, a1, o2.z, o2.w);
-                            nib4_to_f16_one((qa[k] >> (2 * tq0 + 2)) & m2, hm1, ha1, o3.x, o3.y);
-                            nib4_to_f16_one((qb[k] >> (2 * tq0 + 2)) & m2, hm1, ha1, o3.z, o3.w);
-                            *reinterpret_cast<uint4*>(b0 + tile_off(r, c)) = o0;
-                            *reinterpret_cast<uint4*>(b0 + kTile + tile_off(r, c)) = o1;
-                            *reinterpret_cast<uint4*>(b1 + tile_off(r, c)) = o2;
-                            *reinterpret_cast<uint4*>(b1 + kTile + tile_off(r, c)) = o3;
-                        }
+                        tc::tmem_st_wait();
+                        tc::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&sm.a_full[f]);
                     }
-                    tc::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tc::mbar_arrive(&sm.fullF[f0]);
-                        tc::mbar_arrive(&sm.fullF[f1]);
+                    if (!ok) break;
+                    if (h == 0) {
+                        if (!wwait(sm, &sm.c_empty[x], ((sbc / RX) & 1) ^ 1)) break;
+                        const float d = n < N ? __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk + 208)))
+                                              : 0.0f;
+                        sm.cvec[x][r] = d;
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&sm.c_full[x]);
                     }
                 }
                 __syncwarp();
-                if constexpr (!Q6) {
-                    if (lane == 0) tc::mbar_arrive(&sm.emptyB[rb.i]);
-                }
-                rb.next(RB);
+                if (lane == 0) tc::mbar_arrive(&sm.b_empty[b]);
             }
         }
-        if constexpr (Q6) tc::cp_async_wait<0>();   // no copy of this CTA is left in flight
+        if constexpr (Q6) {   // no bulk copy of this CTA is left in flight
+            if (h == 0 && aborted(sm))
+                for (int i = 0; i < kRB; ++i)
+                    if (issB >> i & 1u) tc::mbar_wait(&sm.b_full[i], phB >> i & 1u, kWaitLimitNs);
+        }
     } else {
         // ============================================================ epilogue
         tc::setmaxnreg_inc<kRegsEpi>();
         const int ew = warp - 4 - kConvWarps;
-        const int q = warp & 3;                 // TMEM lane quarter (warp % 4)
-        const int cq = ew >> 2;                 // column half: 64 * cq .. 64 * cq + 63
-        const int rloc = 32 * q + lane;
+        const int q = warp & 3, ch = ew >> 2;         // lane quarter, column half (96 tokens)
+        const int r = 32 * q + lane;
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
-        Ring rd, rt, rs, rm;
+        int sbc = 0;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of<Q6>(u, whole, splits, num_mt, S);
-            const bool add = Q6 ? (u >= whole && splits > 1) : (splits > 1);   // partial sums of a split tile
-            const int m0 = wk.m0, n0 = wk.n0;
-            const int m = m0 + rloc;
-            for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb) {
-                if (!wwait(sm, &sm.fullD[rd.i], rd.ph)) break;
-                float da[8];
-                {
-                    const float4* dp = reinterpret_cast<const float4*>(sm.draw[rd.i] + rloc * 32);
-                    const float4 x0 = dp[0], x1 = dp[1];
-                    da[0] = x0.x; da[1] = x0.y; da[2] = x0.z; da[3] = x0.w;
-                    da[4] = x1.x; da[5] = x1.y; da[6] = x1.z; da[7] = x1.w;
-                }
-                if constexpr (!Q6) {
-                    if (cq == 0) {
-                        // min-term activation operand, row rloc: K' = j (hi part of d_a,j * s_j), 8 + j (lo part)
-                        if (!wwait(sm, &sm.emptyM[rm.i], rm.ph ^ 1u)) break;
-                        const int4* sp = reinterpret_cast<const int4*>(sm.draw[rd.i] + kDRaw + rloc * 32);
-                        const int4 s0 = sp[0], s1 = sp[1];
-                        const int sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-                        float hi[8], lo[8];
+            const Work wk = work_of(u, splits, num_mt, S);
+            float acc[96];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float beta = da[j] * (float)sv[j];
-                            hi[j] = __uint_as_float(__float_as_uint(beta) & 0xFFFFE000u);
-                            lo[j] = beta - hi[j];
-                        }
-                        uint8_t* tile = sm.ms[rm.i];
-                        *reinterpret_cast<float4*>(tile + tile_off(rloc, 0)) = make_float4(hi[0], hi[1], hi[2], hi[3]);
-                        *reinterpret_cast<float4*>(tile + tile_off(rloc, 1)) = make_float4(hi[4], hi[5], hi[6], hi[7]);
-                        *reinterpret_cast<float4*>(tile + tile_off(rloc, 2)) = make_float4(lo[0], lo[1], lo[2], lo[3]);
-                        *reinterpret_cast<float4*>(tile + tile_off(rloc, 3)) = make_float4(lo[4], lo[5], lo[6], lo[7]);
-                        tc::fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&sm.fullM[rm.i]);
-                    }
-                    rm.next(RM);
+            for (int i = 0; i < 96; ++i) acc[i] = 0.0f;
+            bool ok = true;
+            for (int sb = wk.sb0; sb < wk.sb1; ++sb, ++sbc) {
+                const int s = sbc & 1, x = sbc % RX;
+                if (!wwait(sm, &sm.c_full[x], (sbc / RX) & 1) || !wwait(sm, &sm.ax_full[x], (sbc / RX) & 1) ||
+                    !wwait(sm, &sm.t_full[s], (sbc >> 1) & 1)) {
+                    ok = false;
+                    break;
                 }
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&sm.emptyD[rd.i]);
-                rd.next(RD);
-
-                // per 32-block: acc += d_a * I (exact integer block dot from the MMA)
-                float2 acc[32];
+                tc::tc_fence_after();
+                const float c = sm.cvec[x][r];
+                const uint32_t ta = tbase + lane_bits + (s ? kSCol1 : kSCol0) + 96 * ch;
 #pragma unroll
-                for (int c = 0; c < 32; ++c) acc[c] = make_float2(0.0f, 0.0f);
-                bool ok = true;
-#pragma unroll 1
-                for (int j = 0; j < 8; ++j) {
-                    if (!wwait(sm, &sm.tfull[rt.i], rt.ph)) { ok = false; break; }
-                    tc::tc_fence_after();
-                    uint32_t I0[32], I1[32];
-                    const uint32_t ta = tbase + lane_bits + kSlotCol0 + 128u * rt.i + 64u * cq;
-                    tc::tmem_ld32(ta, I0);
-                    tc::tmem_ld32(ta + 32, I1);
+                for (int cc = 0; cc < 3; ++cc) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(ta + 32 * cc, v);
                     tc::tmem_ld_wait();
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&sm.tempty[rt.i]);
-                    rt.next(RT);
-                    // d_a of block j picked by selects: a dynamically indexed array would live in local memory
-                    float dj = da[0];
+                    const float4* fp = reinterpret_cast<const float4*>(&sm.af[x][96 * ch + 32 * cc]);
 #pragma unroll
-                    for (int u = 1; u < 8; ++u) dj = (j == u) ? da[u] : dj;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        tc::ffma2(acc[c].x, acc[c].y, dj, dj, __uint_as_float(I0[2 * c]), __uint_as_float(I0[2 * c + 1]));
-                        tc::ffma2(acc[16 + c].x, acc[16 + c].y, dj, dj, __uint_as_float(I1[2 * c]), __uint_as_float(I1[2 * c + 1]));
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 f4 = fp[i];
+                        float g0, g1, g2, g3;
+                        tc::fmul2(g0, g1, c, c, f4.x, f4.y);
+                        tc::fmul2(g2, g3, c, c, f4.z, f4.w);
+                        float* a = &acc[32 * cc + 4 * i];
+                        tc::ffma2(a[0], a[1], g0, g1, __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]));
+                        tc::ffma2(a[2], a[3], g2, g3, __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
                     }
                 }
-                if (!ok) break;
-                // per super-block: out += d * acc (- dmin * MS for q4_K)
-                uint32_t ms_slot = 0;
-                if constexpr (!Q6) {
-                    if (!wwait(sm, &sm.tfull[rt.i], rt.ph)) break;
-                    tc::tc_fence_after();
-                    ms_slot = kSlotCol0 + 128u * rt.i;
-                }
-                if (!wwait(sm, &sm.fullS[rs.i], rs.ph)) break;
-                const bool first = (sb == wk.sb0), last = (sb == wk.sb1 - 1);
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const int col = 64 * cq + 16 * h;
-                    uint32_t o[16], mv[16];
-                    if (!first) tc::tmem_ld16(tbase + lane_bits + kOutCol + col, o);
-                    if constexpr (!Q6) tc::tmem_ld16(tbase + lane_bits + ms_slot + col, mv);
-                    tc::tmem_ld_wait();
-                    const float4* wdp = reinterpret_cast<const float4*>(&sm.wd[rs.i][col]);
-                    const float4* wmp = reinterpret_cast<const float4*>(&sm.wdmin[rs.i][col]);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float4 wv = wdp[u];
-                        const float w4[4] = {wv.x, wv.y, wv.z, wv.w};
-                        float m4v[4] = {0.f, 0.f, 0.f, 0.f};
-                        if constexpr (!Q6) {
-                            const float4 mm = wmp[u];
-                            m4v[0] = mm.x; m4v[1] = mm.y; m4v[2] = mm.z; m4v[3] = mm.w;
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int cc = 4 * u + e;                 // 0..15 within the chunk
-                            const int ai = 8 * h + (cc >> 1);         // float2 index in acc
-                            const float av = (cc & 1) ? acc[ai].y : acc[ai].x;
-                            float v = first ? 0.0f : __uint_as_float(o[cc]);
-                            v = fmaf(w4[e], av, v);
-                            if constexpr (!Q6) v = fmaf(-m4v[e], __uint_as_float(mv[cc]), v);
-                            o[cc] = __float_as_uint(v);               // the result overwrites the loaded value
-                        }
-                    }
-                    if (last) {
-                        if (m < M) {
-                            float* orow = out + (size_t)m * N + n0 + col;
-                            // split-K: partial sums are added into the zeroed output
-                            if (n0 + col + 16 <= N && (N & 3) == 0) {
-#pragma unroll
-                                for (int x = 0; x < 4; ++x) {
-                                    const float4 v4 = make_float4(__uint_as_float(o[4 * x]), __uint_as_float(o[4 * x + 1]),
-                                                                  __uint_as_float(o[4 * x + 2]), __uint_as_float(o[4 * x + 3]));
-                                    if (add) atomicAdd(reinterpret_cast<float4*>(orow) + x, v4);
-                                    else reinterpret_cast<float4*>(orow)[x] = v4;
-                                }
-                            } else {
-                                for (int x = 0; x < 16; ++x) {
-                                    if (n0 + col + x < N) {
-                                        if (add) atomicAdd(orow + x, __uint_as_float(o[x]));
-                                        else orow[x] = __uint_as_float(o[x]);
-                                    }
-                                }
-                            }
-                        }
-                    } else {
-                        tc::tmem_st16(tbase + lane_bits + kOutCol + col, o);
-                    }
-                }
-                tc::tmem_st_wait();
                 tc::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    tc::mbar_arrive(&sm.emptyS[rs.i]);
-                    if constexpr (!Q6) tc::mbar_arrive(&sm.tempty[rt.i]);
+                    tc::mbar_arrive(&sm.t_empty[s]);
+                    tc::mbar_arrive(&sm.ax_empty[x]);
+                    tc::mbar_arrive(&sm.c_empty[x]);
                 }
-                rs.next(RS);
-                if constexpr (!Q6) rt.next(RT);
+            }
+            if (!ok) break;
+            const int n = wk.n0 + r;
+            if (n < N) {
+                const int t0 = wk.m0 + 96 * ch;
+                float* op = out + (size_t)t0 * N + n;
+#pragma unroll
+                for (int i = 0; i < 96; ++i) {
+                    if (t0 + i < M) {
+                        if (splits > 1) atomicAdd(op + (size_t)i * N, acc[i]);
+                        else op[(size_t)i * N] = acc[i];
+                    }
+                }
             }
         }
     }
@@ -774,10 +655,9 @@ bool make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Split-K for the tiles of the last, partial wave (all tiles when there are fewer
-// than SMs): each such tile's super-blocks are divided among `splits` work units
-// (at least 2 super-blocks each), chosen to minimise the number of unit waves per
-// split plus a small per-split cost.
+// Split-K when there are fewer tiles than SMs: each tile's super-blocks are divided
+// among `splits` work units (at least 2 super-blocks each), chosen to minimise the
+// number of unit waves per split plus a small per-split cost.
 int choose_splits(long long tiles, int S, int sms) {
     if (tiles >= sms) return 1;
     int best = 1;
@@ -798,61 +678,68 @@ int check_gemm(const mq_q8_plane* a, const void* w, int N, const float* out) {
     if (N < 0 || a->M < 0 || !mq::valid_k(a->K)) return MQ_ERR_SHAPE;
     int rc = mq::check_plane(a, a->M, a->K);
     if (rc != MQ_OK || N == 0 || a->M == 0) return rc;
-    if (!a->qh || !w || !out) return MQ_ERR_NULL;
+    if (!mq::has_op(a) || !w || !out) return MQ_ERR_NULL;
     if (!mq::aligned16(w) || !mq::aligned16(out)) return MQ_ERR_ALIGN;
     return mq::check_arch();
+}
+
+// Once per device: the register split between warpgroups assumes the launch register
+// count, and the kernel's shared-memory size is set. Later calls make no attribute
+// calls, so a sequence of entry points can be captured in a graph.
+template <bool Q6>
+bool gemm_ready(size_t smem) {
+    constexpr int kMaxDevices = 64;
+    static int state[kMaxDevices];   // 0 unknown, 1 ready, 2 failed
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    int v = __atomic_load_n(&state[dev], __ATOMIC_ACQUIRE);
+    if (v == 0) {
+        std::lock_guard<std::mutex> lk(mu);
+        v = state[dev];
+        if (v == 0) {
+            cudaFuncAttributes fa;
+            v = (cudaFuncGetAttributes(&fa, gemm_kernel<Q6>) == cudaSuccess && fa.numRegs == kLaunchRegs &&
+                 cudaFuncSetAttribute(gemm_kernel<Q6>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+                     cudaSuccess)
+                    ? 1
+                    : 2;
+            __atomic_store_n(&state[dev], v, __ATOMIC_RELEASE);
+        }
+    }
+    return v == 1;
 }
 
 template <bool Q6>
 int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     int rc = check_gemm(a, w, N, out);
     if (rc != MQ_OK || N == 0 || a->M == 0) return rc;
-    const int M = a->M, K = a->K;
-    // Once per process: the register split between warpgroups assumes the launch
-    // register count, and the kernel's shared-memory size is set. Later calls make
-    // no attribute calls, so a sequence of entry points can be captured in a graph.
+    const int M = a->M, K = a->K, S = K / mq::QK_K;
     const size_t smem = sizeof(Smem<Q6>) + 1024;
-    static int ready = -1;
-    if (ready < 0) {
-        cudaFuncAttributes fa;
-        ready = (cudaFuncGetAttributes(&fa, gemm_kernel<Q6>) == cudaSuccess && fa.numRegs == kLaunchRegs &&
-                 cudaFuncSetAttribute(gemm_kernel<Q6>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
-                     cudaSuccess)
-                    ? 1
-                    : 0;
-    }
-    if (!ready) return MQ_ERR_LAUNCH;
-    const unsigned long long row = (unsigned long long)(K / mq::QK_K) * Cfg<Q6>::kSB;
-    CUtensorMap tmA, tmD, tmS, tmW;
+    if (!gemm_ready<Q6>(smem)) return MQ_ERR_LAUNCH;
+    const unsigned long long row = (unsigned long long)S * Cfg<Q6>::kSB;
+    CUtensorMap tmAct, tmAx, tmAf, tmW;
     if (Q6) {
-        tmW = CUtensorMap{};   // unused: q6_K rows are not 16-byte aligned for a tensor map
-    } else if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row, (uint64_t)N, row, mq::Q4K_BYTES, BN)) {
+        tmW = CUtensorMap{};   // unused: q6_K rows are 2-byte aligned; the converters stage them
+    } else if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row, (uint64_t)N, row, mq::Q4K_BYTES, BW)) {
         return MQ_ERR_LAUNCH;
     }
-    if (!make_map(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->qh, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 32, BM,
-                  CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->d, (uint64_t)K / 32, (uint64_t)M, (uint64_t)K / 8, 8, BM) ||
-        !make_map(&tmS, CU_TENSOR_MAP_DATA_TYPE_INT32, a->s, (uint64_t)K / 32, (uint64_t)M, (uint64_t)K / 8, 8, BM))
+    const int mp = mq::af_stride(M);
+    if (!make_map(&tmAct, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ah, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, KS, BT,
+                  CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tmAx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ax, (uint64_t)S * 16, (uint64_t)M, (uint64_t)S * 32, 16,
+                  BT, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map(&tmAf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->af, (uint64_t)mp, (uint64_t)S, (uint64_t)mp * 4, BT, 1))
         return MQ_ERR_LAUNCH;
-    const long long num_mt = (M + BM - 1) / BM, tiles = num_mt * ((N + BN - 1) / BN);
+    const long long tiles = (long long)((M + BT - 1) / BT) * ((N + BW - 1) / BW);
     const int sms = mq::num_sms();
-    // q6_K: full waves of whole tiles, and the tiles of the last, partial wave split along
-    // K. q4_K: split only when there are fewer tiles than SMs (then every tile is).
-    const long long whole = Q6 ? (tiles / sms) * sms : 0;
-    const int splits = tiles > whole ? choose_splits(tiles - whole, K / mq::QK_K, sms) : 1;
-    if (splits > 1) {
-        // The split tiles are the last ones in m-fastest order: they lie in the tile columns
-        // from the one holding tile `whole` on. Zero those columns (whole tiles among them
-        // overwrite the zeros with plain stores).
-        const size_t col0 = (size_t)(whole / num_mt) * BN;
-        if (cudaMemset2DAsync(out + col0, (size_t)N * sizeof(float), 0, ((size_t)N - col0) * sizeof(float),
-                              (size_t)M, stream) != cudaSuccess)
-            return MQ_ERR_LAUNCH;
-    }
-    const long long units = whole + (tiles - whole) * splits;
+    const int splits = choose_splits(tiles, S, sms);
+    if (splits > 1 && cudaMemsetAsync(out, 0, (size_t)M * N * sizeof(float), stream) != cudaSuccess)
+        return MQ_ERR_LAUNCH;
+    const long long units = tiles * splits;
     const int grid = (int)(units < sms ? units : sms);
-    gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmA, tmD, tmS, tmW, static_cast<const uint8_t*>(w), out, M, N, K,
-                                                      (int)whole, splits, row, row * (unsigned long long)N);
+    gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, static_cast<const uint8_t*>(w), out, M,
+                                                      N, K, splits, row, row * (unsigned long long)N);
     return mq::launch_status();
 }
 

@@ -311,23 +311,26 @@ int check_gemv(const mq_q8_plane* a, const void* w, int N, const float* out) {
     if (N < 0 || a->M != 1 || !mq::valid_k(a->K)) return MQ_ERR_SHAPE;
     int rc = mq::check_plane(a, a->M, a->K);
     if (rc != MQ_OK || N == 0) return rc;
-    if (!w || !out) return MQ_ERR_NULL;
+    if (!mq::has_q8(a) || !w || !out) return MQ_ERR_NULL;
     if (!mq::aligned16(w) || !mq::aligned16(out)) return MQ_ERR_ALIGN;
     return mq::check_arch();
 }
 
-// Persistent grid: as many blocks as are resident at once (queried once per
-// kernel), never more than there are rows for.
+// Persistent grid: as many blocks as are resident at once (queried once per kernel
+// and device), never more than there are rows for.
 template <typename Kern>
 int gemv_grid(int N, Kern kern) {
-    static int per_sm = 0;
-    if (per_sm == 0) {
-        int b = 0;
+    constexpr int kMaxDevices = 64;
+    static int per_sm[kMaxDevices];   // 0: not queried yet on that device
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = -1;
+    int b = dev >= 0 ? __atomic_load_n(&per_sm[dev], __ATOMIC_ACQUIRE) : 0;
+    if (b == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kThreads, 0) != cudaSuccess || b < 1) b = 1;
-        per_sm = b;
+        if (dev >= 0) __atomic_store_n(&per_sm[dev], b, __ATOMIC_RELEASE);
     }
     const long long need = ((long long)N + kRowsPerBlock - 1) / kRowsPerBlock;
-    const long long cap = (long long)mq::num_sms() * per_sm;
+    const long long cap = (long long)mq::num_sms() * b;
     return (int)(need < cap ? need : cap);
 }
 

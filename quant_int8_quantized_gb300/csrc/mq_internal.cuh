@@ -20,15 +20,27 @@ int check_arch();   // MQ_OK if the current device is compute capability 10.3
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+inline bool has_q8(const mq_q8_plane* p) { return p->qs || p->d || p->s; }
+inline bool has_op(const mq_q8_plane* p) { return p->ah || p->ax || p->af; }
+
+// Shape and pointers of a plane: each array group (q8: qs, d, s; operand: ah, ax, af)
+// is all present or all absent, at least one is present, and every array is 16-byte
+// aligned.
 inline int check_plane(const mq_q8_plane* p, int M, int K) {
     if (!p) return MQ_ERR_NULL;
     if (p->M != M || p->K != K) return MQ_ERR_SHAPE;
     if (M == 0) return MQ_OK;
-    if (!p->qs || !p->d || !p->s) return MQ_ERR_NULL;
-    if (!aligned16(p->qs) || !aligned16(p->d) || !aligned16(p->s)) return MQ_ERR_ALIGN;
-    if (p->qh && !aligned16(p->qh)) return MQ_ERR_ALIGN;
+    const bool q8 = has_q8(p), op = has_op(p);
+    if (!q8 && !op) return MQ_ERR_NULL;
+    if (q8 && (!p->qs || !p->d || !p->s)) return MQ_ERR_NULL;
+    if (op && (!p->ah || !p->ax || !p->af)) return MQ_ERR_NULL;
+    if (q8 && (!aligned16(p->qs) || !aligned16(p->d) || !aligned16(p->s))) return MQ_ERR_ALIGN;
+    if (op && (!aligned16(p->ah) || !aligned16(p->ax) || !aligned16(p->af))) return MQ_ERR_ALIGN;
     return MQ_OK;
 }
+
+// Row stride (elements) of the operand array af: M rounded up to a multiple of 4.
+inline int af_stride(int M) { return (M + 3) & ~3; }
 
 inline bool valid_k(int K) { return K > 0 && (K % QK_K) == 0; }
 
@@ -124,7 +136,7 @@ __device__ __forceinline__ int mq_rint_div(float v, float d, float inv) {
 // q = rint(v / d) with the correctly rounded quotient (see mq_rint_div).
 // Returns the packed int8 quants; d and s are valid in every lane of the group.
 __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v2, float v3,
-                                                     float& d_out, int& s_out, uint2& h_out) {
+                                                     float& d_out, int& s_out, int (&q)[4]) {
     float am = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
@@ -155,9 +167,10 @@ __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v
     s += __shfl_xor_sync(0xffffffffu, s, 1);
     d_out = d;
     s_out = s;
-    // the same four quants as binary16 (exact for |q| <= 127)
-    h_out.x = (uint32_t)__half_as_ushort(__int2half_rn(q0)) | ((uint32_t)__half_as_ushort(__int2half_rn(q1)) << 16);
-    h_out.y = (uint32_t)__half_as_ushort(__int2half_rn(q2)) | ((uint32_t)__half_as_ushort(__int2half_rn(q3)) << 16);
+    q[0] = q0;
+    q[1] = q1;
+    q[2] = q2;
+    q[3] = q3;
     return (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) | ((uint32_t)(q2 & 0xff) << 16) |
            ((uint32_t)(q3 & 0xff) << 24);
 }

@@ -8,36 +8,125 @@
 // and the qs store of a round are 512 B / 128 B coalesced warp accesses
 // ("55 · r52", §3.3 pitfall 2). No f32 intermediate is ever written.
 //
-// HBM roofline: quantize reads 4 B and writes 1.25 B per element; rms reads
-// 4 B (x) and writes 1.25 B; swiglu reads 8 B (g, u) and writes 1.25 B.
+// A plane may also carry the prefill GEMM's operand form (ah, ax, af; see mq.h).
+// It is derived per super-block of 256, i.e. per pair of rounds (2p, 2p+1), which
+// is why the kernels hand whole pairs to a warp: the super-block's largest block
+// scale is a warp-wide max, the block sums of ah are xor-shuffle sums (exact:
+// the values of one block are multiples of its smallest one's ulp and stay far
+// below 2^24 of it).
+//
+// HBM roofline per element: quantize reads 4 B, rms 4 B (x), swiglu 8 B (g, u);
+// the q8 arrays take 1.25 B, the operand arrays 2.25 B.
 
 #include "mq_internal.cuh"
 
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kRoundsPerIter = 4;   // float4 loads in flight per lane (inputs of a few rows: 1, more warps)
+constexpr int kRoundsPerIter = 4;   // float4 loads in flight per lane (inputs of a few rows: fewer, more warps)
 
-__device__ __forceinline__ void store_round(uint32_t* __restrict__ qs, float* __restrict__ d,
-                                            int32_t* __restrict__ s, uint2* __restrict__ qh, long long round,
-                                            int lane, uint32_t q, float dd, int ss, uint2 h) {
-    qs[round * 32 + lane] = q;
-    if (qh) qh[round * 32 + lane] = h;
+// Where a producer writes: the q8 arrays (qs == nullptr: absent) and the operand
+// arrays (ah == nullptr: absent). Plane arrays are flat: rows are contiguous and a
+// round (128 elements) never crosses a row, nor a pair of rounds a super-block.
+struct Out {
+    uint32_t* qs;
+    float* d;
+    int32_t* s;
+    uint2* ah;
+    uint16_t* ax;
+    float* af;
+    int kr;     // rounds per row (K / 128)
+    int mp;     // af row stride (M rounded up to a multiple of 4)
+};
+
+__device__ __forceinline__ void store_q8(const Out& o, long long round, int lane, uint32_t q, float dd, int ss) {
+    o.qs[round * 32 + lane] = q;
     if ((lane & 7) == 0) {
         const long long b = round * 4 + (lane >> 3);
-        d[b] = dd;
-        s[b] = ss;
+        o.d[b] = dd;
+        o.s[b] = ss;
     }
 }
 
-// x is viewed as a flat array of M*K floats (rows are contiguous, K % 128 == 0),
-// so every round lies inside one row and the plane arrays are flat too.
+// Quantize one round (q8 arrays only).
+__device__ __forceinline__ void quant_round(const Out& o, long long round, int lane, float v0, float v1, float v2,
+                                            float v3) {
+    float dd;
+    int ss, q[4];
+    const uint32_t pq = mq_quant4_group8(v0, v1, v2, v3, dd, ss, q);
+    store_q8(o, round, lane, pq, dd, ss);
+}
+
+// Quantize the two rounds of super-block `pair` (rounds 2 pair, 2 pair + 1) and write
+// every array group the plane holds. v[r] is this lane's float4 of round r.
+__device__ __forceinline__ void quant_pair(const Out& o, long long pair, int lane, const float4 (&v)[2]) {
+    float dd[2];
+    int ss[2], q[2][4];
+    uint32_t pq[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) pq[r] = mq_quant4_group8(v[r].x, v[r].y, v[r].z, v[r].w, dd[r], ss[r], q[r]);
+    const long long r0 = 2 * pair;
+    if (o.qs) {
+        store_q8(o, r0, lane, pq[0], dd[0], ss[0]);
+        store_q8(o, r0 + 1, lane, pq[1], dd[1], ss[1]);
+    }
+    if (o.ah) {
+        // e from the super-block's largest block scale D (a max, exact in any order):
+        // D = f 2^E with f in [1/2, 1), e = 3 - E clamped to [-126, 126], e = 0 for D = 0.
+        float D = fmaxf(dd[0], dd[1]);
+        D = fmaxf(D, __shfl_xor_sync(0xffffffffu, D, 8));
+        D = fmaxf(D, __shfl_xor_sync(0xffffffffu, D, 16));
+        int e = 0;
+        if (D != 0.0f) {
+            int E;
+            frexpf(D, &E);
+            e = min(126, max(-126, 3 - E));
+        }
+        const float scale = __int_as_float((e + 127) << 23);      // 2^e, exact
+        float sig[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            unsigned short h[4];
+            float part = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half hv = __float2half_rn(__fmul_rn(__fmul_rn(dd[r], (float)q[r][i]), scale));
+                h[i] = __half_as_ushort(hv);
+                part = __fadd_rn(part, __half2float(hv));
+            }
+            o.ah[(r0 + r) * 32 + lane] = make_uint2((uint32_t)h[0] | ((uint32_t)h[1] << 16),
+                                                    (uint32_t)h[2] | ((uint32_t)h[3] << 16));
+            part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 4));
+            part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 2));
+            part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
+            sig[r] = part;
+        }
+        if ((lane & 7) == 0) {   // block j = 4r + lane/8 of the super-block: slots j (hi), 8 + j (lo)
+            uint16_t* rec = o.ax + pair * 16;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const __half hi = __float2half_rn(sig[r]);
+                const __half lo = __float2half_rn(__fsub_rn(sig[r], __half2float(hi)));
+                const int j = 4 * r + (lane >> 3);
+                rec[j] = __half_as_ushort(hi);
+                rec[8 + j] = __half_as_ushort(lo);
+            }
+        }
+        if (lane == 0) {
+            const int spr = o.kr >> 1;                                 // super-blocks per row
+            const long long row = pair / spr;
+            const int t = (int)(pair - row * spr);
+            o.af[(long long)t * o.mp + row] = __int_as_float((127 - e) << 23);   // 2^-e
+        }
+    }
+}
+
+// x is viewed as a flat array of M*K floats (rows are contiguous, K % 256 == 0).
+// R rounds per warp and iteration; R >= 2 is even, so every pair of rounds is one
+// super-block (required when the plane holds the operand form). R == 1 writes the q8
+// arrays only.
 template <int R>
-__global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __restrict__ x,
-                                                               uint32_t* __restrict__ qs,
-                                                               float* __restrict__ d,
-                                                               int32_t* __restrict__ s,
-                                                               uint2* __restrict__ qh, long long rounds) {
+__global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __restrict__ x, Out o, long long rounds) {
     mq_grid_release();
     mq_grid_wait();
     const int lane = threadIdx.x & 31;
@@ -48,14 +137,15 @@ __global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __r
 #pragma unroll
         for (int u = 0; u < R; ++u)
             if (r0 + u < rounds) v[u] = __ldcs(x + (r0 + u) * 32 + lane);
+        if constexpr (R == 1) {
+            quant_round(o, r0, lane, v[0].x, v[0].y, v[0].z, v[0].w);
+        } else {
 #pragma unroll
-        for (int u = 0; u < R; ++u) {
-            if (r0 + u < rounds) {   // warp-uniform
-                float dd;
-                int ss;
-                uint2 h;
-                const uint32_t q = mq_quant4_group8(v[u].x, v[u].y, v[u].z, v[u].w, dd, ss, h);
-                store_round(qs, d, s, qh, r0 + u, lane, q, dd, ss, h);
+            for (int u = 0; u < R; u += 2) {
+                if (r0 + u < rounds) {   // warp-uniform; rounds is even, so the pair is whole
+                    const float4 pv[2] = {v[u], v[u + 1]};
+                    quant_pair(o, (r0 + u) >> 1, lane, pv);
+                }
             }
         }
     }
@@ -94,13 +184,14 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, exp_cw(-g))), u);
 }
 
+__device__ __forceinline__ float4 silu_mul4(float4 g, float4 u) {
+    return make_float4(silu_mul(g.x, u.x), silu_mul(g.y, u.y), silu_mul(g.z, u.z), silu_mul(g.w, u.w));
+}
+
 template <int R>
 __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __restrict__ g,
-                                                                const float4* __restrict__ u,
-                                                                uint32_t* __restrict__ qs,
-                                                                float* __restrict__ d,
-                                                                int32_t* __restrict__ s,
-                                                                uint2* __restrict__ qh, long long rounds) {
+                                                                const float4* __restrict__ u, Out o,
+                                                                long long rounds) {
     mq_grid_release();
     mq_grid_wait();
     const int lane = threadIdx.x & 31;
@@ -115,16 +206,16 @@ __global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __
                 uv[k] = __ldcs(u + (r0 + k) * 32 + lane);
             }
         }
+        if constexpr (R == 1) {
+            const float4 v = silu_mul4(gv[0], uv[0]);
+            quant_round(o, r0, lane, v.x, v.y, v.z, v.w);
+        } else {
 #pragma unroll
-        for (int k = 0; k < R; ++k) {
-            if (r0 + k < rounds) {
-                float dd;
-                int ss;
-                uint2 h;
-                const uint32_t q = mq_quant4_group8(silu_mul(gv[k].x, uv[k].x), silu_mul(gv[k].y, uv[k].y),
-                                                    silu_mul(gv[k].z, uv[k].z), silu_mul(gv[k].w, uv[k].w),
-                                                    dd, ss, h);
-                store_round(qs, d, s, qh, r0 + k, lane, q, dd, ss, h);
+            for (int k = 0; k < R; k += 2) {
+                if (r0 + k < rounds) {
+                    const float4 pv[2] = {silu_mul4(gv[k], uv[k]), silu_mul4(gv[k + 1], uv[k + 1])};
+                    quant_pair(o, (r0 + k) >> 1, lane, pv);
+                }
             }
         }
     }
@@ -154,59 +245,58 @@ __device__ __forceinline__ float rms_scale_warp(const float4* __restrict__ xr, i
     return rms_scale_finish(ss, K, eps);
 }
 
-__device__ __forceinline__ void rms_quant_one(float4 xv, float4 wv, float scale, uint32_t* __restrict__ qs,
-                                              float* __restrict__ d, int32_t* __restrict__ s,
-                                              uint2* __restrict__ qh, long long round, int lane) {
-    float dd;
-    int ss;
-    uint2 h;
-    const uint32_t q = mq_quant4_group8(__fmul_rn(__fmul_rn(xv.x, scale), wv.x), __fmul_rn(__fmul_rn(xv.y, scale), wv.y),
-                                        __fmul_rn(__fmul_rn(xv.z, scale), wv.z), __fmul_rn(__fmul_rn(xv.w, scale), wv.w),
-                                        dd, ss, h);
-    store_round(qs, d, s, qh, round, lane, q, dd, ss, h);
+__device__ __forceinline__ float4 rms_apply(float4 xv, float4 wv, float scale) {
+    return make_float4(__fmul_rn(__fmul_rn(xv.x, scale), wv.x), __fmul_rn(__fmul_rn(xv.y, scale), wv.y),
+                       __fmul_rn(__fmul_rn(xv.z, scale), wv.z), __fmul_rn(__fmul_rn(xv.w, scale), wv.w));
 }
 
-// Rows of at most 32 * kRegRoundsMax rounds (K <= 16384): one block per row, round
-// r held in registers by warp r % nw (at most kRegRounds rounds a warp), all of
-// a row's loads in flight at once.
+// Rows of at most 64 * kRegPairsMax rounds (K <= 16384): one block per row; pair p
+// (rounds 2p, 2p+1) is held in registers by warp p % nw, at most kRegPairs pairs a
+// warp, all of a row's loads in flight at once.
 // Each lane leaves the sum of squares of its float4 of each round in shared
 // memory; warp 0 adds them per lane in round order — the same sequence as
 // rms_scale_warp — and the scale goes through shared memory. The row is read
 // from HBM once ("72 · D3-7", Excerpt C: a wide block per decode row).
-constexpr int kRegRoundsMax = 4;
+constexpr int kRegPairsMax = 2;
 
-template <bool kPrefetchW, int kRegRounds>
+template <bool kPrefetchW, int kRegPairs>
 __global__ void __launch_bounds__(1024) rms_quant_staged_kernel(const float4* __restrict__ x,
-                                                                const float4* __restrict__ w4,
-                                                                uint32_t* __restrict__ qs,
-                                                                float* __restrict__ d,
-                                                                int32_t* __restrict__ s,
-                                                                uint2* __restrict__ qh, int K, float eps) {
+                                                                const float4* __restrict__ w4, Out o, int K,
+                                                                float eps) {
     mq_grid_release();
     mq_grid_wait();
     extern __shared__ float s_sq[];   // [rounds][32]
     __shared__ float s_scale;
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int nrounds = K >> 7;
+    const int nrounds = K >> 7, npairs = nrounds >> 1;
     const float4* xr = x + (long long)blockIdx.x * (K >> 2);
-    float4 xv[kRegRounds];
+    float4 xv[kRegPairs][2];
 #pragma unroll
-    for (int i = 0; i < kRegRounds; ++i) {
-        const int r = wid + i * nw;
-        if (r < nrounds) xv[i] = __ldcs(xr + r * 32 + lane);
+    for (int i = 0; i < kRegPairs; ++i) {
+        const int p = wid + i * nw;
+        if (p < npairs) {
+            xv[i][0] = __ldcs(xr + (2 * p) * 32 + lane);
+            xv[i][1] = __ldcs(xr + (2 * p + 1) * 32 + lane);
+        }
     }
 #pragma unroll
-    for (int i = 0; i < kRegRounds; ++i) {
-        const int r = wid + i * nw;
-        if (r < nrounds) s_sq[r * 32 + lane] = sum_sq4(xv[i]);
+    for (int i = 0; i < kRegPairs; ++i) {
+        const int p = wid + i * nw;
+        if (p < npairs) {
+            s_sq[(2 * p) * 32 + lane] = sum_sq4(xv[i][0]);
+            s_sq[(2 * p + 1) * 32 + lane] = sum_sq4(xv[i][1]);
+        }
     }
-    float4 wv[kRegRounds];   // for a few rows the weight row is fetched while warp 0 computes the scale
+    float4 wv[kRegPairs][2];   // for a few rows the weight row is fetched while warp 0 computes the scale
     if constexpr (kPrefetchW) {
 #pragma unroll
-        for (int i = 0; i < kRegRounds; ++i) {
-            const int r = wid + i * nw;
-            if (r < nrounds) wv[i] = __ldg(w4 + r * 32 + lane);
+        for (int i = 0; i < kRegPairs; ++i) {
+            const int p = wid + i * nw;
+            if (p < npairs) {
+                wv[i][0] = __ldg(w4 + (2 * p) * 32 + lane);
+                wv[i][1] = __ldg(w4 + (2 * p + 1) * 32 + lane);
+            }
         }
     }
     __syncthreads();
@@ -219,50 +309,59 @@ __global__ void __launch_bounds__(1024) rms_quant_staged_kernel(const float4* __
     }
     __syncthreads();
     const float scale = s_scale;
-    const long long round0 = (long long)blockIdx.x * nrounds;
+    const long long pair0 = (long long)blockIdx.x * npairs;
 #pragma unroll
-    for (int i = 0; i < kRegRounds; ++i) {
-        const int r = wid + i * nw;
-        if (r < nrounds)
-            rms_quant_one(xv[i], kPrefetchW ? wv[i] : __ldg(w4 + r * 32 + lane), scale, qs, d, s, qh, round0 + r, lane);
+    for (int i = 0; i < kRegPairs; ++i) {
+        const int p = wid + i * nw;
+        if (p < npairs) {
+            const float4 w0 = kPrefetchW ? wv[i][0] : __ldg(w4 + (2 * p) * 32 + lane);
+            const float4 w1 = kPrefetchW ? wv[i][1] : __ldg(w4 + (2 * p + 1) * 32 + lane);
+            const float4 pv[2] = {rms_apply(xv[i][0], w0, scale), rms_apply(xv[i][1], w1, scale)};
+            quant_pair(o, pair0 + p, lane, pv);
+        }
     }
 }
 
-// Longer rows: one block per row with one warp per round (at most 32 warps, or 4
-// when there are many rows; more rounds wrap around). Every warp loads its first
-// round while warp 0 computes the scale with rms_scale_warp (the row is read
-// twice, the second time mostly from cache).
+// Longer rows: one block per row with one warp per pair of rounds (at most 32 warps,
+// or 4 when there are many rows; more pairs wrap around). Every warp loads its first
+// pair while warp 0 computes the scale with rms_scale_warp (the row is read twice,
+// the second time mostly from cache).
 __global__ void __launch_bounds__(1024) rms_quant_wide_kernel(const float4* __restrict__ x,
-                                                              const float4* __restrict__ w4,
-                                                              uint32_t* __restrict__ qs,
-                                                              float* __restrict__ d,
-                                                              int32_t* __restrict__ s,
-                                                              uint2* __restrict__ qh, int K, float eps) {
+                                                              const float4* __restrict__ w4, Out o, int K,
+                                                              float eps) {
     mq_grid_release();
     mq_grid_wait();
     __shared__ float s_scale;
     const int lane = threadIdx.x & 31;
     const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int nrounds = K >> 7;
+    const int npairs = K >> 8;
     const float4* xr = x + (long long)blockIdx.x * (K >> 2);
-    const float4 x0 = mq_ld_dep(xr + wid * 32 + lane);   // wid < nrounds by construction of the launch
-    const float4 w0 = __ldg(w4 + wid * 32 + lane);
+    // wid < npairs by construction of the launch
+    const float4 x0 = mq_ld_dep(xr + (2 * wid) * 32 + lane), x1 = mq_ld_dep(xr + (2 * wid + 1) * 32 + lane);
+    const float4 w0 = __ldg(w4 + (2 * wid) * 32 + lane), w1 = __ldg(w4 + (2 * wid + 1) * 32 + lane);
     if (wid == 0) {
         const float sc = rms_scale_warp(xr, K, eps, lane);
         if (lane == 0) s_scale = sc;
     }
     __syncthreads();
     const float scale = s_scale;
-    const long long round0 = (long long)blockIdx.x * nrounds;
-    rms_quant_one(x0, w0, scale, qs, d, s, qh, round0 + wid, lane);
+    const long long pair0 = (long long)blockIdx.x * npairs;
+    {
+        const float4 pv[2] = {rms_apply(x0, w0, scale), rms_apply(x1, w1, scale)};
+        quant_pair(o, pair0 + wid, lane, pv);
+    }
 #pragma unroll 2
-    for (int k = wid + nw; k < nrounds; k += nw)
-        rms_quant_one(mq_ld_dep(xr + k * 32 + lane), __ldg(w4 + k * 32 + lane), scale, qs, d, s, qh, round0 + k, lane);
+    for (int p = wid + nw; p < npairs; p += nw) {
+        const float4 pv[2] = {rms_apply(mq_ld_dep(xr + (2 * p) * 32 + lane), __ldg(w4 + (2 * p) * 32 + lane), scale),
+                              rms_apply(mq_ld_dep(xr + (2 * p + 1) * 32 + lane), __ldg(w4 + (2 * p + 1) * 32 + lane),
+                                        scale)};
+        quant_pair(o, pair0 + p, lane, pv);
+    }
 }
 
 // Inputs that would not give every SM two blocks at four rounds a warp (decode
-// rows) are spread one round per warp: the rounds' latencies then overlap across
-// warps instead of queueing inside one.
+// rows) are spread one round per warp (two when the operand form is written): the
+// rounds' latencies then overlap across warps instead of queueing inside one.
 bool few_rounds(long long rounds) { return rounds < 2LL * mq::num_sms() * (kThreads / 32) * kRoundsPerIter; }
 
 int flat_grid(long long rounds, int rounds_per_iter) {
@@ -283,17 +382,27 @@ int check_producer(const void* a, const void* b, int M, int K, const mq_q8_plane
     return mq::check_arch();
 }
 
+Out out_of(const mq_q8_plane* p) {
+    return Out{reinterpret_cast<uint32_t*>(p->qs), p->d, p->s, reinterpret_cast<uint2*>(p->ah), p->ax, p->af,
+               p->K / 128, mq::af_stride(p->M)};
+}
+
+// Rounds per warp and iteration of the flat kernels.
+int flat_rounds(long long rounds, const mq_q8_plane* out) {
+    if (!few_rounds(rounds)) return kRoundsPerIter;
+    return mq::has_op(out) ? 2 : 1;
+}
+
 }  // namespace
 
 extern "C" int mq_quantize_q8(const float* x, int M, int K, const mq_q8_plane* out, cudaStream_t stream) {
     int rc = check_producer(x, x, M, K, out);
     if (rc != MQ_OK || M == 0) return rc;
     const long long rounds = (long long)M * K / 128;
-    const bool few = few_rounds(rounds);
-    return mq::launch_pdl(few ? quantize_q8_kernel<1> : quantize_q8_kernel<kRoundsPerIter>,
-                          dim3(flat_grid(rounds, few ? 1 : kRoundsPerIter)), dim3(kThreads), 0, stream,
-                          reinterpret_cast<const float4*>(x), reinterpret_cast<uint32_t*>(out->qs), out->d, out->s,
-                          reinterpret_cast<uint2*>(out->qh), rounds);
+    const int R = flat_rounds(rounds, out);
+    auto kern = R == 1 ? quantize_q8_kernel<1> : R == 2 ? quantize_q8_kernel<2> : quantize_q8_kernel<kRoundsPerIter>;
+    return mq::launch_pdl(kern, dim3(flat_grid(rounds, R)), dim3(kThreads), 0, stream,
+                          reinterpret_cast<const float4*>(x), out_of(out), rounds);
 }
 
 extern "C" int mq_swiglu_quant(const float* g, const float* u, int M, int K, const mq_q8_plane* out,
@@ -301,12 +410,10 @@ extern "C" int mq_swiglu_quant(const float* g, const float* u, int M, int K, con
     int rc = check_producer(g, u, M, K, out);
     if (rc != MQ_OK || M == 0) return rc;
     const long long rounds = (long long)M * K / 128;
-    const bool few = few_rounds(rounds);
-    return mq::launch_pdl(few ? swiglu_quant_kernel<1> : swiglu_quant_kernel<kRoundsPerIter>,
-                          dim3(flat_grid(rounds, few ? 1 : kRoundsPerIter)), dim3(kThreads), 0, stream,
-                          reinterpret_cast<const float4*>(g), reinterpret_cast<const float4*>(u),
-                          reinterpret_cast<uint32_t*>(out->qs), out->d, out->s, reinterpret_cast<uint2*>(out->qh),
-                          rounds);
+    const int R = flat_rounds(rounds, out);
+    auto kern = R == 1 ? swiglu_quant_kernel<1> : R == 2 ? swiglu_quant_kernel<2> : swiglu_quant_kernel<kRoundsPerIter>;
+    return mq::launch_pdl(kern, dim3(flat_grid(rounds, R)), dim3(kThreads), 0, stream,
+                          reinterpret_cast<const float4*>(g), reinterpret_cast<const float4*>(u), out_of(out), rounds);
 }
 
 extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float eps, const mq_q8_plane* out,
@@ -315,29 +422,26 @@ extern "C" int mq_rms_quant(const float* x, const float* w, int M, int K, float 
     if (rc != MQ_OK || M == 0) return rc;
     const float4* x4 = reinterpret_cast<const float4*>(x);
     const float4* w4 = reinterpret_cast<const float4*>(w);
-    uint32_t* qs = reinterpret_cast<uint32_t*>(out->qs);
-    uint2* qh = reinterpret_cast<uint2*>(out->qh);
-    // One block per row. Rows of up to 128 rounds are read once into registers: one warp
-    // per round for a few rows (decode); two rounds a warp (four for rows over 64 rounds)
-    // once there are enough rows to fill the machine. Longer rows take the kernel that
-    // reads them twice.
-    const int rounds = K / 128;
+    const Out o = out_of(out);
+    // One block per row. Rows of up to 64 pairs of rounds are read once into registers:
+    // one warp per pair for a few rows (decode) and for rows of up to 32 pairs; two pairs
+    // a warp for longer rows when there are enough rows to fill the machine. Longer rows
+    // take the kernel that reads them twice.
+    const int rounds = K / 128, pairs = rounds / 2;
     const bool many = M >= 4 * mq::num_sms();
-    if (rounds <= 32 * kRegRoundsMax) {
+    if (pairs <= 32 * kRegPairsMax) {
         const size_t smem = (size_t)rounds * 32 * sizeof(float);
         if (!many)
-            return mq::launch_pdl(rms_quant_staged_kernel<true, kRegRoundsMax>, dim3(M),
-                                  dim3(32 * (rounds < 32 ? rounds : 32)), smem, stream, x4, w4, qs, out->d, out->s, qh,
-                                  K, eps);
-        if (rounds <= 64)   // two rounds a warp (measured faster than four at 3314 x 3584)
-            return mq::launch_pdl(rms_quant_staged_kernel<false, 2>, dim3(M), dim3(32 * ((rounds + 1) / 2)), smem,
-                                  stream, x4, w4, qs, out->d, out->s, qh, K, eps);
-        return mq::launch_pdl(rms_quant_staged_kernel<false, kRegRoundsMax>, dim3(M),
-                              dim3(32 * ((rounds + kRegRoundsMax - 1) / kRegRoundsMax)), smem, stream, x4, w4, qs, out->d,
-                              out->s, qh, K, eps);
+            return mq::launch_pdl(rms_quant_staged_kernel<true, kRegPairsMax>, dim3(M),
+                                  dim3(32 * (pairs < 32 ? pairs : 32)), smem, stream, x4, w4, o, K, eps);
+        if (pairs <= 32)   // one pair (two rounds) a warp: measured fastest at 3314 x 3584
+            return mq::launch_pdl(rms_quant_staged_kernel<false, 1>, dim3(M), dim3(32 * pairs), smem, stream, x4,
+                                  w4, o, K, eps);
+        return mq::launch_pdl(rms_quant_staged_kernel<false, kRegPairsMax>, dim3(M),
+                              dim3(32 * ((pairs + kRegPairsMax - 1) / kRegPairsMax)), smem, stream, x4, w4, o, K,
+                              eps);
     }
     const int cap = many ? 4 : 32;
-    const int warps = rounds < cap ? rounds : cap;
-    return mq::launch_pdl(rms_quant_wide_kernel, dim3(M), dim3(32 * warps), 0, stream, x4, w4, qs, out->d, out->s, qh,
-                          K, eps);
+    const int warps = pairs < cap ? pairs : cap;
+    return mq::launch_pdl(rms_quant_wide_kernel, dim3(M), dim3(32 * warps), 0, stream, x4, w4, o, K, eps);
 }

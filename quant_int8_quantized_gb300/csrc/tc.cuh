@@ -135,6 +135,30 @@ __device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t sbo)
     return d;
 }
 
+// Shared-memory matrix descriptor, K-major with a 128- or 32-byte swizzle, as TMA
+// writes it with CU_TENSOR_MAP_SWIZZLE_128B / _32B: rows of 128 (32) bytes in 8-row
+// atoms of 1024 (256) bytes; `sbo` = the atom size for densely packed atoms. The tile
+// base must be aligned to the atom; a K offset inside the row is added to the start
+// address.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;                       // layout type: 128-byte swizzle
+    return d;
+}
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(256 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)6 << 61;                       // layout type: 32-byte swizzle
+    return d;
+}
+
 // Instruction descriptor: f32 accumulator, both operands K-major.
 // ab_format: 0 = f16, 1 = bf16 (kind::f16); 2 = tf32 (kind::tf32).
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t M, uint32_t N, uint32_t ab_format) {
@@ -151,6 +175,17 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
             d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// A operand in tensor memory (M rows in lanes, K packed two f16 per 32-bit column:
+// K = 16 takes 8 columns), B from shared memory.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -188,6 +223,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+// 32 lanes x 32 consecutive columns: thread i writes lane (base lane + i).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ----------------------------------------------------------------- TMA / bulk copies
@@ -199,6 +247,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
             smem_u32(dst)),
         "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
+}
+
+// 1-D bulk copy global -> shared (both addresses 16-byte aligned, bytes a multiple of
+// 16), completion counted on `bar` (bytes).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 // Per-thread asynchronous 16-byte copy global -> shared (both 16-byte aligned).
@@ -238,6 +295,17 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Packed f32x2 multiply: (d0, d1) = (a0, a1) * (b0, b1).
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{ .reg .b64 ra, rb, rc;\n"
+        "  mov.b64 ra, {%2, %3};\n"
+        "  mov.b64 rb, {%4, %5};\n"
+        "  mul.rn.f32x2 rc, ra, rb;\n"
+        "  mov.b64 {%0, %1}, rc; }"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // Packed f32x2 fused multiply-add on register pairs: (d0, d1) += (a0, a1) * (b0, b1).

@@ -31,7 +31,8 @@ class MQError(RuntimeError):
 
 class CPlane(ctypes.Structure):
     _fields_ = [("qs", ctypes.c_void_p), ("d", ctypes.c_void_p), ("s", ctypes.c_void_p),
-                ("qh", ctypes.c_void_p), ("M", ctypes.c_int), ("K", ctypes.c_int)]
+                ("ah", ctypes.c_void_p), ("ax", ctypes.c_void_p), ("af", ctypes.c_void_p),
+                ("M", ctypes.c_int), ("K", ctypes.c_int)]
 
 
 _lib = None
@@ -48,7 +49,7 @@ def lib() -> ctypes.CDLL:
         pp = ctypes.POINTER(CPlane)
         psz = ctypes.POINTER(ctypes.c_size_t)
         sig = {
-            "mq_plane_bytes": (sz, [i, i, psz, psz, psz]),
+            "mq_plane_bytes": (sz, [i, i, psz, psz, psz, psz, psz, psz]),
             "mq_q4k_row_bytes": (sz, [i]),
             "mq_q6k_row_bytes": (sz, [i]),
             "mq_quantize_q8": (i, [vp, i, i, pp, vp]),
@@ -101,35 +102,56 @@ def _dev_tensor(t, dtype, name):
 
 
 class Plane:
-    """Device q8 plane: qs int8 [M, K], d f32 [M, K/32], s int32 [M, K/32], and
-    optionally qh f16 [M, K] (the same quants in the tensor-core operand form,
-    required by the GEMM)."""
+    """Device activation plane (include/mq.h): the q8 arrays qs int8 [M, K],
+    d f32 [M, K/32], s int32 [M, K/32] (read by the GEMV), and/or the GEMM's
+    operand arrays ah f16 [M, K], ax f16 [M, K/256, 16], af f32 [K/256, Mp]
+    with Mp = M rounded up to a multiple of 4. Producers fill whichever groups
+    are present."""
 
-    def __init__(self, qs: torch.Tensor, d: torch.Tensor, s: torch.Tensor, qh: torch.Tensor = None):
-        self.qs, self.d, self.s, self.qh = qs, d, s, qh
-        self.M, self.K = int(qs.shape[0]), int(qs.shape[1])
-        _dev_tensor(qs, torch.int8, "plane.qs")
-        _dev_tensor(d, torch.float32, "plane.d")
-        _dev_tensor(s, torch.int32, "plane.s")
-        if qh is not None:
-            _dev_tensor(qh, torch.float16, "plane.qh")
+    def __init__(self, qs=None, d=None, s=None, ah=None, ax=None, af=None, M=None, K=None):
+        self.qs, self.d, self.s, self.ah, self.ax, self.af = qs, d, s, ah, ax, af
+        ref = qs if qs is not None else ah
+        if ref is None:
+            raise ValueError("a plane needs its q8 arrays, its operand arrays, or both")
+        self.M, self.K = int(ref.shape[0]), int(ref.shape[1])
+        if qs is not None:
+            _dev_tensor(qs, torch.int8, "plane.qs")
+            _dev_tensor(d, torch.float32, "plane.d")
+            _dev_tensor(s, torch.int32, "plane.s")
+        if ah is not None:
+            _dev_tensor(ah, torch.float16, "plane.ah")
+            _dev_tensor(ax, torch.float16, "plane.ax")
+            _dev_tensor(af, torch.float32, "plane.af")
+
+    @staticmethod
+    def af_stride(M: int) -> int:
+        return (M + 3) // 4 * 4
 
     @classmethod
-    def empty(cls, M: int, K: int, device="cuda", f16: bool = True) -> "Plane":
-        return cls(torch.empty((M, K), dtype=torch.int8, device=device),
-                   torch.empty((M, K // 32), dtype=torch.float32, device=device),
-                   torch.empty((M, K // 32), dtype=torch.int32, device=device),
-                   torch.empty((M, K), dtype=torch.float16, device=device) if f16 else None)
+    def empty(cls, M: int, K: int, device="cuda", q8: bool = True, op: bool = True) -> "Plane":
+        """Allocate a plane with the q8 arrays (q8=True) and/or the operand arrays (op=True)."""
+        kw = {}
+        if q8:
+            kw.update(qs=torch.empty((M, K), dtype=torch.int8, device=device),
+                      d=torch.empty((M, K // 32), dtype=torch.float32, device=device),
+                      s=torch.empty((M, K // 32), dtype=torch.int32, device=device))
+        if op:
+            kw.update(ah=torch.empty((M, K), dtype=torch.float16, device=device),
+                      ax=torch.empty((M, K // 256, 16), dtype=torch.float16, device=device),
+                      af=torch.empty((K // 256, cls.af_stride(M)), dtype=torch.float32, device=device))
+        return cls(**kw)
 
     def c(self) -> CPlane:
-        return CPlane(self.qs.data_ptr(), self.d.data_ptr(), self.s.data_ptr(),
-                      self.qh.data_ptr() if self.qh is not None else None, self.M, self.K)
+        def p(t):
+            return t.data_ptr() if t is not None else None
+        return CPlane(p(self.qs), p(self.d), p(self.s), p(self.ah), p(self.ax), p(self.af), self.M, self.K)
 
 
 def mq_plane_bytes(M: int, K: int):
-    a, b, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
-    tot = lib().mq_plane_bytes(M, K, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
-    return int(tot), int(a.value), int(b.value), int(c.value)
+    """(total, qs, d, s, ah, ax, af) bytes of an M x K plane."""
+    v = [ctypes.c_size_t() for _ in range(6)]
+    tot = lib().mq_plane_bytes(M, K, *[ctypes.byref(x) for x in v])
+    return (int(tot),) + tuple(int(x.value) for x in v)
 
 
 def mq_q4k_row_bytes(K: int) -> int:

@@ -21,47 +21,80 @@ def require_gpu():
 class Guarded:
     """A device tensor carved out of a larger poisoned byte buffer.
 
-    Every byte of the buffer starts as 0xCD; `check()` asserts that the guard
-    bands before and after the tensor are untouched (no out-of-bounds write),
-    and `untouched()` counts tensor bytes still equal to the poison (no write).
+    Every byte of the buffer starts as the poison (0xCD; 0xFF for binary16
+    tensors, whose 0xCDCD is an ordinary value but 0xFFFF a NaN the kernels never
+    write); `check()` asserts that the guard bands before and after the tensor
+    are untouched (no out-of-bounds write), and `untouched()` counts 4-byte words
+    of the tensor still equal to the poison (no write).
     """
 
     def __init__(self, shape, dtype, device="cuda"):
         n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
         self.nbytes = n
-        self.raw = torch.full((n + 2 * GUARD,), POISON, dtype=torch.uint8, device=device)
+        self.poison = 0xFF if dtype == torch.float16 else POISON
+        self.raw = torch.full((n + 2 * GUARD,), self.poison, dtype=torch.uint8, device=device)
         self.t = self.raw[GUARD:GUARD + n].view(dtype).view(shape) if n else torch.empty(shape, dtype=dtype, device=device)
 
     def check(self):
         raw = self.raw.cpu().numpy()
-        assert np.all(raw[:GUARD] == POISON), "write before the buffer"
-        assert np.all(raw[GUARD + self.nbytes:] == POISON), "write after the buffer"
+        assert np.all(raw[:GUARD] == self.poison), "write before the buffer"
+        assert np.all(raw[GUARD + self.nbytes:] == self.poison), "write after the buffer"
 
     def untouched(self):
         """Number of 4-byte words of the tensor still equal to the poison (never written).
         For f32 outputs the poison word is -4.3e8, not a value these kernels produce."""
         words = self.raw[GUARD:GUARD + self.nbytes - self.nbytes % 4].view(torch.int32)
-        poison = int(np.frombuffer(bytes([POISON] * 4), np.int32)[0])
+        poison = int(np.frombuffer(bytes([self.poison] * 4), np.int32)[0])
         return int((words == poison).sum().item())
 
 
 class GuardedPlane:
-    def __init__(self, M, K, f16=True):
-        self.g = [Guarded((M, K), torch.int8), Guarded((M, K // 32), torch.float32),
-                  Guarded((M, K // 32), torch.int32)]
-        if f16:
-            self.g.append(Guarded((M, K), torch.float16))
-        self.plane = mq.Plane(self.g[0].t, self.g[1].t, self.g[2].t, self.g[3].t if f16 else None)
+    """A plane whose arrays are all Guarded: the q8 arrays (q8=True) and/or the GEMM
+    operand arrays (op=True)."""
 
-    def check(self):
-        for g in self.g:
+    def __init__(self, M, K, q8=True, op=True):
+        self.M, self.K = M, K
+        self.g = {}
+        if q8:
+            self.g.update(qs=Guarded((M, K), torch.int8), d=Guarded((M, K // 32), torch.float32),
+                          s=Guarded((M, K // 32), torch.int32))
+        if op:
+            self.g.update(ah=Guarded((M, K), torch.float16), ax=Guarded((M, K // 256, 16), torch.float16),
+                          af=Guarded((K // 256, mq.Plane.af_stride(M)), torch.float32))
+        self.plane = mq.Plane(**{k: v.t for k, v in self.g.items()})
+
+    def check(self, ref=None):
+        """Guard bands intact; with both groups, the operand arrays equal the oracle's
+        operand form of this plane's own q8 arrays; with `ref` = (qs, d) from the oracle,
+        they equal the operand form of that plane."""
+        for g in self.g.values():
             g.check()
-        if self.plane.qh is not None:   # the f16 copy holds exactly the int8 quants
-            qs = self.plane.qs.cpu().numpy().astype(np.float32)
-            assert np.array_equal(self.plane.qh.cpu().numpy().astype(np.float32), qs), "qh != qs"
+        if "ah" not in self.g:
+            return
+        if ref is None:
+            if "qs" not in self.g:
+                return
+            ref = (self.plane.qs.cpu().numpy(), self.plane.d.cpu().numpy())
+        assert_operand_form(self.plane, ref[0], ref[1])
 
     def numpy(self):
         return (self.plane.qs.cpu().numpy(), self.plane.d.cpu().numpy(), self.plane.s.cpu().numpy())
+
+
+def assert_operand_form(plane, qs, d, rows=None, what="operand form"):
+    """ah, ax and af of the device plane (rows `rows`, default all) equal, bit for bit, the
+    oracle's operand form of the q8 plane (qs, d) (given for those rows)."""
+    from oracle import mq_oracle as O
+    ah, ax, af = O.operand_form(qs, d)
+    idx = None if rows is None else torch.as_tensor(np.asarray(rows), device=plane.ah.device)
+    gah = (plane.ah if idx is None else plane.ah[idx]).cpu().numpy()
+    gax = (plane.ax if idx is None else plane.ax[idx]).cpu().numpy()
+    gaf = plane.af.cpu().numpy()
+    gaf = gaf[:, :plane.M] if rows is None else gaf[:, np.asarray(rows)]
+    bad = np.argwhere(gah.view(np.uint16) != ah.view(np.uint16))
+    assert bad.size == 0, f"{what}: {len(bad)} ah mismatches, first at {bad[:5].tolist()}"
+    assert np.array_equal(gax.view(np.uint16), ax.view(np.uint16)), f"{what}: ax differs"
+    assert np.array_equal(gaf.view(np.uint32), af.view(np.uint32)), f"{what}: af differs"
 
 
 def assert_plane_equal(got, ref, what=""):

@@ -43,8 +43,10 @@ def test_binding_covers_every_declared_symbol(L):
 
 
 def test_size_helpers(L):
-    tot, qs, d, s = mq.mq_plane_bytes(3314, 3584)
-    assert (qs, d, s) == (3314 * 3584, 3314 * 112 * 4, 3314 * 112 * 4) and tot == qs + d + s
+    tot, qs, d, s, ah, ax, af = mq.mq_plane_bytes(3314, 3584)
+    assert (qs, d, s) == (3314 * 3584, 3314 * 112 * 4, 3314 * 112 * 4)
+    assert (ah, ax, af) == (3314 * 3584 * 2, 3314 * 14 * 32, 14 * 3316 * 4)
+    assert tot == qs + d + s + ah + ax + af
     assert mq.mq_q4k_row_bytes(3584) == 14 * 144
     assert mq.mq_q6k_row_bytes(18944) == 74 * 210
 
@@ -55,8 +57,8 @@ def test_status_strings(L):
     assert "UNKNOWN" in mq.status_str(99)
 
 
-def _plane(M, K, qs=1, d=1, s=1, qh=None):
-    return mq.CPlane(qs, d, s, qh, M, K)
+def _plane(M, K, qs=1, d=1, s=1, ah=None, ax=None, af=None):
+    return mq.CPlane(qs, d, s, ah, ax, af, M, K)
 
 
 def test_validation_before_any_cuda_call(L):
@@ -93,7 +95,7 @@ def test_matmul_validation_before_any_cuda_call(L):
     p = _plane(2, 512, 16, 16, 16)
     for fn in (L.mq_gemv_q4k, L.mq_gemv_q6k):
         assert fn(ctypes.byref(p), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE  # M != 1
-    p1 = _plane(1, 512, 16, 16, 16, 16)
+    p1 = _plane(1, 512, 16, 16, 16, 16, 16, 16)
     for fn in (L.mq_gemm_q4k, L.mq_gemm_q6k, L.mq_gemv_q4k, L.mq_gemv_q6k):
         assert fn(None, ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
         assert fn(ctypes.byref(p1), None, 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
@@ -103,9 +105,17 @@ def test_matmul_validation_before_any_cuda_call(L):
         assert fn(ctypes.byref(p1), ctypes.c_void_p(16), 0, None, null) == mq.MQ_OK      # N == 0: no-op
     bad = _plane(1, 300, 16, 16, 16)
     assert L.mq_gemm_q4k(ctypes.byref(bad), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE
-    # the GEMM needs the f16 copy of the quants; a misaligned one is rejected everywhere
+    # the GEMM needs the operand arrays, the GEMV the q8 arrays; a group is all present or all
+    # absent, and a misaligned array is rejected everywhere
     for fn in (L.mq_gemm_q4k, L.mq_gemm_q6k):
         assert fn(ctypes.byref(_plane(4, 512, 16, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
-        assert fn(ctypes.byref(_plane(4, 512, 16, 16, 16, 40)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_ALIGN
-    p8 = _plane(4, 256, 16, 16, 16, 24)
+        assert fn(ctypes.byref(_plane(4, 512, 16, 16, 16, 40, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_ALIGN
+        assert fn(ctypes.byref(_plane(4, 512, 16, 16, 16, 16, None, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
+    for fn in (L.mq_gemv_q4k, L.mq_gemv_q6k):
+        assert fn(ctypes.byref(_plane(1, 512, None, None, None, 16, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
+    p8 = _plane(4, 256, 16, 16, 16, 16, 16, 24)
     assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 256, ctypes.byref(p8), null) == mq.MQ_ERR_ALIGN
+    p9 = _plane(4, 256, None, None, None)
+    assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 256, ctypes.byref(p9), null) == mq.MQ_ERR_NULL
+    p10 = _plane(4, 256, 16, None, 16)
+    assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 256, ctypes.byref(p10), null) == mq.MQ_ERR_NULL

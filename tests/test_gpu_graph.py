@@ -43,7 +43,7 @@ def test_decode_layer_graph_replay_matches_eager():
     Wq = synth.weights("q4k", H, H, 5, "g.wq", device=dev)
     Wv = synth.weights("q6k", KV, H, 5, "g.wv", device=dev)
     Wd = synth.weights("q6k", H, F, 5, "g.wd", device=dev)
-    ph, pf = mq.Plane.empty(1, H, dev, f16=False), mq.Plane.empty(1, F, dev, f16=False)
+    ph, pf = mq.Plane.empty(1, H, dev, op=False), mq.Plane.empty(1, F, dev, op=False)
     oq = torch.empty((H,), device=dev)
     ov = torch.empty((KV,), device=dev)
     od = torch.empty((H,), device=dev)
@@ -116,7 +116,7 @@ def test_decode_layer_two_streams_matches_one_stream():
     Wq = [synth.weights("q4k", H, H, 7, f"s.wq{l}", device=dev) for l in range(2)]
     Wkv = [synth.weights("q6k", 2 * KV, H, 7, f"s.wkv{l}", device=dev) for l in range(2)]
     Wo = [synth.weights("q4k", H, H, 7, f"s.wo{l}", device=dev) for l in range(2)]
-    ph, pa = mq.Plane.empty(1, H, dev, f16=False), mq.Plane.empty(1, H, dev, f16=False)
+    ph, pa = mq.Plane.empty(1, H, dev, op=False), mq.Plane.empty(1, H, dev, op=False)
     oq = [torch.empty((H,), device=dev) for _ in range(2)]
     okv = [torch.empty((2 * KV,), device=dev) for _ in range(2)]
     oo = [torch.empty((H,), device=dev) for _ in range(2)]

@@ -126,7 +126,7 @@ def test_gemv_full_size_sampled_outputs(kind, N, K):
     the first and the last."""
     x = synth.normal((1, K), 0, f"fv{K}", device="cuda")
     w = synth.weights(kind, N, K, 0, f"fvw{kind}{N}", device="cuda")
-    p = mq.Plane.empty(1, K, f16=False)
+    p = mq.Plane.empty(1, K, op=False)
     mq.mq_quantize_q8(x, p)
     g = Guarded((1, N), torch.float32)
     mq.gemv(kind, p, w, N, g.t)

@@ -1,8 +1,8 @@
 """Parity of the q8 plane producers (CUDA, through the C ABI) with the CPU oracle.
 
-quantize and the fused RMSNorm producer must be bit-exact; the fused SwiGLU
-producer depends on expf, which CUDA and the host libm may round differently,
-and is held to +-1 quant level on at most 1e-4 of elements.
+All three producers (quantize, fused RMSNorm, fused SwiGLU with its pinned exp)
+must be bit-exact: the q8 arrays against the oracle's plane, and the GEMM
+operand arrays (ah, ax, af) against the oracle's operand form of it.
 Every output buffer starts poisoned (0xCD) inside guard bands, so an unwritten
 slot or an out-of-bounds write fails the test.
 """
@@ -12,7 +12,7 @@ import torch
 
 from oracle import mq_oracle as O
 from quant_int8_quantized_gb300 import mq, synth
-from tests._gpu_util import GuardedPlane, assert_plane_equal, require_gpu
+from tests._gpu_util import GuardedPlane, assert_operand_form, assert_plane_equal, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -163,14 +163,41 @@ def test_producers_full_size_sampled_rows():
     torch.cuda.synchronize()
     for gx in (gp, gpf, gpq):   # every block's d and s written (their poison words are impossible values)
         gx.check()
-        assert gx.g[1].untouched() == 0 and gx.g[2].untouched() == 0
+        assert gx.g["d"].untouched() == 0 and gx.g["s"].untouched() == 0
+        assert gx.g["ah"].untouched() == 0 and gx.g["ax"].untouched() == 0
     idx = torch.from_numpy(rows).cuda()
     sub = lambda pl: (pl.qs[idx].cpu().numpy(), pl.d[idx].cpu().numpy(), pl.s[idx].cpu().numpy())
     xs, ws = x[idx].cpu().numpy(), w.cpu().numpy()
     assert_plane_equal(sub(p), O.rms_quant(xs, ws, 1e-6), "rms full")
     assert_plane_equal(sub(pq), O.quantize_q8(g[idx].cpu().numpy()), "quantize full")
     assert_plane_equal(sub(pf), O.swiglu_quant(g[idx].cpu().numpy(), u[idx].cpu().numpy()), "swiglu full")
+    for pl, what in ((p, "rms"), (pq, "quantize"), (pf, "swiglu")):
+        qs_, d_, _ = sub(pl)
+        assert_operand_form(pl, qs_, d_, rows=rows, what=f"{what} full operand form")
+        assert not np.any(pl.af[:, :M].cpu().numpy().view(np.uint32) == 0xCDCDCDCD), f"{what}: af unwritten"
     assert mq.mq_device_status() == mq.MQ_OK
+
+
+@pytest.mark.parametrize("kind", ["quantize", "rms", "swiglu"])
+@pytest.mark.parametrize("M,K", [(1, 256), (5, 512), (130, 3584), (333, 18944), (3, 5120)])
+def test_operand_only_plane(kind, M, K):
+    """A GEMM-only plane (no q8 arrays): the producers write ah, ax, af equal to the oracle's
+    operand form of the oracle's plane, and nothing else."""
+    x = _x(M, K, f"op{kind}{M}x{K}", outliers=True)
+    gp = GuardedPlane(M, K, q8=False)
+    if kind == "quantize":
+        mq.mq_quantize_q8(x.cuda(), gp.plane)
+        ref = O.quantize_q8(x.numpy())
+    elif kind == "rms":
+        w = synth.normal((K,), 0, f"opw{K}", mean=1.0, std=0.1)
+        mq.mq_rms_quant(x.cuda(), w.cuda(), 1e-6, gp.plane)
+        ref = O.rms_quant(x.numpy(), w.numpy(), 1e-6)
+    else:
+        u = _x(M, K, f"opu{M}x{K}")
+        mq.mq_swiglu_quant(x.cuda(), u.cuda(), gp.plane)
+        ref = O.swiglu_quant(x.numpy(), u.numpy())
+    torch.cuda.synchronize()
+    gp.check(ref=(ref[0], ref[1]))
 
 
 def test_misaligned_input_rejected():

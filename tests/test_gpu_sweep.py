@@ -19,7 +19,7 @@ import torch
 
 from oracle import mq_oracle as O
 from quant_int8_quantized_gb300 import mq, synth
-from tests._gpu_util import assert_plane_equal, require_gpu
+from tests._gpu_util import assert_operand_form, assert_plane_equal, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -58,7 +58,7 @@ def test_sweep(kind, N, K):
     cols = _sample(N, 384, N + K, [N - 1])
     for M in SWEEP_M:
         x = synth.with_outliers(synth.normal((M, K), 0, f"sweep.x.{M}x{K}", device=dev), 0, f"sweep.o.{M}x{K}")
-        p = mq.Plane.empty(M, K, dev, f16=M > 1)
+        p = mq.Plane.empty(M, K, dev, op=M > 1)
         mq.mq_quantize_q8(x, p)
         out = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
         if M == 1:
@@ -100,7 +100,7 @@ def test_ffn_layer_chain():
     ref = O.rms_quant(x[rt].cpu().numpy(), w_rms.cpu().numpy(), 1e-6)
     got = (p_h.qs[rt].cpu().numpy(), p_h.d[rt].cpu().numpy(), p_h.s[rt].cpu().numpy())
     assert_plane_equal(got, ref, "ffn rms plane")
-    assert torch.equal(p_h.qh[rt].float(), p_h.qs[rt].float())
+    assert_operand_form(p_h, got[0], got[1], rows=rows, what="ffn rms operand form")
     # stage 2: gate and up on the GPU's plane
     cols_f = _sample(F, 256, 5, [F - 1])
     _check_sampled(g, p_h, Wg, "q4k", F, H, rows, cols_f)
