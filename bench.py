@@ -173,8 +173,9 @@ class Stack:
         self.rms_w = [S.normal((HID,), seed, f"L{l}.rms1", 1.0, 0.1, device=dev) for l in range(LAYERS)]
         self.rms2_w = [S.normal((HID,), seed, f"L{l}.rms2", 1.0, 0.1, device=dev) for l in range(LAYERS)]
         self.final_w = S.normal((HID,), seed, "final_norm", 1.0, 0.1, device=dev)
-        self.W = [{n: S.weights(kind, N, K, seed, f"L{l}.{n}", device=dev) for n, kind, N, K, _ in PREFILL_MATS}
-                  for l in range(LAYERS)]
+        # q6_K weights are prepacked once, as at weight registration (the GEMM's weight form)
+        self.W = [{n: mq.gemm_weights(kind, S.weights(kind, N, K, seed, f"L{l}.{n}", device=dev), N, K)
+                   for n, kind, N, K, _ in PREFILL_MATS} for l in range(LAYERS)]
         self.lm_head = S.q6k_weights(VOCAB, HID, seed, "lm_head", device=dev)
         f32 = dict(dtype=torch.float32, device=dev)
         self.out = {n: torch.empty((M_TOK, N), **f32) for n, _, N, _, _ in PREFILL_MATS}
@@ -422,6 +423,7 @@ def run_sweep(steps: int, warmup: int):
     for kind in ("q4k", "q6k"):
         for N, K in SWEEP_NK:
             w = S.weights(kind, N, K, 0, f"sweep.{kind}.{N}x{K}", device=dev)
+            wg = mq.gemm_weights(kind, w, N, K)
             for M in SWEEP_M:
                 x = S.with_outliers(S.normal((M, K), 0, f"sweep.x.{M}x{K}", device=dev), 0, f"sweep.o.{M}x{K}")
                 p = mq.Plane.empty(M, K, dev, op=M > 1)
@@ -431,7 +433,7 @@ def run_sweep(steps: int, warmup: int):
                     fn = lambda: mq.gemv(kind, p, w, N, out.view(-1))
                     act = plane_bytes(1, K) - (0 if kind == "q4k" else K // 32 * 4)
                 else:
-                    fn = lambda: mq.gemm(kind, p, w, N, out)
+                    fn = lambda: mq.gemm(kind, p, wg, N, out)
                     act = gemm_act_bytes(kind, M, K)
                 nbytes = wbytes(kind, N, K) + act + 4 * M * N
                 for _ in range(max(1, warmup)):
@@ -480,7 +482,8 @@ def run_case(spec: str, steps: int, warmup: int):
         p = mq.Plane.empty(M, K, dev)
         mq.mq_quantize_q8(x, p)
         out = torch.empty((M, N), dtype=torch.float32, device=dev)
-        fn = (lambda: mq.gemm(wk, p, w, N, out)) if kind.startswith("gemm") else (lambda: mq.gemv(wk, p, w, N, out))
+        wg = mq.gemm_weights(wk, w, N, K) if kind.startswith("gemm") else w
+        fn = (lambda: mq.gemm(wk, p, wg, N, out)) if kind.startswith("gemm") else (lambda: mq.gemv(wk, p, w, N, out))
         flops = 2.0 * M * N * K
         act = gemm_act_bytes(wk, M, K) if kind.startswith("gemm") else plane_bytes(M, K) - (0 if wk == "q4k" else M * (K // 32) * 4)
         nbytes = wbytes(wk, N, K) + act + 4 * M * N

@@ -111,6 +111,24 @@ size_t mq_q4k_row_bytes(int K);
 size_t mq_q6k_row_bytes(int K);
 
 /*
+ * Prepacked q6_K (the prefill GEMM's weight form): the same super-blocks re-laid
+ * out once, at weight registration ([r60] §1 and §3.2, registration-time layouts;
+ * [D3-7] Excerpt A, padded q6_K blocks), into 224-byte blocks, so that every
+ * block starts on a 16-byte boundary and each half of it is contiguous. Half h
+ * (h = 0, 1) of a packed block, at byte 112*h:
+ *     64 bytes  raw ql[64h .. 64h+63]   (low 4 bits)
+ *     32 bytes  raw qh[32h .. 32h+31]   (high 2 bits)
+ *      8 bytes  raw scales[8h .. 8h+7]  (int8)
+ *      2 bytes  d (f16), then 6 zero bytes.
+ * mq_q6k_packed_row_bytes(K) = K/256 * 224. mq_prepack_q6k reads N raw rows (w,
+ * 2-byte aligned, N*K/256*210 bytes) and writes N packed rows (packed, 16-byte
+ * aligned, caller-owned) on `stream`. Returns MQ_ERR_SHAPE for K not a positive
+ * multiple of 256 or N < 0.
+ */
+size_t mq_q6k_packed_row_bytes(int K);
+int mq_prepack_q6k(const void* w, int N, int K, void* packed, cudaStream_t stream);
+
+/*
  * mq_quantize_q8 — standalone activation quantization ([r52] §2.2; [D3-7]
  * Excerpt C, the per-32-block epilogue; [D3-7] Excerpt A2, the decode
  * quantize). x: f32 [M][K] row-major. For every block of 32:
@@ -159,8 +177,8 @@ int mq_swiglu_quant(const float* g, const float* u, int M, int K,
  *     out[m][n] = sum_k (d_a[m][k/32] * q_a[m][k]) * w[n][k]
  * with w the dequantized weight (q4_K: d*sc*q - dmin*m per 32; q6_K:
  * d*sc*(q-32) per 16). a: plane with a->M >= 1 rows, a->K = K and its operand
- * arrays (ah, ax, af; MQ_ERR_NULL otherwise); w: N rows of super-blocks in the
- * layout above (q6_K rows need only 2-byte alignment within the buffer); out:
+ * arrays (ah, ax, af; MQ_ERR_NULL otherwise); w: N rows of super-blocks, q4_K
+ * in the raw layout above, q6_K in the prepacked layout (mq_prepack_q6k); out:
  * f32 [a->M][N] row-major, overwritten. Any M >= 1 is accepted (the kernel is
  * built for M >= 16).
  * Arithmetic: per 256-wide super-block, the f16 tensor pipe multiplies the

@@ -37,12 +37,11 @@
 //
 // One persistent CTA per SM, 640 threads:
 //   warp 0      TMA producer: activation slots (K = 64 x 192 tokens), the block-sum
-//               record and 2^-e row of each super-block, q4_K weight rows;
+//               record and 2^-e row of each super-block, weight rows;
 //   warp 1      MMA issuer;
 //   warp 2      TMEM allocator;
 //   warps 4-11  weight converters, thread = weight row, two warps per TMEM lane
-//               quarter, each half of a super-block's K; they also stage q6_K rows
-//               (2-byte aligned) with one 224-byte bulk copy per row;
+//               quarter, each half of a super-block's K;
 //   warps 12-19 epilogue, thread = weight row, two warps per lane quarter, 96
 //               token columns each, accumulators in registers across the
 //               super-blocks of a work unit.
@@ -74,7 +73,7 @@ constexpr int kConvWarps = 8;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + 32 * kConvWarps + 32 * kEpiWarps;
 constexpr int kLaunchRegs = 96;         // 65536 / 640, rounded down to the allocation unit
-constexpr int kRegsWG0 = 32, kRegsConv = 64, kRegsEpi = 160;
+constexpr int kRegsWG0 = 64, kRegsConv = 64, kRegsEpi = 144;
 static_assert(128 * kRegsWG0 + 32 * kConvWarps * kRegsConv + 32 * kEpiWarps * kRegsEpi <= kThreads * kLaunchRegs,
               "register split");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -85,8 +84,11 @@ static_assert(kACol + 128 <= kTmemCols, "tensor memory");
 
 template <bool Q6>
 struct Cfg {
-    static constexpr int kSB = Q6 ? mq::Q6K_BYTES : mq::Q4K_BYTES;
-    static constexpr int kRowBytes = Q6 ? 224 : 144;   // staged bytes per weight row (q6_K: its aligned window)
+    // q4_K: raw 144-byte super-blocks. q6_K: the 224-byte prepacked form (mq.h), staged
+    // with a 240-byte pitch (the box reads 16 bytes past the block) so that one 16-byte
+    // load per thread and row hits 8 distinct bank groups per 8 rows.
+    static constexpr int kSB = Q6 ? mq::Q6K_PACKED_BYTES : mq::Q4K_BYTES;
+    static constexpr int kRowBytes = Q6 ? 240 : 144;   // staged bytes per weight row (the TMA box)
     static constexpr int kStage = BW * kRowBytes;
     static constexpr int kRB = Q6 ? 2 : 3;             // weight stages
     // Weight-operand slots in tensor memory. q4_K: slot j holds K chunk j of every super-block
@@ -196,26 +198,12 @@ __device__ __forceinline__ uint32_t byte_of(uint32_t y, uint32_t z, uint32_t w, 
     return (v >> (8 * (i & 3))) & 0xffu;
 }
 
-// Eight little-endian words starting at a 2-byte aligned shared-memory address.
-__device__ __forceinline__ void lds32x8_unaligned(const uint8_t* p, uint32_t (&w)[8]) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const uint32_t* b = reinterpret_cast<const uint32_t*>(a & ~(uintptr_t)3);
-    const uint32_t sh = (uint32_t)(a & 3) * 8;
-    uint32_t v[9];
-#pragma unroll
-    for (int i = 0; i < 9; ++i) v[i] = b[i];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = __funnelshift_r(v[i], v[i + 1], sh);
-}
-
 template <bool Q6>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmAct,
                                                            const __grid_constant__ CUtensorMap tmAx,
                                                            const __grid_constant__ CUtensorMap tmAf,
                                                            const __grid_constant__ CUtensorMap tmW,
-                                                           const uint8_t* __restrict__ W, float* __restrict__ out,
-                                                           int M, int N, int K, int splits,
-                                                           unsigned long long wstride, unsigned long long wtotal) {
+                                                           float* __restrict__ out, int M, int N, int K, int splits) {
     using C = Cfg<Q6>;
     constexpr int kRB = C::kRB, kRF = C::kRF;
     extern __shared__ uint8_t smem_raw[];
@@ -234,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc::mbar_init(&sm.c_empty[i], kEpiWarps);
         }
         for (int i = 0; i < kRB; ++i) {
-            tc::mbar_init(&sm.b_full[i], Q6 ? BW : 1);       // q6_K: one bulk copy per row
+            tc::mbar_init(&sm.b_full[i], 1);
             tc::mbar_init(&sm.b_empty[i], kConvWarps);
         }
         for (int i = 0; i < kRF; ++i) {
@@ -274,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     tc::tma_load_2d(sm.af[x], &tmAf, wk.m0, sb, &sm.ax_full[x]);
                     issX |= 1u << x;
                     phX = (phX & ~(1u << x)) | (((sbc / RX) & 1) << x);
-                    if constexpr (!Q6) {
+                    {
                         const int b = sbc % kRB;
                         if (!wait1(sm, &sm.b_empty[b], ((sbc / kRB) & 1) ^ 1)) break;
                         tc::mbar_arrive_expect_tx(&sm.b_full[b], C::kStage);
@@ -301,55 +289,78 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
         } else if (warp == 1 && lane == 0) {
             // ---------------------------------------------------- MMA issuer
+            // The tensor pipe queues only a few MMAs, so every wait between MMA groups that
+            // finds the pipe empty leaves it idle. The issuer therefore tests the barriers of
+            // the next group in the middle of the current one, with MMAs still queued: group
+            // (sbc, j) for j = 0..3 is K chunk j of super-block sbc; after chunk 3 come the
+            // super-block's q4_K min-term MMAs and the next super-block's accumulator slot.
             const uint32_t idesc = tc::instr_desc(BW, BT, 0);
-            bool issued = false;
-            int sbc = 0, ga = 0;
-            for (int u = blockIdx.x; u < units && !aborted(sm); u += gridDim.x) {
+            int total = 0;   // super-blocks this CTA accumulates (the issuer needs no tile positions)
+            for (int u = blockIdx.x; u < units; u += gridDim.x) {
                 const Work wk = work_of(u, splits, num_mt, S);
-                for (int sb = wk.sb0; sb < wk.sb1 && !aborted(sm); ++sb, ++sbc) {
-                    const int s = sbc & 1;
-                    const uint32_t dcol = tbase + (s ? kSCol1 : kSCol0);
-                    if (!wait1(sm, &sm.t_empty[s], ((sbc >> 1) & 1) ^ 1)) break;
-                    bool ok = true;
-                    for (int j = 0; j < 4; ++j, ++ga) {
-                        // slot f; its use number u (q4_K: one use a super-block; q6_K: two)
-                        const int a = ga % RA, f = Q6 ? (j & 1) : j, u = Q6 ? 2 * sbc + (j >> 1) : sbc;
-                        if (!wait1(sm, &sm.act_full[a], (ga / RA) & 1) || !wait1(sm, &sm.a_full[f], u & 1)) {
-                            ok = false;
-                            break;
-                        }
-                        tc::tc_fence_after();
-                        const uint32_t sa = tc::smem_u32(sm.act[a]);
-                        const uint32_t fa = tbase + kACol + C::kFCols * f;
+                total += wk.sb1 - wk.sb0;
+            }
+            // readiness of chunk j of super-block sbc, whose activation slot is ga
+            auto chunk_ready = [&](int sbc_, int j_, int ga_) {
+                const int f = Q6 ? (j_ & 1) : j_;
+                const uint32_t pf = Q6 ? (uint32_t)(j_ >> 1) : (uint32_t)(sbc_ & 1);
+                return wait1(sm, &sm.act_full[ga_ % RA], (ga_ / RA) & 1) && wait1(sm, &sm.a_full[f], pf);
+            };
+            auto sb_ready = [&](int sbc_, int ga_) {   // accumulator slot free, first chunk ready
+                return wait1(sm, &sm.t_empty[sbc_ & 1], ((sbc_ >> 1) & 1) ^ 1) && chunk_ready(sbc_, 0, ga_);
+            };
+            bool ok = total > 0 && sb_ready(0, 0);
+            tc::tc_fence_after();
+            int ga = 0;
+            for (int sbc = 0; sbc < total && ok; ++sbc) {
+                const int s = sbc & 1, x = sbc % RX;
+                const uint32_t dcol = tbase + (s ? kSCol1 : kSCol0);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t bd = tc::smem_desc_sw128(sa + 32 * k);
-                            tc::mma_f16_ts(dcol, fa + 8 * k, bd, idesc, (j | k) ? 1u : 0u);
-                            if constexpr (Q6) tc::mma_f16_ts(dcol, fa + 32 + 8 * k, bd, idesc, 1u);
-                        }
-                        tc::mma_commit(&sm.act_empty[a]);
-                        // q6_K: the next writer of slot f is the other half
-                        tc::mma_commit(&sm.a_empty[f][Q6 ? 1 - (j >> 1) : 0]);
-                        issued = true;
+                for (int j = 0; j < 4; ++j) {
+                    const int a = (ga + j) % RA, f = Q6 ? (j & 1) : j;
+                    const uint32_t sa = tc::smem_u32(sm.act[a]);
+                    const uint32_t fa = tbase + kACol + C::kFCols * f;
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const uint64_t bd = tc::smem_desc_sw128(sa + 32 * k);
+                        tc::mma_f16_ts(dcol, fa + 8 * k, bd, idesc, (j | k) ? 1u : 0u);
+                        if constexpr (Q6) tc::mma_f16_ts(dcol, fa + 32 + 8 * k, bd, idesc, 1u);
+                    }
+                    // while those run: the next group's barriers
+                    if (j < 3) {
+                        ok = chunk_ready(sbc, j + 1, ga + j + 1);
+                    } else if constexpr (!Q6) {
+                        ok = wait1(sm, &sm.ax_full[x], (sbc / RX) & 1) && wait1(sm, &sm.m_full[sbc & 1], (sbc >> 1) & 1);
                     }
                     if (!ok) break;
-                    const int x = sbc % RX;
-                    if (!wait1(sm, &sm.ax_full[x], (sbc / RX) & 1)) break;
-                    if constexpr (!Q6) {
-                        const int m = sbc & 1;
-                        if (!wait1(sm, &sm.m_full[m], (sbc >> 1) & 1)) break;
-                        tc::tc_fence_after();
-                        const uint64_t bd = tc::smem_desc_sw32(tc::smem_u32(sm.ax[x]));
-                        const uint32_t ma = tc::smem_u32(sm.mop[m]);
-                        tc::mma_f16(dcol, tc::smem_desc_noswizzle(ma, 128, 256), bd, idesc, 1u);
-                        tc::mma_f16(dcol, tc::smem_desc_noswizzle(ma + kMTile, 128, 256), bd, idesc, 1u);
-                        tc::mma_commit(&sm.m_empty[m]);
+                    tc::tc_fence_after();
+#pragma unroll
+                    for (int k = 2; k < 4; ++k) {
+                        const uint64_t bd = tc::smem_desc_sw128(sa + 32 * k);
+                        tc::mma_f16_ts(dcol, fa + 8 * k, bd, idesc, 1u);
+                        if constexpr (Q6) tc::mma_f16_ts(dcol, fa + 32 + 8 * k, bd, idesc, 1u);
                     }
-                    tc::mma_commit(&sm.ax_empty[x]);
-                    tc::mma_commit(&sm.t_full[s]);
+                    tc::mma_commit(&sm.act_empty[a]);
+                    // q6_K: the next writer of slot f is the other half
+                    tc::mma_commit(&sm.a_empty[f][Q6 ? 1 - (j >> 1) : 0]);
+                }
+                if (!ok) break;
+                ga += 4;
+                if constexpr (!Q6) {
+                    const uint64_t bd = tc::smem_desc_sw32(tc::smem_u32(sm.ax[x]));
+                    const uint32_t ma = tc::smem_u32(sm.mop[sbc & 1]);
+                    tc::mma_f16(dcol, tc::smem_desc_noswizzle(ma, 128, 256), bd, idesc, 1u);
+                    tc::mma_f16(dcol, tc::smem_desc_noswizzle(ma + kMTile, 128, 256), bd, idesc, 1u);
+                    tc::mma_commit(&sm.m_empty[sbc & 1]);
+                }
+                tc::mma_commit(&sm.ax_empty[x]);   // q6_K: a token arrival (the block sums are the epilogue's)
+                tc::mma_commit(&sm.t_full[s]);
+                if (sbc + 1 < total) {
+                    ok = sb_ready(sbc + 1, ga);
+                    tc::tc_fence_after();
                 }
             }
-            if (issued) {   // every MMA of this CTA has completed before TMEM is freed
+            if (total > 0) {   // every MMA of this CTA has completed before TMEM is freed
                 tc::mma_commit(&sm.mma_done);
                 tc::mbar_wait(&sm.mma_done, 0, kWaitLimitNs);
             }
@@ -363,49 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int r = 32 * q + lane;                            // weight row within the tile
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         int sbc = 0;
-        uint32_t issB = 0, phB = 0;                             // q6_K copies in flight (for an abort)
-        // q6_K: threads of the h == 0 warps stage their row's super-block window, one stage ahead
-        auto q6_issue = [&](int sbc_i, const Work& wk_i, int sb_i) {
-            const int b = sbc_i % kRB;
-            if (!wwait(sm, &sm.b_empty[b], ((sbc_i / kRB) & 1) ^ 1)) return false;
-            const int n = wk_i.n0 + r;
-            uint8_t* dst = sm.braw[b] + r * C::kRowBytes;
-            uint32_t bytes = 0;
-            const unsigned long long a0 =
-                n < N ? (((unsigned long long)n * wstride + (unsigned long long)sb_i * C::kSB) & ~15ull) : 0;
-            if (n < N) {
-                bytes = C::kRowBytes;
-                if (a0 + C::kRowBytes > wtotal) {   // the matrix's last super-block: copy its tail by hand
-                    bytes = (uint32_t)((wtotal - a0) & ~15ull);
-                    for (unsigned long long p = a0 + bytes; p < wtotal; ++p) dst[p - a0] = W[p];
-                }
-            }
-            tc::mbar_arrive_expect_tx(&sm.b_full[b], bytes);
-            if (bytes) tc::bulk_load(dst, W + a0, bytes, &sm.b_full[b]);
-            issB |= 1u << b;
-            phB = (phB & ~(1u << b)) | (((sbc_i / kRB) & 1) << b);
-            return true;
-        };
-        if constexpr (Q6) {
-            if (h == 0 && blockIdx.x < units) {
-                const Work w0 = work_of(blockIdx.x, splits, num_mt, S);
-                q6_issue(0, w0, w0.sb0);
-            }
-        }
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
             const Work wk = work_of(u, splits, num_mt, S);
             const int n = wk.n0 + r;
             for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb, ++sbc) {
                 const int b = sbc % kRB, x = sbc % RX;
-                if constexpr (Q6) {
-                    if (h == 0) {   // stage the next super-block (of this unit or the next one)
-                        const int nu = (sb + 1 < wk.sb1) ? u : u + (int)gridDim.x;
-                        if (nu < units) {
-                            const Work nw = (nu == u) ? wk : work_of(nu, splits, num_mt, S);
-                            if (!q6_issue(sbc + 1, nw, nu == u ? sb + 1 : nw.sb0)) break;
-                        }
-                    }
-                }
                 if (!wwait(sm, &sm.b_full[b], (sbc / kRB) & 1)) break;
                 const uint8_t* row = sm.braw[b] + r * C::kRowBytes;
                 if constexpr (!Q6) {
@@ -494,29 +467,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         if (lane == 0) tc::mbar_arrive(&sm.c_full[x]);
                     }
                 } else {
-                    // ---- q6_K: the row's super-block sits at offset o of its aligned window
-                    const int o = n < N ? (int)(((unsigned long long)n * wstride + (unsigned long long)sb * C::kSB) & 15ull)
-                                        : 0;
-                    const uint8_t* blk = row + o;
+                    // ---- q6_K (prepacked): half h of the block is 112 bytes at 112 h: ql (64), qh (32),
+                    //      the half's 8 scales, d. Slot j = 2h + jj covers quarters t = 2jj + i, i = 0, 1:
+                    //      low bits from ql bytes 32i.. (high nibble when jj = 1), high bits from qh
+                    //      bits 2t, scale of element l = byte 2t + (l >= 16).
+                    const uint8_t* half = row + 112 * h;
+                    const uint4 c6 = *reinterpret_cast<const uint4*>(half + 96);
                     bool ok = true;
-                    // slot j = 2h + jj covers half h, quarters 2jj and 2jj + 1
-                    uint32_t qh[8];
-                    lds32x8_unaligned(blk + 128 + 32 * h, qh);
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
-                        const int j = 2 * h + jj, f = jj;
+                        const int f = jj;
                         // slot jj alternates between the halves: half 0 waits for the previous
                         // super-block's half-1 use to be read, half 1 for this super-block's half-0 use
                         if (!wwait(sm, &sm.a_empty[f][h], h ? (sbc & 1) : ((sbc & 1) ^ 1))) { ok = false; break; }
                         tc::tc_fence_after();   // the stores below come after the MMAs that read the slot
                         const uint32_t fa = tbase + lane_bits + kACol + C::kFCols * f;
-                        const uint32_t scw = (uint32_t)blk[192 + 8 * h + 4 * jj] | ((uint32_t)blk[193 + 8 * h + 4 * jj] << 8) |
-                                             ((uint32_t)blk[194 + 8 * h + 4 * jj] << 16) |
-                                             ((uint32_t)blk[195 + 8 * h + 4 * jj] << 24);
+                        const uint32_t scw = jj ? c6.y : c6.x;          // scale bytes 4jj .. 4jj + 3
+                        const uint4 h0 = *reinterpret_cast<const uint4*>(half + 64);
+                        const uint4 h1 = *reinterpret_cast<const uint4*>(half + 80);
+                        const uint32_t qh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {          // quarter t = 2 jj + i
-                            uint32_t ql[8];
-                            lds32x8_unaligned(blk + 64 * h + 32 * i, ql);
+                            const uint4 l0 = *reinterpret_cast<const uint4*>(half + 32 * i);
+                            const uint4 l1 = *reinterpret_cast<const uint4*>(half + 32 * i + 16);
+                            const uint32_t ql[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
                             const int nsh = jj ? 4 : 0, hsh = 2 * (2 * jj + i);
                             uint32_t p1[16], p2[16];
 #pragma unroll
@@ -538,9 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (!ok) break;
                     if (h == 0) {
                         if (!wwait(sm, &sm.c_empty[x], ((sbc / RX) & 1) ^ 1)) break;
-                        const float d = n < N ? __half2float(__ushort_as_half(*reinterpret_cast<const unsigned short*>(blk + 208)))
-                                              : 0.0f;
-                        sm.cvec[x][r] = d;
+                        sm.cvec[x][r] = n < N ? __half2float(__ushort_as_half((unsigned short)(c6.z & 0xffffu))) : 0.0f;
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&sm.c_full[x]);
                     }
@@ -548,11 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&sm.b_empty[b]);
             }
-        }
-        if constexpr (Q6) {   // no bulk copy of this CTA is left in flight
-            if (h == 0 && aborted(sm))
-                for (int i = 0; i < kRB; ++i)
-                    if (issB >> i & 1u) tc::mbar_wait(&sm.b_full[i], phB >> i & 1u, kWaitLimitNs);
         }
     } else {
         // ============================================================ epilogue
@@ -719,11 +686,8 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
     if (!gemm_ready<Q6>(smem)) return MQ_ERR_LAUNCH;
     const unsigned long long row = (unsigned long long)S * Cfg<Q6>::kSB;
     CUtensorMap tmAct, tmAx, tmAf, tmW;
-    if (Q6) {
-        tmW = CUtensorMap{};   // unused: q6_K rows are 2-byte aligned; the converters stage them
-    } else if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row, (uint64_t)N, row, mq::Q4K_BYTES, BW)) {
+    if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row, (uint64_t)N, row, Cfg<Q6>::kRowBytes, BW))
         return MQ_ERR_LAUNCH;
-    }
     const int mp = mq::af_stride(M);
     if (!make_map(&tmAct, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ah, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, KS, BT,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -738,8 +702,7 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
         return MQ_ERR_LAUNCH;
     const long long units = tiles * splits;
     const int grid = (int)(units < sms ? units : sms);
-    gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, static_cast<const uint8_t*>(w), out, M,
-                                                      N, K, splits, row, row * (unsigned long long)N);
+    gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits);
     return mq::launch_status();
 }
 

@@ -13,6 +13,7 @@ constexpr int QK = 32;          // activation block
 constexpr int QK_K = 256;       // weight super-block
 constexpr int Q4K_BYTES = 144;
 constexpr int Q6K_BYTES = 210;
+constexpr int Q6K_PACKED_BYTES = 224;   // prepacked q6_K super-block (mq_prepack_q6k)
 
 // Host-side validation helpers ------------------------------------------------
 

@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libmq.so")
 
 MQ_OK, MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_ARCH, MQ_ERR_LAUNCH, MQ_ERR_DEVICE = range(7)
 
-EXPORTED = ["mq_plane_bytes", "mq_q4k_row_bytes", "mq_q6k_row_bytes", "mq_quantize_q8", "mq_rms_quant",
+EXPORTED = ["mq_plane_bytes", "mq_q4k_row_bytes", "mq_q6k_row_bytes", "mq_q6k_packed_row_bytes", "mq_prepack_q6k",
+            "mq_quantize_q8", "mq_rms_quant",
             "mq_swiglu_quant", "mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k",
             "mq_device_status", "mq_status_str"]
 
@@ -52,6 +53,8 @@ def lib() -> ctypes.CDLL:
             "mq_plane_bytes": (sz, [i, i, psz, psz, psz, psz, psz, psz]),
             "mq_q4k_row_bytes": (sz, [i]),
             "mq_q6k_row_bytes": (sz, [i]),
+            "mq_q6k_packed_row_bytes": (sz, [i]),
+            "mq_prepack_q6k": (i, [vp, i, i, vp, vp]),
             "mq_quantize_q8": (i, [vp, i, i, pp, vp]),
             "mq_rms_quant": (i, [vp, vp, i, i, f, pp, vp]),
             "mq_swiglu_quant": (i, [vp, vp, i, i, pp, vp]),
@@ -162,6 +165,20 @@ def mq_q6k_row_bytes(K: int) -> int:
     return int(lib().mq_q6k_row_bytes(K))
 
 
+def mq_q6k_packed_row_bytes(K: int) -> int:
+    return int(lib().mq_q6k_packed_row_bytes(K))
+
+
+def mq_prepack_q6k(w: torch.Tensor, N: int, K: int, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Raw q6_K rows [N, K/256*210] (uint8) -> the prepacked layout [N, K/256*224] the GEMM reads."""
+    _dev_tensor(w, torch.uint8, "w")
+    if out is None:
+        out = torch.empty((N, mq_q6k_packed_row_bytes(K)), dtype=torch.uint8, device=w.device)
+    _dev_tensor(out, torch.uint8, "out")
+    _check(lib().mq_prepack_q6k(_ptr(w), int(N), int(K), _ptr(out), _stream(stream)), "mq_prepack_q6k")
+    return out
+
+
 def mq_quantize_q8(x: torch.Tensor, out: Plane, stream=None) -> Plane:
     _dev_tensor(x, torch.float32, "x")
     cp = out.c()
@@ -216,6 +233,11 @@ def mq_gemv_q6k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=Non
 
 def mq_device_status(stream=None) -> int:
     return int(lib().mq_device_status(_stream(stream)))
+
+
+def gemm_weights(kind: str, w: torch.Tensor, N: int, K: int, stream=None) -> torch.Tensor:
+    """The weight form the GEMM reads: q4_K rows as they are, q6_K rows prepacked."""
+    return mq_prepack_q6k(w, N, K, stream=stream) if kind == "q6k" else w
 
 
 def gemm(kind: str, a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:

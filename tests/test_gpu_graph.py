@@ -81,7 +81,7 @@ def test_prefill_gemm_graph_replay_matches_eager():
     M, N, K = 200, 384, 1024
     x = synth.normal((M, K), 6, "g.px", device=dev)
     W4 = synth.weights("q4k", N, K, 6, "g.pw4", device=dev)
-    W6 = synth.weights("q6k", N, K, 6, "g.pw6", device=dev)
+    W6 = mq.mq_prepack_q6k(synth.weights("q6k", N, K, 6, "g.pw6", device=dev), N, K)
     p = mq.Plane.empty(M, K, dev)
     o4 = torch.empty((M, N), device=dev)
     o6 = torch.empty((M, N), device=dev)

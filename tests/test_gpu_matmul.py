@@ -41,7 +41,10 @@ def _run(kind, x, N, K, fn, outliers_name=None):
     w = synth.weights(kind, N, K, 0, f"{kind}.{N}x{K}")
     p = _plane_from(x)
     g = Guarded((x.shape[0], N), torch.float32)
-    fn(kind, p, w.cuda(), N, g.t)
+    wd = w.cuda()
+    if fn is mq.gemm:
+        wd = mq.gemm_weights(kind, wd, N, K)
+    fn(kind, p, wd, N, g.t)
     torch.cuda.synchronize()
     g.check()
     return g.t, p, w
@@ -95,7 +98,7 @@ def test_gemm_full_size_sampled_rows(kind, N, K):
     p = mq.Plane.empty(M, K)
     mq.mq_quantize_q8(x, p)
     g = Guarded((M, N), torch.float32)
-    mq.gemm(kind, p, w, N, g.t)
+    mq.gemm(kind, p, mq.gemm_weights(kind, w, N, K), N, g.t)
     torch.cuda.synchronize()
     g.check()
     assert g.untouched() == 0, "unwritten outputs"
@@ -174,7 +177,7 @@ def test_gemv_matches_gemm_at_one_row(kind):
     a = torch.empty((1, N), device="cuda")
     b = torch.empty((1, N), device="cuda")
     mq.gemv(kind, p, w, N, a)
-    mq.gemm(kind, p, w, N, b)
+    mq.gemm(kind, p, mq.gemm_weights(kind, w, N, K), N, b)
     torch.cuda.synchronize()
     ref, bound = O.gemm_rows(p.qs.cpu().numpy(), p.d.cpu().numpy(), w.cpu().numpy(), kind, N, K)
     assert np.all(np.abs(a.cpu().numpy() - b.cpu().numpy()) <= 2 * bound)
@@ -187,3 +190,24 @@ def test_gemv_rejects_multi_row_plane():
     with pytest.raises(mq.MQError) as e:
         mq.mq_gemv_q4k(p, w, 8, out)
     assert e.value.status == mq.MQ_ERR_SHAPE
+
+
+@pytest.mark.parametrize("N,K", [(1, 256), (7, 768), (300, 512), (64, 18944)])
+def test_prepack_q6k_is_the_documented_layout(N, K):
+    """Half h of each packed 224-byte block: raw ql[64h..], qh[32h..], scales[8h..], d, 6 zeros.
+    The expected bytes are assembled here from the raw block, field by field."""
+    S = K // 256
+    raw = np.random.default_rng(N + K).integers(0, 256, size=(N, S, 210), dtype=np.uint8)
+    want = np.zeros((N, S, 224), np.uint8)
+    for h in range(2):
+        o = 112 * h
+        want[..., o:o + 64] = raw[..., 64 * h:64 * h + 64]
+        want[..., o + 64:o + 96] = raw[..., 128 + 32 * h:128 + 32 * h + 32]
+        want[..., o + 96:o + 104] = raw[..., 192 + 8 * h:192 + 8 * h + 8]
+        want[..., o + 104:o + 106] = raw[..., 208:210]
+    w = torch.from_numpy(np.ascontiguousarray(raw.reshape(N, S * 210))).cuda()
+    g = Guarded((N, S * 224), torch.uint8)
+    mq.mq_prepack_q6k(w, N, K, g.t)
+    torch.cuda.synchronize()
+    g.check()
+    assert np.array_equal(g.t.cpu().numpy().reshape(N, S, 224), want)

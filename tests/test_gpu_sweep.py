@@ -55,6 +55,7 @@ def _check_sampled(out, plane, w, kind, N, K, rows, cols):
 def test_sweep(kind, N, K):
     dev = torch.device("cuda")
     w = synth.weights(kind, N, K, 0, f"sweep.{kind}.{N}x{K}", device=dev)
+    wg = mq.gemm_weights(kind, w, N, K)
     cols = _sample(N, 384, N + K, [N - 1])
     for M in SWEEP_M:
         x = synth.with_outliers(synth.normal((M, K), 0, f"sweep.x.{M}x{K}", device=dev), 0, f"sweep.o.{M}x{K}")
@@ -64,7 +65,7 @@ def test_sweep(kind, N, K):
         if M == 1:
             mq.gemv(kind, p, w, N, out.view(-1))
         else:
-            mq.gemm(kind, p, w, N, out)
+            mq.gemm(kind, p, wg, N, out)
         torch.cuda.synchronize()
         assert not torch.isnan(out).any(), f"unwritten outputs at M={M}"
         rows = _sample(M, 8, M * 7 + K, [0, M - 1])
@@ -90,7 +91,7 @@ def test_ffn_layer_chain():
     p_f = mq.Plane.empty(M, F, dev)
     mq.mq_swiglu_quant(g, u, p_f)
     y = torch.empty((M, H), device=dev)
-    mq.mq_gemm_q6k(p_f, Wd, H, y)
+    mq.mq_gemm_q6k(p_f, mq.mq_prepack_q6k(Wd, H, F), H, y)
     torch.cuda.synchronize()
     assert mq.mq_device_status() == mq.MQ_OK
 
