@@ -64,7 +64,7 @@ __device__ unsigned int g_gemm_error;   // bit 0: a bounded wait gave up
 constexpr int BW = 128;                 // weight rows per tile (MMA M)
 constexpr int BT = 192;                 // tokens per tile (MMA N)
 constexpr int KS = 64;                  // K per activation slot and weight-operand slot
-constexpr int RA = 5;                   // activation slots
+constexpr int RA = 5;                   // activation slots (q6_K; q4_K: one per K chunk, see Cfg)
 constexpr int RX = 3;                   // per-super-block stages (block sums, 2^-e, weight scales c)
 constexpr int kActBytes = BT * KS * 2;  // 24576
 constexpr int kAxBytes = BT * 32;       // 16 binary16 block-sum parts per token
@@ -97,19 +97,25 @@ struct Cfg {
     // consecutive phases of its barrier, which a parity wait tells apart.
     static constexpr int kRF = Q6 ? 2 : 4;
     static constexpr uint32_t kFCols = Q6 ? 64 : 32;   // tensor-memory columns per weight-operand slot
+    // q4_K: activation slot j and weight-operand slot j both hold K chunk j, so one
+    // barrier pair per chunk covers both (the TMA and the 4 converter warps of its half
+    // arrive on "full", the MMAs' commit on "empty"), and the min-term operand joins
+    // the per-super-block block-sum stage the same way: half the issuer's waits.
+    static constexpr bool kJoint = !Q6;
+    static constexpr int kRA = Q6 ? RA : 4;
 };
 
 template <bool Q6>
 struct Smem {
-    alignas(1024) uint8_t act[RA][kActBytes];
+    alignas(1024) uint8_t act[Cfg<Q6>::kRA][kActBytes];
     alignas(256) uint8_t ax[RX][kAxBytes];
     alignas(16) float af[RX][BT];
     float cvec[RX][BW];
     alignas(128) uint8_t braw[Cfg<Q6>::kRB][Cfg<Q6>::kStage];
-    alignas(128) uint8_t mop[2][Q6 ? 16 : 2 * kMTile];   // q4_K min-term operand (hi part, lo part)
-    uint64_t act_full[RA], act_empty[RA], ax_full[RX], ax_empty[RX], c_full[RX], c_empty[RX];
+    alignas(128) uint8_t mop[Q6 ? 1 : RX][Q6 ? 16 : 2 * kMTile];   // q4_K min-term operand (hi, lo) per stage
+    uint64_t act_full[Cfg<Q6>::kRA], act_empty[Cfg<Q6>::kRA], ax_full[RX], ax_empty[RX], c_full[RX], c_empty[RX];
     uint64_t b_full[Cfg<Q6>::kRB], b_empty[Cfg<Q6>::kRB];
-    uint64_t a_full[Cfg<Q6>::kRF], a_empty[Cfg<Q6>::kRF][2], m_full[2], m_empty[2];
+    uint64_t a_full[Cfg<Q6>::kRF], a_empty[Cfg<Q6>::kRF][2];
     uint64_t t_full[2], t_empty[2], mma_done;
     uint32_t tmem;
     int abort;
@@ -121,9 +127,12 @@ struct Smem {
 struct Work {
     int m0, n0, sb0, sb1;
 };
-__device__ __forceinline__ Work work_of(int u, int splits, int num_mt, int S) {
+// nfast: weight-row tiles fastest (when the activation operand is the larger one, so
+// that each token tile's activations are read from memory once).
+__device__ __forceinline__ Work work_of(int u, int splits, int num_mt, int num_nt, bool nfast, int S) {
     const int t = u / splits, sp = u - t * splits;
-    return Work{(t % num_mt) * BT, (t / num_mt) * BW, (sp * S) / splits, ((sp + 1) * S) / splits};
+    const int mt = nfast ? t / num_nt : t % num_mt, nt = nfast ? t % num_nt : t / num_mt;
+    return Work{mt * BT, nt * BW, (sp * S) / splits, ((sp + 1) * S) / splits};
 }
 
 // Non-suspending test of a phase (acquire semantics, like the waits).
@@ -203,7 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                                            const __grid_constant__ CUtensorMap tmAx,
                                                            const __grid_constant__ CUtensorMap tmAf,
                                                            const __grid_constant__ CUtensorMap tmW,
-                                                           float* __restrict__ out, int M, int N, int K, int splits) {
+                                                           float* __restrict__ out, int M, int N, int K, int splits,
+                                                           int nfast) {
     using C = Cfg<Q6>;
     constexpr int kRB = C::kRB, kRF = C::kRF;
     extern __shared__ uint8_t smem_raw[];
@@ -214,9 +224,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int units = num_mt * num_nt * splits;
 
     if (tid == 0) {
-        for (int i = 0; i < RA; ++i) { tc::mbar_init(&sm.act_full[i], 1); tc::mbar_init(&sm.act_empty[i], 1); }
+        for (int i = 0; i < C::kRA; ++i) {
+            tc::mbar_init(&sm.act_full[i], C::kJoint ? 5 : 1);
+            tc::mbar_init(&sm.act_empty[i], 1);
+        }
         for (int i = 0; i < RX; ++i) {
-            tc::mbar_init(&sm.ax_full[i], 1);
+            tc::mbar_init(&sm.ax_full[i], C::kJoint ? 5 : 1);
             tc::mbar_init(&sm.ax_empty[i], 1 + kEpiWarps);   // the MMAs (block sums) and the epilogue (2^-e)
             tc::mbar_init(&sm.c_full[i], 4);
             tc::mbar_init(&sm.c_empty[i], kEpiWarps);
@@ -231,8 +244,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc::mbar_init(&sm.a_empty[i][1], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            tc::mbar_init(&sm.m_full[i], 4);
-            tc::mbar_init(&sm.m_empty[i], 1);
             tc::mbar_init(&sm.t_full[i], 1);
             tc::mbar_init(&sm.t_empty[i], kEpiWarps);
         }
@@ -253,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t issA = 0, phA = 0, issX = 0, phX = 0, issB = 0, phB = 0;   // copies in flight (for an abort)
             int sbc = 0, ga = 0;
             for (int u = blockIdx.x; u < units && !aborted(sm); u += gridDim.x) {
-                const Work wk = work_of(u, splits, num_mt, S);
+                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S);
                 for (int sb = wk.sb0; sb < wk.sb1 && !aborted(sm); ++sb, ++sbc) {
                     const int x = sbc % RX;
                     if (!wait1(sm, &sm.ax_empty[x], ((sbc / RX) & 1) ^ 1)) break;
@@ -272,18 +283,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     }
                     bool ok = true;
                     for (int j = 0; j < 4; ++j, ++ga) {
-                        const int a = ga % RA;
-                        if (!wait1(sm, &sm.act_empty[a], ((ga / RA) & 1) ^ 1)) { ok = false; break; }
+                        const int a = ga % C::kRA;
+                        const uint32_t pa = (ga / C::kRA) & 1;
+                        if (!wait1(sm, &sm.act_empty[a], pa ^ 1)) { ok = false; break; }
                         tc::mbar_arrive_expect_tx(&sm.act_full[a], kActBytes);
                         tc::tma_load_2d(sm.act[a], &tmAct, sb * 256 + KS * j, wk.m0, &sm.act_full[a]);
                         issA |= 1u << a;
-                        phA = (phA & ~(1u << a)) | (((ga / RA) & 1) << a);
+                        phA = (phA & ~(1u << a)) | (pa << a);
                     }
                     if (!ok) break;
                 }
             }
             if (aborted(sm)) {   // let every copy already issued land before the CTA exits
-                for (int i = 0; i < RA; ++i) if (issA >> i & 1u) tc::mbar_wait(&sm.act_full[i], phA >> i & 1u, kWaitLimitNs);
+                for (int i = 0; i < C::kRA; ++i) if (issA >> i & 1u) tc::mbar_wait(&sm.act_full[i], phA >> i & 1u, kWaitLimitNs);
                 for (int i = 0; i < RX; ++i) if (issX >> i & 1u) tc::mbar_wait(&sm.ax_full[i], phX >> i & 1u, kWaitLimitNs);
                 for (int i = 0; i < kRB; ++i) if (issB >> i & 1u) tc::mbar_wait(&sm.b_full[i], phB >> i & 1u, kWaitLimitNs);
             }
@@ -297,14 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint32_t idesc = tc::instr_desc(BW, BT, 0);
             int total = 0;   // super-blocks this CTA accumulates (the issuer needs no tile positions)
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
-                const Work wk = work_of(u, splits, num_mt, S);
+                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S);
                 total += wk.sb1 - wk.sb0;
             }
             // readiness of chunk j of super-block sbc, whose activation slot is ga
             auto chunk_ready = [&](int sbc_, int j_, int ga_) {
-                const int f = Q6 ? (j_ & 1) : j_;
-                const uint32_t pf = Q6 ? (uint32_t)(j_ >> 1) : (uint32_t)(sbc_ & 1);
-                return wait1(sm, &sm.act_full[ga_ % RA], (ga_ / RA) & 1) && wait1(sm, &sm.a_full[f], pf);
+                if constexpr (C::kJoint) return wait1(sm, &sm.act_full[j_], sbc_ & 1);
+                return wait1(sm, &sm.act_full[ga_ % C::kRA], (ga_ / C::kRA) & 1) && wait1(sm, &sm.a_full[j_ & 1], j_ >> 1);
             };
             auto sb_ready = [&](int sbc_, int ga_) {   // accumulator slot free, first chunk ready
                 return wait1(sm, &sm.t_empty[sbc_ & 1], ((sbc_ >> 1) & 1) ^ 1) && chunk_ready(sbc_, 0, ga_);
@@ -317,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const uint32_t dcol = tbase + (s ? kSCol1 : kSCol0);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int a = (ga + j) % RA, f = Q6 ? (j & 1) : j;
+                    const int a = (ga + j) % C::kRA, f = Q6 ? (j & 1) : j;
                     const uint32_t sa = tc::smem_u32(sm.act[a]);
                     const uint32_t fa = tbase + kACol + C::kFCols * f;
 #pragma unroll
@@ -330,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (j < 3) {
                         ok = chunk_ready(sbc, j + 1, ga + j + 1);
                     } else if constexpr (!Q6) {
-                        ok = wait1(sm, &sm.ax_full[x], (sbc / RX) & 1) && wait1(sm, &sm.m_full[sbc & 1], (sbc >> 1) & 1);
+                        ok = wait1(sm, &sm.ax_full[x], (sbc / RX) & 1);   // block sums and min-term operand
                     }
                     if (!ok) break;
                     tc::tc_fence_after();
@@ -342,16 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     }
                     tc::mma_commit(&sm.act_empty[a]);
                     // q6_K: the next writer of slot f is the other half
-                    tc::mma_commit(&sm.a_empty[f][Q6 ? 1 - (j >> 1) : 0]);
+                    if constexpr (!C::kJoint) tc::mma_commit(&sm.a_empty[f][1 - (j >> 1)]);
                 }
                 if (!ok) break;
                 ga += 4;
                 if constexpr (!Q6) {
                     const uint64_t bd = tc::smem_desc_sw32(tc::smem_u32(sm.ax[x]));
-                    const uint32_t ma = tc::smem_u32(sm.mop[sbc & 1]);
+                    const uint32_t ma = tc::smem_u32(sm.mop[x]);
                     tc::mma_f16(dcol, tc::smem_desc_noswizzle(ma, 128, 256), bd, idesc, 1u);
                     tc::mma_f16(dcol, tc::smem_desc_noswizzle(ma + kMTile, 128, 256), bd, idesc, 1u);
-                    tc::mma_commit(&sm.m_empty[sbc & 1]);
                 }
                 tc::mma_commit(&sm.ax_empty[x]);   // q6_K: a token arrival (the block sums are the epilogue's)
                 tc::mma_commit(&sm.t_full[s]);
@@ -375,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         int sbc = 0;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of(u, splits, num_mt, S);
+            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S);
             const int n = wk.n0 + r;
             for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb, ++sbc) {
                 const int b = sbc % kRB, x = sbc % RX;
@@ -403,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                     for (int jj = 0; jj < 2; ++jj) {
                         const int j = 2 * h + jj, f = j;   // slot j: this half's own, one use a super-block
-                        if (!wwait(sm, &sm.a_empty[f][0], (sbc & 1) ^ 1)) { ok = false; break; }
+                        if (!wwait(sm, &sm.act_empty[f], (sbc & 1) ^ 1)) { ok = false; break; }
                         tc::tc_fence_after();   // the stores below come after the MMAs that read the slot
                         const int s0 = j < 2 ? (int)(byte_of(hdr.y, hdr.z, hdr.w, 2 * j) & 63u)
                                              : (int)((byte_of(hdr.y, hdr.z, hdr.w, 2 * j + 4) & 15u) |
@@ -428,12 +438,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         tc::tmem_st_wait();
                         tc::tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&sm.a_full[f]);
+                        if (lane == 0) tc::mbar_arrive(&sm.act_full[f]);
                     }
                     if (!ok) break;
                     if (h == 0) {
-                        const int mslot = sbc & 1;
-                        if (!wwait(sm, &sm.m_empty[mslot], ((sbc >> 1) & 1) ^ 1)) break;
+                        if (!wwait(sm, &sm.ax_empty[x], ((sbc / RX) & 1) ^ 1)) break;
                         uint32_t mh[8];
 #pragma unroll
                         for (int j = 0; j < 8; j += 2) {
@@ -452,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         }
                         // row r of the hi tile [hi_0..hi_7, hi_0..hi_7] and of the lo tile, K-major
                         // without swizzle: core matrices of 8 rows x 16 B, K-adjacent ones 128 B apart
-                        uint8_t* mt = sm.mop[mslot] + (r >> 3) * 256 + (r & 7) * 16;
+                        uint8_t* mt = sm.mop[x] + (r >> 3) * 256 + (r & 7) * 16;
                         const uint4 vh = make_uint4(mh[0], mh[1], mh[2], mh[3]), vl = make_uint4(mh[4], mh[5], mh[6], mh[7]);
                         *reinterpret_cast<uint4*>(mt) = vh;
                         *reinterpret_cast<uint4*>(mt + 128) = vh;
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         *reinterpret_cast<uint4*>(mt + kMTile + 128) = vl;
                         tc::fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&sm.m_full[mslot]);
+                        if (lane == 0) tc::mbar_arrive(&sm.ax_full[x]);
                         if (!wwait(sm, &sm.c_empty[x], ((sbc / RX) & 1) ^ 1)) break;
                         sm.cvec[x][r] = n < N ? c : 0.0f;
                         __syncwarp();
@@ -530,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         int sbc = 0;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of(u, splits, num_mt, S);
+            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S);
             float acc[96];
 #pragma unroll
             for (int i = 0; i < 96; ++i) acc[i] = 0.0f;
@@ -702,7 +711,9 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
         return MQ_ERR_LAUNCH;
     const long long units = tiles * splits;
     const int grid = (int)(units < sms ? units : sms);
-    gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits);
+    // weight-row tiles fastest when the activations outweigh the weights
+    const int nfast = (double)M * K * 2 > (double)N * row ? 1 : 0;
+    gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits, nfast);
     return mq::launch_status();
 }
 
