@@ -32,8 +32,8 @@
 // (N = 128: 67%; A from shared memory: at most 80%).
 // Tensor memory (512 columns): two 192-column super-block accumulators (the
 // epilogue drains one while the MMAs fill the other), the weight operand slots
-// (q4_K: 4 slots of K = 64, 32 columns each; q6_K: 2 slots of K = 64 with both
-// parts, 64 columns each).
+// (4 slots of 32 columns: q4_K one K = 64 chunk each, q6_K one K = 32 quarter with
+// both parts each).
 //
 // One persistent CTA per SM, 640 threads:
 //   warp 0      TMA producer: activation slots (K = 64 x 192 tokens), the block-sum
@@ -91,12 +91,13 @@ struct Cfg {
     static constexpr int kRowBytes = Q6 ? 240 : 144;   // staged bytes per weight row (the TMA box)
     static constexpr int kStage = BW * kRowBytes;
     static constexpr int kRB = Q6 ? 2 : 3;             // weight stages
-    // Weight-operand slots in tensor memory. q4_K: slot j holds K chunk j of every super-block
-    // and is written by one converter half only. q6_K: slot j & 1, written alternately by the
-    // two halves, each waiting on its own "empty" barrier: every waiter then waits for
-    // consecutive phases of its barrier, which a parity wait tells apart.
-    static constexpr int kRF = Q6 ? 2 : 4;
-    static constexpr uint32_t kFCols = Q6 ? 64 : 32;   // tensor-memory columns per weight-operand slot
+    // Weight-operand slots in tensor memory, 32 columns each. q4_K: slot j holds K chunk j
+    // (64 wide) of every super-block and is written by one converter half only. q6_K: slot
+    // t holds quarter t of a super-block half (32 wide, both exact parts), written
+    // alternately by the two halves, each waiting on its own "empty" barrier: every waiter
+    // then waits for consecutive phases of its barrier, which a parity wait tells apart.
+    static constexpr int kRF = 4;
+    static constexpr uint32_t kFCols = 32;
     // q4_K: activation slot j and weight-operand slot j both hold K chunk j, so one
     // barrier pair per chunk covers both (the TMA and the 4 converter warps of its half
     // arrive on "full", the MMAs' commit on "empty"), and the min-term operand joins
@@ -313,9 +314,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 total += wk.sb1 - wk.sb0;
             }
             // readiness of chunk j of super-block sbc, whose activation slot is ga
+            // q4_K: chunk j is ready when its joint barrier completes; q6_K: its activation
+            // slot and its first quarter's operand (the second quarter is waited for between
+            // the first quarter's MMAs)
             auto chunk_ready = [&](int sbc_, int j_, int ga_) {
                 if constexpr (C::kJoint) return wait1(sm, &sm.act_full[j_], sbc_ & 1);
-                return wait1(sm, &sm.act_full[ga_ % C::kRA], (ga_ / C::kRA) & 1) && wait1(sm, &sm.a_full[j_ & 1], j_ >> 1);
+                return wait1(sm, &sm.act_full[ga_ % C::kRA], (ga_ / C::kRA) & 1) &&
+                       wait1(sm, &sm.a_full[(2 * j_) & 3], (uint32_t)(j_ >> 1));
             };
             auto sb_ready = [&](int sbc_, int ga_) {   // accumulator slot free, first chunk ready
                 return wait1(sm, &sm.t_empty[sbc_ & 1], ((sbc_ >> 1) & 1) ^ 1) && chunk_ready(sbc_, 0, ga_);
@@ -328,32 +333,44 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const uint32_t dcol = tbase + (s ? kSCol1 : kSCol0);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int a = (ga + j) % C::kRA, f = Q6 ? (j & 1) : j;
+                    const int a = (ga + j) % C::kRA;
                     const uint32_t sa = tc::smem_u32(sm.act[a]);
-                    const uint32_t fa = tbase + kACol + C::kFCols * f;
+                    if constexpr (!Q6) {
+                        const uint32_t fa = tbase + kACol + C::kFCols * j;
 #pragma unroll
-                    for (int k = 0; k < 2; ++k) {
-                        const uint64_t bd = tc::smem_desc_sw128(sa + 32 * k);
-                        tc::mma_f16_ts(dcol, fa + 8 * k, bd, idesc, (j | k) ? 1u : 0u);
-                        if constexpr (Q6) tc::mma_f16_ts(dcol, fa + 32 + 8 * k, bd, idesc, 1u);
-                    }
-                    // while those run: the next group's barriers
-                    if (j < 3) {
-                        ok = chunk_ready(sbc, j + 1, ga + j + 1);
-                    } else if constexpr (!Q6) {
-                        ok = wait1(sm, &sm.ax_full[x], (sbc / RX) & 1);   // block sums and min-term operand
-                    }
-                    if (!ok) break;
-                    tc::tc_fence_after();
+                        for (int k = 0; k < 2; ++k)
+                            tc::mma_f16_ts(dcol, fa + 8 * k, tc::smem_desc_sw128(sa + 32 * k), idesc, (j | k) ? 1u : 0u);
+                        // while those run: the next group's barriers
+                        ok = j < 3 ? chunk_ready(sbc, j + 1, ga + j + 1) : wait1(sm, &sm.ax_full[x], (sbc / RX) & 1);
+                        if (!ok) break;
+                        tc::tc_fence_after();
 #pragma unroll
-                    for (int k = 2; k < 4; ++k) {
-                        const uint64_t bd = tc::smem_desc_sw128(sa + 32 * k);
-                        tc::mma_f16_ts(dcol, fa + 8 * k, bd, idesc, 1u);
-                        if constexpr (Q6) tc::mma_f16_ts(dcol, fa + 32 + 8 * k, bd, idesc, 1u);
+                        for (int k = 2; k < 4; ++k)
+                            tc::mma_f16_ts(dcol, fa + 8 * k, tc::smem_desc_sw128(sa + 32 * k), idesc, 1u);
+                        tc::mma_commit(&sm.act_empty[a]);
+                    } else {
+                        // quarters q = 2j, 2j + 1 (operand slot q & 3, written by half j >> 1); each
+                        // K = 16 step is two MMAs, the parts sc*lo and 16*sc*(hi - 2)
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const int qq = (2 * j + i) & 3;
+                            const uint32_t fa = tbase + kACol + C::kFCols * qq;
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                const uint64_t bd = tc::smem_desc_sw128(sa + 64 * i + 32 * k);
+                                tc::mma_f16_ts(dcol, fa + 8 * k, bd, idesc, (j | i | k) ? 1u : 0u);
+                                tc::mma_f16_ts(dcol, fa + 16 + 8 * k, bd, idesc, 1u);
+                            }
+                            tc::mma_commit(&sm.a_empty[qq][1 - (j >> 1)]);   // the next writer is the other half
+                            // while those run: the next quarter (and at the chunk's end the next chunk)
+                            if (i == 0) ok = wait1(sm, &sm.a_full[qq + 1], (uint32_t)(j >> 1));
+                            else if (j < 3) ok = chunk_ready(sbc, j + 1, ga + j + 1);
+                            if (!ok) break;
+                            tc::tc_fence_after();
+                        }
+                        if (!ok) break;
+                        tc::mma_commit(&sm.act_empty[a]);
                     }
-                    tc::mma_commit(&sm.act_empty[a]);
-                    // q6_K: the next writer of slot f is the other half
-                    if constexpr (!C::kJoint) tc::mma_commit(&sm.a_empty[f][1 - (j >> 1)]);
                 }
                 if (!ok) break;
                 ga += 4;
@@ -482,41 +499,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     //      bits 2t, scale of element l = byte 2t + (l >= 16).
                     const uint8_t* half = row + 112 * h;
                     const uint4 c6 = *reinterpret_cast<const uint4*>(half + 96);
+                    const uint4 h0 = *reinterpret_cast<const uint4*>(half + 64);
+                    const uint4 h1 = *reinterpret_cast<const uint4*>(half + 80);
+                    const uint32_t qh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
                     bool ok = true;
+                    // quarter t of this half -> operand slot t, written alternately by the halves:
+                    // half 0 waits for the previous super-block's half-1 use to be read, half 1 for
+                    // this super-block's half-0 use
 #pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        const int f = jj;
-                        // slot jj alternates between the halves: half 0 waits for the previous
-                        // super-block's half-1 use to be read, half 1 for this super-block's half-0 use
-                        if (!wwait(sm, &sm.a_empty[f][h], h ? (sbc & 1) : ((sbc & 1) ^ 1))) { ok = false; break; }
+                    for (int t = 0; t < 4; ++t) {
+                        if (!wwait(sm, &sm.a_empty[t][h], h ? (sbc & 1) : ((sbc & 1) ^ 1))) { ok = false; break; }
                         tc::tc_fence_after();   // the stores below come after the MMAs that read the slot
-                        const uint32_t fa = tbase + lane_bits + kACol + C::kFCols * f;
-                        const uint32_t scw = jj ? c6.y : c6.x;          // scale bytes 4jj .. 4jj + 3
-                        const uint4 h0 = *reinterpret_cast<const uint4*>(half + 64);
-                        const uint4 h1 = *reinterpret_cast<const uint4*>(half + 80);
-                        const uint32_t qh[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+                        const uint32_t fa = tbase + lane_bits + kACol + C::kFCols * t;
+                        const uint32_t scw = (t < 2) ? c6.x : c6.y;     // scale bytes 2t, 2t + 1 of the half
+                        const uint4 l0 = *reinterpret_cast<const uint4*>(half + 32 * (t & 1));
+                        const uint4 l1 = *reinterpret_cast<const uint4*>(half + 32 * (t & 1) + 16);
+                        const uint32_t ql[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+                        const int nsh = (t >> 1) * 4, hsh = 2 * t;
+                        uint32_t p1[16], p2[16];
 #pragma unroll
-                        for (int i = 0; i < 2; ++i) {          // quarter t = 2 jj + i
-                            const uint4 l0 = *reinterpret_cast<const uint4*>(half + 32 * i);
-                            const uint4 l1 = *reinterpret_cast<const uint4*>(half + 32 * i + 16);
-                            const uint32_t ql[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-                            const int nsh = jj ? 4 : 0, hsh = 2 * (2 * jj + i);
-                            uint32_t p1[16], p2[16];
-#pragma unroll
-                            for (int w = 0; w < 8; ++w) {
-                                const float sc = (float)(int)(int8_t)(scw >> (8 * (2 * i + (w >> 2))));
-                                nib4_one((ql[w] >> nsh) & 0x0F0F0F0Fu, h2_of(16.0f * sc), h2_of(-16.0f * sc), p1[2 * w],
-                                         p1[2 * w + 1]);
-                                nib4_one((qh[w] >> hsh) & 0x03030303u, h2_of(256.0f * sc), h2_of(-288.0f * sc), p2[2 * w],
-                                         p2[2 * w + 1]);
-                            }
-                            tc::tmem_st16(fa + 16 * i, p1);
-                            tc::tmem_st16(fa + 32 + 16 * i, p2);
+                        for (int w = 0; w < 8; ++w) {
+                            const float sc = (float)(int)(int8_t)(scw >> (8 * (2 * (t & 1) + (w >> 2))));
+                            nib4_one((ql[w] >> nsh) & 0x0F0F0F0Fu, h2_of(16.0f * sc), h2_of(-16.0f * sc), p1[2 * w],
+                                     p1[2 * w + 1]);
+                            nib4_one((qh[w] >> hsh) & 0x03030303u, h2_of(256.0f * sc), h2_of(-288.0f * sc), p2[2 * w],
+                                     p2[2 * w + 1]);
                         }
+                        tc::tmem_st16(fa, p1);
+                        tc::tmem_st16(fa + 16, p2);
                         tc::tmem_st_wait();
                         tc::tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&sm.a_full[f]);
+                        if (lane == 0) tc::mbar_arrive(&sm.a_full[t]);
                     }
                     if (!ok) break;
                     if (h == 0) {
