@@ -211,3 +211,87 @@ def test_prepack_q6k_is_the_documented_layout(N, K):
     torch.cuda.synchronize()
     g.check()
     assert np.array_equal(g.t.cpu().numpy().reshape(N, S, 224), want)
+
+
+def _unit_activations(rng, M, K, small_first_half=False):
+    """Integer activations whose every 32-block holds a 127, so d_a = 1 and q_a = x. With
+    small_first_half, elements 0..15 of each block lie in [-1, 1] and the 127 sits in 16..31."""
+    x = rng.integers(-8, 9, size=(M, K)).astype(np.float32)
+    for b in range(K // 32):
+        if small_first_half:
+            x[:, 32 * b:32 * b + 16] = rng.integers(-1, 2, size=(M, 16))
+            x[np.arange(M), 32 * b + 16 + rng.integers(0, 16, size=M)] = 127.0
+        else:
+            x[np.arange(M), 32 * b + rng.integers(0, 32, size=M)] = 127.0
+    return torch.from_numpy(x)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 256, 512), (130, 200, 768), (300, 1100, 1280)])
+def test_gemm_q4k_exact_integer_dots(M, N, K):
+    """Unit super-block scales (d = dmin = 1), sub-block scales 0 or 1, mins 0..7 and d_a = 1:
+    the operand form is exact (ah = 4q, block sums 4s, dmin/d = 1), every product and partial
+    sum is an integer below 2^24, so the GEMM must equal the f64 oracle bit for bit."""
+    rng = np.random.default_rng(M + N + K)
+    S = K // 256
+    blk = np.zeros((N, S, 144), np.uint8)
+    blk[..., 0:2] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+    blk[..., 2:4] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+    sc = rng.integers(0, 2, size=(N, S, 8))
+    mn = rng.integers(0, 8, size=(N, S, 8))
+    # 6-bit fields < 16: bytes 0..3 scales 0..3, 4..7 mins 0..3, 8..11 scale | min << 4 of 4..7
+    blk[..., 4:8] = sc[..., :4]
+    blk[..., 8:12] = mn[..., :4]
+    blk[..., 12:16] = sc[..., 4:] | (mn[..., 4:] << 4)
+    blk[..., 16:144] = rng.integers(0, 256, size=(N, S, 128), dtype=np.uint8)
+    w = torch.from_numpy(np.ascontiguousarray(blk.reshape(N, S * 144))).cuda()
+    p = _plane_from(_unit_activations(rng, M, K))
+    assert np.all(p.d.cpu().numpy() == 1.0)
+    g = Guarded((M, N), torch.float32)
+    mq.mq_gemm_q4k(p, w, N, g.t)
+    torch.cuda.synchronize()
+    g.check()
+    ref, _ = O.gemm_rows(p.qs.cpu().numpy(), p.d.cpu().numpy(), w.cpu().numpy(), "q4k", N, K)
+    assert np.all(np.abs(ref) < 2 ** 22)
+    got = g.t.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, ref), f"max diff {np.max(np.abs(got - ref))}"
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 256, 256), (130, 200, 768), (64, 300, 1280)])
+def test_gemm_q6k_exact_integer_dots(M, N, K):
+    """d = 1, sub-block scales +-1, and in sub-blocks 2j (the first half of each 32-block, where
+    the activations lie in [-1, 1]) also scale -128 with high bits 0, so the operand's two exact
+    parts reach 2432 and 4096. With d_a = 1 every partial sum is an integer below 2^24 and the
+    GEMM must equal the f64 oracle bit for bit."""
+    rng = np.random.default_rng(M + N + K + 1)
+    S = K // 256
+    blk = rng.integers(0, 256, size=(N, S, 210), dtype=np.uint8)
+    scales = rng.choice(np.array([-1, 1], np.int8), size=(N, S, 16))
+    big = rng.random((N, S, 8)) < 0.5                      # sub-block 2j gets -128 with hi = 0
+    scales[..., 0::2] = np.where(big, np.int8(-128), scales[..., 0::2])
+    blk[..., 192:208] = scales.view(np.uint8)
+    blk[..., 208:210] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+    # hi = 0 for every element of a "big" sub-block: element e = 128h + 32t + l of sub-block
+    # g = e // 16 takes its high bits from qh[32h + l] bits 2t, 2t + 1
+    qh = blk[..., 128:192].copy()
+    for e in range(256):
+        g = e // 16
+        if g % 2:
+            continue
+        h, r = divmod(e, 128)
+        t, l = divmod(r, 32)
+        mask = np.uint8(~(3 << (2 * t)) & 0xFF)
+        qh[..., 32 * h + l] = np.where(big[..., g // 2], qh[..., 32 * h + l] & mask, qh[..., 32 * h + l])
+    blk[..., 128:192] = qh
+    w = torch.from_numpy(np.ascontiguousarray(blk.reshape(N, S * 210))).cuda()
+    p = _plane_from(_unit_activations(rng, M, K, small_first_half=True))
+    assert np.all(p.d.cpu().numpy() == 1.0)
+    g = Guarded((M, N), torch.float32)
+    mq.mq_gemm_q6k(p, mq.mq_prepack_q6k(w, N, K), N, g.t)
+    torch.cuda.synchronize()
+    g.check()
+    ref, _ = O.gemm_rows(p.qs.cpu().numpy(), p.d.cpu().numpy(), w.cpu().numpy(), "q6k", N, K)
+    wd = O.dequant_q6k(w.cpu().numpy(), N, K)
+    assert np.max(np.abs(wd)) >= 2176               # the scale -128 with hi = 0 is exercised
+    assert np.all(np.abs(ref) < 2 ** 22)
+    got = g.t.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, ref), f"max diff {np.max(np.abs(got - ref))}"
