@@ -260,12 +260,68 @@ class Stack:
         per_layer = sum(2.0 * M_TOK * N * K for _, _, N, K, _ in PREFILL_MATS)
         return LAYERS * per_layer + 2.0 * VOCAB * HID
 
+    LAUNCHES_PER_DECODE_UNSTACKED = D_LAYERS * 10   # rms, q, k, v, quantize, o, gate, up, swiglu, down
+
+    def decode_step_unstacked(self):
+        """The decode layer as config 4 names it: seven GEMVs a layer, one stream. k, v, gate
+        and up are row slices of the stacked matrices (the same bytes, no copy)."""
+        mq = self.mq
+        for l in range(D_LAYERS):
+            W = self.DW[l]
+            mq.mq_rms_quant(self.dx, self.drms[l], EPS, self.dp_h)
+            mq.mq_gemv_q4k(self.dp_h, W["q"], D_HID, self.dout["q"])
+            mq.mq_gemv_q6k(self.dp_h, W["kv"][:D_KV], D_KV, self.dout["kv"][:D_KV])
+            mq.mq_gemv_q6k(self.dp_h, W["kv"][D_KV:], D_KV, self.dout["kv"][D_KV:])
+            mq.mq_quantize_q8(self.dattn, self.dp_a)
+            mq.mq_gemv_q4k(self.dp_a, W["o"], D_HID, self.dout["o"])
+            mq.mq_gemv_q4k(self.dp_h, W["gate_up"][:D_FFN], D_FFN, self.dout["gate_up"][:D_FFN])
+            mq.mq_gemv_q4k(self.dp_h, W["gate_up"][D_FFN:], D_FFN, self.dout["gate_up"][D_FFN:])
+            mq.mq_swiglu_quant(self.dg, self.du, self.dp_f)
+            mq.mq_gemv_q6k(self.dp_f, W["down"], D_HID, self.dout["down"])
+
     @staticmethod
     def decode_bytes():
         per_layer = sum(wbytes(kind, N, K) + 4 * N for _, kind, N, K in DECODE_MATS)
         per_layer += 4 * D_HID * 2 + plane_bytes(1, D_HID) * 2 + 8 * D_FFN + plane_bytes(1, D_FFN)  # producers
         per_layer += 4 * D_HID                                                                        # rms weight
         return D_LAYERS * per_layer
+
+
+def producer_rates(st, dev, stream, reps=20):
+    """Each prefill producer alone at the stack's shapes, writing the GEMM operand arrays, its
+    inputs rotated over buffers that together exceed L2. Rates are counted in the method's
+    bytes (the f32 input, 4 or 8 B per element, and the q8 plane, 1.25 B per element); the
+    operand arrays the GEMM reads instead (2.14 B per element) are listed beside them."""
+    from quant_int8_quantized_gb300 import mq, synth as S
+    hbm = load_peaks()[2]
+    out = {}
+    xs = [S.normal((M_TOK, HID), 0, f"pr.x{i}", device=dev) for i in range(4)]          # 4 x 47.5 MB
+    gs = [S.normal((M_TOK, FFN), 0, f"pr.g{i}", device=dev) for i in range(2)]          # 2 x 251 MB
+    us = [S.normal((M_TOK, FFN), 0, f"pr.u{i}", device=dev) for i in range(2)]
+    w = S.normal((HID,), 0, "pr.w", 1.0, 0.1, device=dev)
+    ph, pf = mq.Plane.empty(M_TOK, HID, dev, q8=False), mq.Plane.empty(M_TOK, FFN, dev, q8=False)
+    cases = [("rms_quant", HID, 4, lambda i: mq.mq_rms_quant(xs[i % 4], w, EPS, ph)),
+             ("quantize_q8", HID, 4, lambda i: mq.mq_quantize_q8(xs[i % 4], ph)),
+             ("swiglu_quant", FFN, 8, lambda i: mq.mq_swiglu_quant(gs[i % 2], us[i % 2], pf))]
+    for name, K, in_b, fn in cases:
+        for i in range(4):
+            fn(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(reps):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        t = a.elapsed_time(b) * 1e-3 / reps
+        n = M_TOK * K
+        method = n * in_b + n * 1.25
+        actual = n * in_b + plane_bytes(M_TOK, K, q8=False, op=True)
+        out[f"{name} {M_TOK}x{K}"] = {"us": t * 1e6, "method_bytes": method, "GBps_method": method / t / 1e9,
+                                      "hbm_frac_method": method / t / 1e9 / hbm, "written_operand_bytes": actual - n * in_b,
+                                      "GBps_actual": actual / t / 1e9, "hbm_frac_actual": actual / t / 1e9 / hbm}
+    del xs, gs, us
+    return out
 
 
 def capture_graph(fn):
@@ -285,34 +341,38 @@ def capture_graph(fn):
 
 # ----------------------------------------------------------------------------- CPU oracle sample
 
-def oracle_sample_tok_s(tokens=2, frac=4, seed=0):
-    """Time the CPU oracle on a bounded sample of the prefill stack and extrapolate to tok/s.
+def oracle_sample_tok_s(frac=8, prod_frac=16, seed=0):
+    """Time the CPU oracle on a bounded sample of the prefill stack at M = 3314 and
+    extrapolate to tok/s.
 
-    Sample: `tokens` tokens through one full layer's producers, and through every
-    matmul of that layer restricted to one in `frac` of its output rows (the
-    oracle's cost is linear in output rows: it dequantizes exactly the rows it
-    computes), plus the last-token lm_head on one in 8*frac of its rows. The
-    layer time (matmul part scaled by `frac`) is multiplied by 28 layers.
+    The oracle's matmul cost is linear in output rows (it dequantizes exactly the weight
+    rows it computes), not in tokens, so the sample keeps all 3314 tokens: one layer's 7
+    matmuls on 1 in `frac` of their output rows (x frac), the layer's 4 producers on 1 in
+    `prod_frac` of the tokens (x prod_frac), times 28 layers, plus the last-token lm_head on
+    1 in 8*frac of its rows. Input generation is not timed.
     """
     from oracle import mq_oracle as O
     from quant_int8_quantized_gb300 import synth as S
-    x = S.normal((tokens, HID), seed, "x").numpy()
-    attn = S.normal((tokens, HID), seed, "attn").numpy()
+    mp = M_TOK // prod_frac
+    x = S.normal((mp, HID), seed, "x").numpy()
+    attn = S.normal((mp, HID), seed, "attn").numpy()
     w1 = S.normal((HID,), seed, "L0.rms1", 1.0, 0.1).numpy()
     w2 = S.normal((HID,), seed, "L0.rms2", 1.0, 0.1).numpy()
-    g = S.normal((tokens, FFN), seed, "L0.g").numpy()
-    u = S.normal((tokens, FFN), seed, "L0.u").numpy()
+    g = S.normal((mp, FFN), seed, "L0.g").numpy()
+    u = S.normal((mp, FFN), seed, "L0.u").numpy()
     Ws = {n: S.weights(kind, N // frac, K, seed, f"L0.{n}").numpy() for n, kind, N, K, _ in PREFILL_MATS}
     lm_rows = VOCAB // (8 * frac)
     lm = S.q6k_weights(lm_rows, HID, seed, "lm_head").numpy()
     t0 = time.perf_counter()
     planes = {"rms": O.rms_quant(x, w1, EPS), "attn": O.quantize_q8(attn), "rms2": O.rms_quant(x, w2, EPS),
               "swiglu": O.swiglu_quant(g, u)}
-    t_prod = time.perf_counter() - t0
+    t_prod = (time.perf_counter() - t0) * (M_TOK / mp)
+    # the matmuls read full-height planes (3314 rows; the sampled producer rows repeated)
+    full = {k: (np.resize(qs, (M_TOK, qs.shape[1])), np.resize(d, (M_TOK, d.shape[1]))) for k, (qs, d, _) in planes.items()}
     t0 = time.perf_counter()
     last = None
     for name, kind, N, K, src in PREFILL_MATS:
-        qs, d, _ = planes[src]
+        qs, d = full[src]
         last, _ = O.gemm_rows(qs, d, Ws[name], kind, N // frac, K)
     t_mat = (time.perf_counter() - t0) * frac
     t0 = time.perf_counter()
@@ -320,9 +380,23 @@ def oracle_sample_tok_s(tokens=2, frac=4, seed=0):
     O.gemm_rows(qs, d, lm, "q6k", lm_rows, HID)
     t_lm = (time.perf_counter() - t0) * (VOCAB / lm_rows)
     est = LAYERS * (t_prod + t_mat) + t_lm
-    sample = (f"{tokens} token(s): layer-0 producers in full, its 7 matmuls on 1/{frac} of their output rows "
-              f"(x{frac}), x{LAYERS} layers; lm_head on {lm_rows} of {VOCAB} rows (x{VOCAB / lm_rows:.1f})")
-    return tokens / est, est, sample
+    sample = (f"M={M_TOK}: one layer's 7 matmuls on 1/{frac} of their output rows (x{frac}) and its 4 producers "
+              f"on 1/{prod_frac} of the tokens (x{prod_frac}), x{LAYERS} layers; lm_head on {lm_rows} of {VOCAB} "
+              f"rows (x{VOCAB / lm_rows:.1f})")
+    return M_TOK / est, est, sample
+
+
+def oracle_one_core(frac, prod_frac):
+    """The same sample in a child process whose numpy may use one thread."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"v, est, s = bench.oracle_sample_tok_s(frac={frac}, prod_frac={prod_frac}); print(json.dumps([v, est]))")
+    try:
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        v, est = json.loads(r.stdout.strip().splitlines()[-1])
+        return {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle", "sample": f"as above, 1/{frac} rows"}
+    except Exception as e:   # a baseline figure, not the measurement: report why it is missing
+        return {"value": None, "unit": "tok/s", "cores": 1, "kind": "oracle", "error": str(e)[:200]}
 
 
 def cpu_cores():
@@ -383,17 +457,18 @@ def run_reference(args):
     if rank != 0:
         return 0
     for _ in range(args.warmup):
-        oracle_sample_tok_s(tokens=1, frac=16)
+        oracle_sample_tok_s(frac=64, prod_frac=64)
     vals, ests = [], []
     for _ in range(args.steps):
-        v, est, sample = oracle_sample_tok_s(tokens=1, frac=16)
+        v, est, sample = oracle_sample_tok_s(frac=64, prod_frac=64)
         vals.append(v)
         ests.append(est)
     value = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * statistics.median(ests),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
-            "data": "synthetic", "config": {"workload": "7B-shaped matmul stack, M=3314 (oracle sample)"},
+            "data": "synthetic", "config": {"workload": "7B-shaped matmul stack prefill (28 layers + lm_head), M=3314",
+                                            "oracle_sample": "each step a bounded sample of the step, extrapolated"},
             "cpu_baseline": {"value": value, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -605,6 +680,28 @@ def main():
                "stacked": "k|v and gate|up weights stored as one matrix each, one GEMV per pair",
                "streams": "the k|v GEMV runs on a second stream beside attn_q (both read only the rms plane)"}
 
+    # ---- decode as config 4 writes it: seven GEMVs a layer on one stream
+    dec_u = None
+    if not args.no_decode:
+        graph_u = capture_graph(st.decode_step_unstacked)
+        for _ in range(3):
+            graph_u.replay()
+        torch.cuda.synchronize()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(args.steps):
+            graph_u.replay()
+        d1.record(stream)
+        torch.cuda.synchronize()
+        dtu = max_over_ranks(d0.elapsed_time(d1) / args.steps, ws) * 1e-3
+        dec_u = {"workload": "14B-shaped decode sweep, 48 layers, M=1, seven GEMVs a layer on one stream",
+                 "GBps": ws * Stack.decode_bytes() / dtu / 1e9, "ms_per_token": dtu * 1e3,
+                 "hbm_frac": Stack.decode_bytes() / dtu / 1e9 / load_peaks()[2],
+                 "launches_per_token": Stack.LAUNCHES_PER_DECODE_UNSTACKED, "launch": "CUDA graph replay"}
+
+    # ---- the prefill producers alone, at the stack's shapes
+    prod = producer_rates(st, dev, stream) if rank == 0 else None
+
     # ---- end to end: inputs from pinned host memory, logits back to the host
     host_x = st.x.cpu().pin_memory()
     host_attn = st.attn.cpu().pin_memory()
@@ -625,7 +722,8 @@ def main():
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         v, est, sample = oracle_sample_tok_s()
-        cpu = {"value": v, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample}
+        cpu = {"value": v, "unit": "tok/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample,
+               "one_core": oracle_one_core(32, 64)}
 
     peak_sus, peak_burst, hbm, peak_kind = load_peaks()
     achieved = q4_f / q4_t / 1e12
@@ -644,6 +742,8 @@ def main():
                        "parallelism": f"replicas x{ws}"},
             "effective_tops": ws * Stack.prefill_flops() / (t_ms * 1e-3) / 1e12,
             "decode": dec,
+            "decode_unstacked": dec_u,
+            "producers": prod,
             "e2e": {"value": job_tok_s(ws, e2e_ms), "unit": "tok/s",
                     "h2d_bytes_per_step": host_x.numel() * 4 + host_attn.numel() * 4,
                     "d2h_bytes_per_step": VOCAB * 4},

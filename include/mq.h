@@ -208,7 +208,8 @@ int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
  * through the read-only path: it must not be written by a kernel still running
  * when mq_rms_quant's kernel starts (an event wait or a synchronization between
  * the two suffices; weights written by cudaMemcpy* or before the stream work
- * began are always safe). The GEMVs and GEMMs are ordinary launches.
+ * began are always safe). The GEMVs, the GEMMs and mq_prepack_q6k are ordinary
+ * launches.
  */
 int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
