@@ -29,7 +29,9 @@
 //
 // Tile: 128 weight rows (MMA M, TMEM lanes) x 192 tokens (MMA N): at N = 192 an
 // M = 128, K = 16 MMA with A in tensor memory keeps the tensor pipe ~92% busy
-// (N = 128: 67%; A from shared memory: at most 80%).
+// (N = 128: 67%; A from shared memory: at most 80%). With fewer than 192 tokens the
+// tile is the token count rounded up to 16 (a small batch, M in [2, 16), takes
+// N = 16): boxes, MMA and epilogue shrink with it, and the weight stream bounds.
 // Tensor memory (512 columns): two 192-column super-block accumulators (the
 // epilogue drains one while the MMAs fill the other), the weight operand slots
 // (4 slots of 32 columns: q4_K one K = 64 chunk each, q6_K one K = 32 quarter with
@@ -130,10 +132,10 @@ struct Work {
 };
 // nfast: weight-row tiles fastest (when the activation operand is the larger one, so
 // that each token tile's activations are read from memory once).
-__device__ __forceinline__ Work work_of(int u, int splits, int num_mt, int num_nt, bool nfast, int S) {
+__device__ __forceinline__ Work work_of(int u, int splits, int num_mt, int num_nt, bool nfast, int S, int bt) {
     const int t = u / splits, sp = u - t * splits;
     const int mt = nfast ? t / num_nt : t % num_mt, nt = nfast ? t % num_nt : t / num_mt;
-    return Work{mt * BT, nt * BW, (sp * S) / splits, ((sp + 1) * S) / splits};
+    return Work{mt * bt, nt * BW, (sp * S) / splits, ((sp + 1) * S) / splits};
 }
 
 // Non-suspending test of a phase (acquire semantics, like the waits).
@@ -214,14 +216,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                                            const __grid_constant__ CUtensorMap tmAf,
                                                            const __grid_constant__ CUtensorMap tmW,
                                                            float* __restrict__ out, int M, int N, int K, int splits,
-                                                           int nfast) {
+                                                           int nfast, int bt) {
     using C = Cfg<Q6>;
     constexpr int kRB = C::kRB, kRF = C::kRF;
     extern __shared__ uint8_t smem_raw[];
     Smem<Q6>& sm = *reinterpret_cast<Smem<Q6>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = K / mq::QK_K;
-    const int num_mt = (M + BT - 1) / BT, num_nt = (N + BW - 1) / BW;
+    const int num_mt = (M + bt - 1) / bt, num_nt = (N + BW - 1) / BW;
     const int units = num_mt * num_nt * splits;
 
     if (tid == 0) {
@@ -265,11 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             uint32_t issA = 0, phA = 0, issX = 0, phX = 0, issB = 0, phB = 0;   // copies in flight (for an abort)
             int sbc = 0, ga = 0;
             for (int u = blockIdx.x; u < units && !aborted(sm); u += gridDim.x) {
-                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S);
+                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt);
                 for (int sb = wk.sb0; sb < wk.sb1 && !aborted(sm); ++sb, ++sbc) {
                     const int x = sbc % RX;
                     if (!wait1(sm, &sm.ax_empty[x], ((sbc / RX) & 1) ^ 1)) break;
-                    tc::mbar_arrive_expect_tx(&sm.ax_full[x], kAxBytes + kAfBytes);
+                    tc::mbar_arrive_expect_tx(&sm.ax_full[x], (uint32_t)bt * (32 + 4));
                     tc::tma_load_2d(sm.ax[x], &tmAx, 16 * sb, wk.m0, &sm.ax_full[x]);
                     tc::tma_load_2d(sm.af[x], &tmAf, wk.m0, sb, &sm.ax_full[x]);
                     issX |= 1u << x;
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         const int a = ga % C::kRA;
                         const uint32_t pa = (ga / C::kRA) & 1;
                         if (!wait1(sm, &sm.act_empty[a], pa ^ 1)) { ok = false; break; }
-                        tc::mbar_arrive_expect_tx(&sm.act_full[a], kActBytes);
+                        tc::mbar_arrive_expect_tx(&sm.act_full[a], (uint32_t)bt * KS * 2);
                         tc::tma_load_2d(sm.act[a], &tmAct, sb * 256 + KS * j, wk.m0, &sm.act_full[a]);
                         issA |= 1u << a;
                         phA = (phA & ~(1u << a)) | (pa << a);
@@ -307,10 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             // the next group in the middle of the current one, with MMAs still queued: group
             // (sbc, j) for j = 0..3 is K chunk j of super-block sbc; after chunk 3 come the
             // super-block's q4_K min-term MMAs and the next super-block's accumulator slot.
-            const uint32_t idesc = tc::instr_desc(BW, BT, 0);
+            const uint32_t idesc = tc::instr_desc(BW, (uint32_t)bt, 0);
             int total = 0;   // super-blocks this CTA accumulates (the issuer needs no tile positions)
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
-                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S);
+                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt);
                 total += wk.sb1 - wk.sb0;
             }
             // readiness of chunk j of super-block sbc, whose activation slot is ga
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         int sbc = 0;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S);
+            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt);
             const int n = wk.n0 + r;
             for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb, ++sbc) {
                 const int b = sbc % kRB, x = sbc % RX;
@@ -553,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         int sbc = 0;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S);
+            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt);
             float acc[96];
 #pragma unroll
             for (int i = 0; i < 96; ++i) acc[i] = 0.0f;
@@ -570,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const uint32_t ta = tbase + lane_bits + (s ? kSCol1 : kSCol0) + 96 * ch;
 #pragma unroll
                 for (int cc = 0; cc < 3; ++cc) {
+                    if (96 * ch + 32 * cc >= bt) break;   // no token of the tile in these columns
                     uint32_t v[32];
                     tc::tmem_ld32(ta + 32 * cc, v);
                     tc::tmem_ld_wait();
@@ -700,6 +703,13 @@ bool gemm_ready(size_t smem) {
     return v == 1;
 }
 
+// Token-tile height: 192 tokens, or for fewer tokens the count rounded up to the
+// MMA's N granule of 16. A small batch (M in [2, 16) and beyond) then moves, multiplies
+// and reads back only the columns it has: the activation boxes, the MMA's N and the
+// epilogue's TMEM loads all shrink with it, and the kernel becomes bound by the
+// weight stream and its conversion rather than by work on empty columns.
+int token_tile(int M) { return M >= BT ? BT : ((M + 15) / 16) * 16; }
+
 template <bool Q6>
 int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     int rc = check_gemm(a, w, N, out);
@@ -712,13 +722,14 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
     if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row, (uint64_t)N, row, Cfg<Q6>::kRowBytes, BW))
         return MQ_ERR_LAUNCH;
     const int mp = mq::af_stride(M);
-    if (!make_map(&tmAct, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ah, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, KS, BT,
+    const int bt = token_tile(M);
+    if (!make_map(&tmAct, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ah, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, KS, bt,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tmAx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ax, (uint64_t)S * 16, (uint64_t)M, (uint64_t)S * 32, 16,
-                  BT, CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !make_map(&tmAf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->af, (uint64_t)mp, (uint64_t)S, (uint64_t)mp * 4, BT, 1))
+                  bt, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_map(&tmAf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->af, (uint64_t)mp, (uint64_t)S, (uint64_t)mp * 4, bt, 1))
         return MQ_ERR_LAUNCH;
-    const long long tiles = (long long)((M + BT - 1) / BT) * ((N + BW - 1) / BW);
+    const long long tiles = (long long)((M + bt - 1) / bt) * ((N + BW - 1) / BW);
     const int sms = mq::num_sms();
     const int splits = choose_splits(tiles, S, sms);
     if (splits > 1 && cudaMemsetAsync(out, 0, (size_t)M * N * sizeof(float), stream) != cudaSuccess)
@@ -727,7 +738,7 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
     const int grid = (int)(units < sms ? units : sms);
     // weight-row tiles fastest when the activations outweigh the weights
     const int nfast = (double)M * K * 2 > (double)N * row ? 1 : 0;
-    gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits, nfast);
+    gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits, nfast, bt);
     return mq::launch_status();
 }
 

@@ -88,6 +88,34 @@ def test_gemm_partial_last_wave_every_element(kind, M, N, K):
     _check(out, p, w, kind, N, K)
 
 
+@pytest.mark.parametrize("kind", ["q4k", "q6k"])
+@pytest.mark.parametrize("M", [2, 3, 8, 15])
+def test_gemm_small_batch_every_element(kind, M):
+    """Small batches, M in [2, 16): one 16-token tile (MMA N = 16), the weight rows split along
+    K across the SMs. Every element of a ragged, several-tile product within the bound."""
+    N, K = 1000, 3584
+    x = synth.with_outliers(synth.normal((M, K), 0, f"sbx{M}"), 0, f"sbo{M}")
+    out, p, w = _run(kind, x, N, K, mq.gemm)
+    _check(out, p, w, kind, N, K)
+
+
+@pytest.mark.parametrize("kind,N,K", [("q4k", 18944, 3584), ("q6k", 3584, 18944)])
+def test_gemm_small_batch_full_size(kind, N, K):
+    """M = 15 on the 7B FFN shapes, every element checked."""
+    M = 15
+    x = synth.normal((M, K), 0, f"sbf{K}", device="cuda")
+    w = synth.weights(kind, N, K, 0, f"sbfw{kind}{N}", device="cuda")
+    p = mq.Plane.empty(M, K)
+    mq.mq_quantize_q8(x, p)
+    g = Guarded((M, N), torch.float32)
+    mq.gemm(kind, p, mq.gemm_weights(kind, w, N, K), N, g.t)
+    torch.cuda.synchronize()
+    g.check()
+    assert g.untouched() == 0, "unwritten outputs"
+    _check(g.t, p, w, kind, N, K)
+    assert mq.mq_device_status() == mq.MQ_OK
+
+
 @pytest.mark.parametrize("kind,N,K", [("q4k", 18944, 3584), ("q6k", 3584, 18944), ("q4k", 512, 3584)])
 def test_gemm_full_size_sampled_rows(kind, N, K):
     """7B prefill shapes at M = 3314, oracle on 24 sampled rows (rows are independent); every
@@ -226,7 +254,7 @@ def _unit_activations(rng, M, K, small_first_half=False):
     return torch.from_numpy(x)
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 256, 512), (130, 200, 768), (300, 1100, 1280)])
+@pytest.mark.parametrize("M,N,K", [(16, 256, 512), (130, 200, 768), (300, 1100, 1280), (3, 300, 768), (8, 200, 1280)])
 def test_gemm_q4k_exact_integer_dots(M, N, K):
     """Unit super-block scales (d = dmin = 1), sub-block scales 0 or 1, mins 0..7 and d_a = 1:
     the operand form is exact (ah = 4q, block sums 4s, dmin/d = 1), every product and partial
@@ -256,7 +284,7 @@ def test_gemm_q4k_exact_integer_dots(M, N, K):
     assert np.array_equal(got, ref), f"max diff {np.max(np.abs(got - ref))}"
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 256, 256), (130, 200, 768), (64, 300, 1280)])
+@pytest.mark.parametrize("M,N,K", [(16, 256, 256), (130, 200, 768), (64, 300, 1280), (2, 300, 768), (15, 200, 1280)])
 def test_gemm_q6k_exact_integer_dots(M, N, K):
     """d = 1, sub-block scales +-1, and in sub-blocks 2j (the first half of each 32-block, where
     the activations lie in [-1, 1]) also scale -128 with high bits 0, so the operand's two exact
