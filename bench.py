@@ -485,13 +485,14 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- the shape/token sweep
 
-SWEEP_M = [1, 2, 3, 8, 15, 16, 64, 512, 3314, 8192]   # M in [2, 16): the small-batch GEMM path
+SWEEP_M = [1, 2, 3, 8, 15, 16, 64, 512, 3314, 8192]   # M in [2, 16): the small-batch paths
+MQ_GEMV_ROWS = 8   # the GEMV takes up to 8 activation rows; M in [2, 8] is timed through both calls
 SWEEP_NK = [(1024, 5120), (3584, 3584), (18944, 3584), (3584, 18944), (13824, 5120)]
 
 
 def run_sweep(steps: int, warmup: int):
-    """Time every (M, N, K, type) case of the sweep (activations with 1% x50 outliers), M = 1
-    through the decode GEMV, M >= 2 through the GEMM, with a 256 MB L2 flush before each timed
+    """Time every (M, N, K, type) case of the sweep (activations with 1% x50 outliers), M <= 8
+    through the GEMV, M >= 2 through the GEMM (both for M in [2, 8]), with a 256 MB L2 flush before each timed
     launch (a read, so that L2 holds no dirty lines whose write-back the timed kernel would pay). Each case's roofline is whichever of the tensor time (2MNK / measured bf16 burst peak)
     and the stream time (algorithmic bytes / measured HBM bandwidth) is larger; `frac` is that
     time over the measured one."""
@@ -511,33 +512,35 @@ def run_sweep(steps: int, warmup: int):
                 p = mq.Plane.empty(M, K, dev, op=M > 1)
                 mq.mq_quantize_q8(x, p)
                 out = torch.empty((M, N), dtype=torch.float32, device=dev)
-                if M == 1:
-                    fn = lambda: mq.gemv(kind, p, w, N, out.view(-1))
-                    act = plane_bytes(1, K) - (0 if kind == "q4k" else K // 32 * 4)
-                else:
-                    fn = lambda: mq.gemm(kind, p, wg, N, out)
-                    act = gemm_act_bytes(kind, M, K)
-                nbytes = wbytes(kind, N, K) + act + 4 * M * N
-                for _ in range(max(1, warmup)):
-                    fn()
-                ts = []
-                for _ in range(steps):
-                    flush.sum()
-                    torch.cuda._sleep(GPU_HOLD_CYCLES)
-                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                    a.record()
-                    fn()
-                    b.record()
-                    torch.cuda.synchronize()
-                    ts.append(a.elapsed_time(b) * 1e-3)
-                t = statistics.median(ts)
-                t_tensor = 2.0 * M * N * K / (peak_burst * 1e12)
-                t_stream = nbytes / (hbm * 1e9)
-                line = {"case": f"{'gemv' if M == 1 else 'gemm'}_{kind}:{M}x{N}x{K}", "us": t * 1e6,
-                        "TFLOPs": 2.0 * M * N * K / t / 1e12, "GBps": nbytes / t / 1e9,
-                        "bound": "tensor" if t_tensor >= t_stream else "hbm",
-                        "frac": max(t_tensor, t_stream) / t}
-                print(json.dumps(line))
+                paths = (["gemv"] if M <= MQ_GEMV_ROWS else []) + (["gemm"] if M > 1 else [])
+                for path in paths:
+                    if path == "gemv":
+                        fn = lambda: mq.gemv(kind, p, w, N, out)
+                        act = M * (plane_bytes(1, K, op=False) - (0 if kind == "q4k" else K // 32 * 4))
+                    else:
+                        fn = lambda: mq.gemm(kind, p, wg, N, out)
+                        act = gemm_act_bytes(kind, M, K)
+                    nbytes = wbytes(kind, N, K) + act + 4 * M * N
+                    for _ in range(max(1, warmup)):
+                        fn()
+                    ts = []
+                    for _ in range(steps):
+                        flush.sum()
+                        torch.cuda._sleep(GPU_HOLD_CYCLES)
+                        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        a.record()
+                        fn()
+                        b.record()
+                        torch.cuda.synchronize()
+                        ts.append(a.elapsed_time(b) * 1e-3)
+                    t = statistics.median(ts)
+                    t_tensor = 2.0 * M * N * K / (peak_burst * 1e12)
+                    t_stream = nbytes / (hbm * 1e9)
+                    line = {"case": f"{path}_{kind}:{M}x{N}x{K}", "us": t * 1e6,
+                            "TFLOPs": 2.0 * M * N * K / t / 1e12, "GBps": nbytes / t / 1e9,
+                            "bound": "tensor" if t_tensor >= t_stream else "hbm",
+                            "frac": max(t_tensor, t_stream) / t}
+                    print(json.dumps(line))
                 del x, p, out
     if mq.mq_device_status() != mq.MQ_OK:
         raise RuntimeError("device status")

@@ -45,12 +45,15 @@ extern "C" {
 enum {
     MQ_OK = 0,
     MQ_ERR_NULL = 1,    /* a required pointer is NULL */
-    MQ_ERR_SHAPE = 2,   /* K not a positive multiple of 256, negative M/N, plane dims mismatch, M != 1 for a GEMV */
+    MQ_ERR_SHAPE = 2,   /* K not a positive multiple of 256, negative M/N, plane dims mismatch, GEMV M outside [1, 8] */
     MQ_ERR_ALIGN = 3,   /* a pointer is not 16-byte aligned */
     MQ_ERR_ARCH = 4,    /* the current device is not a compute capability 10.3 (GB300) GPU */
     MQ_ERR_LAUNCH = 5,  /* the CUDA launch (or tensor-map encoding) failed */
     MQ_ERR_DEVICE = 6   /* a kernel gave up on a bounded wait (reported by mq_device_status) */
 };
+
+/* Most activation rows one mq_gemv_q4k / mq_gemv_q6k call takes. */
+#define MQ_GEMV_MAX_ROWS 8
 
 /*
  * q8 activation plane ([r52] §2.2; [D3-7] Excerpt C): for each row m and each
@@ -196,9 +199,19 @@ int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
 int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 
 /*
- * mq_gemv_q4k / mq_gemv_q6k — decode matrix-vector product (M == 1)
- * ([D3-7] §2 (2b) and Excerpt A/A2, the MMVQ decode path): the same result as
- * the GEMM with a->M == 1. out: f32 [N]. Returns MQ_ERR_SHAPE if a->M != 1.
+ * mq_gemv_q4k / mq_gemv_q6k — decode (M == 1) and small-batch
+ * (1 <= M <= MQ_GEMV_MAX_ROWS) matrix products ([D3-7] §2 (2b) and Excerpt
+ * A/A2, the MMVQ decode path): the same result as the GEMM, within the same
+ * bound. Integer dp4a block dots on the plane's q8 arrays (qs, d, s must be
+ * present; the operand arrays are not read). Each weight super-block is loaded
+ * and decoded once and dotted with every activation row, so a call streams the
+ * weights once whatever M is.
+ *   w   : raw q4_K / q6_K rows, N * (K/256) * 144 or 210 bytes (the q6_K GEMV
+ *         reads the raw layout, not mq_prepack_q6k's), 16-byte aligned.
+ *   out : f32 [M][N] row-major, written (not accumulated).
+ * Returns MQ_ERR_SHAPE if a->M is outside [1, MQ_GEMV_MAX_ROWS]. Between one row
+ * and the GEMM's region the caller picks the faster call per M: the GEMV's cost
+ * grows with M (its integer dot work), the GEMM's does not below 16 rows.
  *
  * Launch overlap: the three producers above are launched with programmatic
  * stream serialization, so each may start while the kernel enqueued before it

@@ -75,14 +75,17 @@ __device__ __forceinline__ void load_q4k(Q4Loads& L, const uint8_t* blk, size_t 
     }
 }
 
+// MR: activation rows handled per launch (M <= MR); each weight load is decoded
+// once and dotted with every row.
+template <int MR>
 __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __restrict__ W,
                                                             const int8_t* __restrict__ aq,
                                                             const float* __restrict__ ad,
                                                             const int32_t* __restrict__ as,
-                                                            float* __restrict__ out, int N, int K) {
+                                                            float* __restrict__ out, int N, int K, int M) {
     mq_grid_release();
     const int lane = threadIdx.x & 31;
-    const int S = K / mq::QK_K, nst = (S + 7) / 8;
+    const int S = K / mq::QK_K, nst = (S + 7) / 8, nb = K / mq::QK;
     const int g = lane >> 2, p = lane & 3;
     const bool hi = p >= 2;
     const uint32_t sh0 = 16u * (uint32_t)(p & 1), sh1 = sh0 + 8u;   // byte (2p mod 4), (2p+1 mod 4) of a word
@@ -94,58 +97,75 @@ __global__ void __launch_bounds__(kThreads) gemv_q4k_kernel(const uint8_t* __res
         const int row = 2 * pr;
         const bool two = row + 1 < N;
         const uint8_t* wr = W + (size_t)row * row_bytes;
-        float acc0 = 0.0f, acc1 = 0.0f;
+        float acc[2][MR];
+#pragma unroll
+        for (int m = 0; m < MR; ++m) acc[0][m] = acc[1][m] = 0.0f;
         Q4Loads cur;
         for (int st = 0; st < nst; ++st) {
             const int sb = 8 * st + g;
             if (sb < S) {
                 load_q4k(cur, wr + (size_t)sb * mq::Q4K_BYTES, row_bytes, two, p);
                 const int b0 = sb * 8 + 2 * p;
-                const int4* a = reinterpret_cast<const int4*>(aq + b0 * 32);   // blocks b0, b0 + 1: 4 x 16 bytes
-                const int4 a0 = __ldg(a), a1 = __ldg(a + 1), a2 = __ldg(a + 2), a3 = __ldg(a + 3);
-                const float2 da = __ldg(reinterpret_cast<const float2*>(ad + b0));
-                const int2 sv = __ldg(reinterpret_cast<const int2*>(as + b0));
+                int sc0[2], sc1[2], mn0[2], mn1[2];
+                float d[2], dmin[2];
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    if (r == 1 && !two) break;
-                    const uint4 q0 = cur.q0[r], q1 = cur.q1[r], hv = cur.hv[r];
-                    int I0 = __dp4a((int)(q0.x & m4), a0.x, 0);
-                    I0 = __dp4a((int)(q0.y & m4), a0.y, I0);
-                    I0 = __dp4a((int)(q0.z & m4), a0.z, I0);
-                    I0 = __dp4a((int)(q0.w & m4), a0.w, I0);
-                    I0 = __dp4a((int)(q1.x & m4), a1.x, I0);
-                    I0 = __dp4a((int)(q1.y & m4), a1.y, I0);
-                    I0 = __dp4a((int)(q1.z & m4), a1.z, I0);
-                    I0 = __dp4a((int)(q1.w & m4), a1.w, I0);
-                    int H = dp4a_us(q0.x & m4h, a2.x, 0);
-                    H = dp4a_us(q0.y & m4h, a2.y, H);
-                    H = dp4a_us(q0.z & m4h, a2.z, H);
-                    H = dp4a_us(q0.w & m4h, a2.w, H);
-                    H = dp4a_us(q1.x & m4h, a3.x, H);
-                    H = dp4a_us(q1.y & m4h, a3.y, H);
-                    H = dp4a_us(q1.z & m4h, a3.z, H);
-                    H = dp4a_us(q1.w & m4h, a3.w, H);
-                    const int I1 = H >> 4;   // exact: every term is a multiple of 16
-                    const uint32_t x0 = hv.y >> sh0, y0 = hv.z >> sh0, z0 = hv.w >> sh0;
-                    const uint32_t x1 = hv.y >> sh1, y1 = hv.z >> sh1, z1 = hv.w >> sh1;
-                    const int sc0 = (int)(hi ? ((z0 & 15u) | ((x0 >> 2) & 48u)) : (x0 & 63u));
-                    const int sc1 = (int)(hi ? ((z1 & 15u) | ((x1 >> 2) & 48u)) : (x1 & 63u));
-                    const int mn0 = (int)(hi ? (((z0 >> 4) & 15u) | ((y0 >> 2) & 48u)) : (y0 & 63u));
-                    const int mn1 = (int)(hi ? (((z1 >> 4) & 15u) | ((y1 >> 2) & 48u)) : (y1 & 63u));
-                    const float d = mq_f16_to_f32((uint16_t)(hv.x & 0xffffu));
-                    const float dmin = mq_f16_to_f32((uint16_t)(hv.x >> 16));
-                    const float v = d * (da.x * (float)(sc0 * I0) + da.y * (float)(sc1 * I1)) -
-                                    dmin * (da.x * (float)(mn0 * sv.x) + da.y * (float)(mn1 * sv.y));
-                    if (r == 0) acc0 += v;
-                    else acc1 += v;
+                for (int m = 0; m < MR; ++m) {
+                    if (m >= M) break;   // uniform
+                    const int4* a = reinterpret_cast<const int4*>(aq + (size_t)m * K + b0 * 32);   // blocks b0, b0 + 1
+                    const int4 a0 = __ldg(a), a1 = __ldg(a + 1), a2 = __ldg(a + 2), a3 = __ldg(a + 3);
+                    const float2 da = __ldg(reinterpret_cast<const float2*>(ad + (size_t)m * nb + b0));
+                    const int2 sv = __ldg(reinterpret_cast<const int2*>(as + (size_t)m * nb + b0));
+                    if (m == 0) {
+                        // per weight row, decoded once (after the first row's activation loads
+                        // are in flight): the 6-bit scales and mins of sub-blocks 2p, 2p+1, d, dmin
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const uint4 hv = cur.hv[r];
+                            const uint32_t x0 = hv.y >> sh0, y0 = hv.z >> sh0, z0 = hv.w >> sh0;
+                            const uint32_t x1 = hv.y >> sh1, y1 = hv.z >> sh1, z1 = hv.w >> sh1;
+                            sc0[r] = (int)(hi ? ((z0 & 15u) | ((x0 >> 2) & 48u)) : (x0 & 63u));
+                            sc1[r] = (int)(hi ? ((z1 & 15u) | ((x1 >> 2) & 48u)) : (x1 & 63u));
+                            mn0[r] = (int)(hi ? (((z0 >> 4) & 15u) | ((y0 >> 2) & 48u)) : (y0 & 63u));
+                            mn1[r] = (int)(hi ? (((z1 >> 4) & 15u) | ((y1 >> 2) & 48u)) : (y1 & 63u));
+                            d[r] = mq_f16_to_f32((uint16_t)(hv.x & 0xffffu));
+                            dmin[r] = mq_f16_to_f32((uint16_t)(hv.x >> 16));
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        if (r == 1 && !two) break;
+                        const uint4 q0 = cur.q0[r], q1 = cur.q1[r];
+                        int I0 = __dp4a((int)(q0.x & m4), a0.x, 0);
+                        I0 = __dp4a((int)(q0.y & m4), a0.y, I0);
+                        I0 = __dp4a((int)(q0.z & m4), a0.z, I0);
+                        I0 = __dp4a((int)(q0.w & m4), a0.w, I0);
+                        I0 = __dp4a((int)(q1.x & m4), a1.x, I0);
+                        I0 = __dp4a((int)(q1.y & m4), a1.y, I0);
+                        I0 = __dp4a((int)(q1.z & m4), a1.z, I0);
+                        I0 = __dp4a((int)(q1.w & m4), a1.w, I0);
+                        int H = dp4a_us(q0.x & m4h, a2.x, 0);
+                        H = dp4a_us(q0.y & m4h, a2.y, H);
+                        H = dp4a_us(q0.z & m4h, a2.z, H);
+                        H = dp4a_us(q0.w & m4h, a2.w, H);
+                        H = dp4a_us(q1.x & m4h, a3.x, H);
+                        H = dp4a_us(q1.y & m4h, a3.y, H);
+                        H = dp4a_us(q1.z & m4h, a3.z, H);
+                        H = dp4a_us(q1.w & m4h, a3.w, H);
+                        const int I1 = H >> 4;   // exact: every term is a multiple of 16
+                        acc[r][m] += d[r] * (da.x * (float)(sc0[r] * I0) + da.y * (float)(sc1[r] * I1)) -
+                                     dmin[r] * (da.x * (float)(mn0[r] * sv.x) + da.y * (float)(mn1[r] * sv.y));
+                    }
                 }
             }
         }
-        acc0 = warp_sum(acc0);
-        acc1 = warp_sum(acc1);
-        if (lane == 0) {
-            out[row] = acc0;
-            if (two) out[row + 1] = acc1;
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+            if (m >= M) break;
+            const float v0 = warp_sum(acc[0][m]), v1 = warp_sum(acc[1][m]);
+            if (lane == 0) {
+                out[(size_t)m * N + row] = v0;
+                if (two) out[(size_t)m * N + row + 1] = v1;
+            }
         }
     }
 }
@@ -208,11 +228,11 @@ __device__ __forceinline__ void q6_issue_chunk(uint32_t dst, const uint8_t* lo, 
 //   S = sum a,
 //   sum (q - 32) a = (L >> 4e) + 16 * (H >> 2p) - 32 * S,
 // every shift exact because each sum is a multiple of the power of two.
-template <int kQ6Stages>
+template <int kQ6Stages, int MR>
 __global__ void __launch_bounds__(32 * kQ6Rows) gemv_q6k_kernel(const uint8_t* __restrict__ W,
                                                                 const int8_t* __restrict__ aq,
                                                                 const float* __restrict__ ad,
-                                                                float* __restrict__ out, int N, int K) {
+                                                                float* __restrict__ out, int N, int K, int M) {
     __shared__ __align__(16) uint8_t stage[kQ6Rows][kQ6Stages][kQ6ChunkBytes];
     mq_grid_release();
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -246,7 +266,10 @@ __global__ void __launch_bounds__(32 * kQ6Rows) gemv_q6k_kernel(const uint8_t* _
     const int shl0 = 4 - 2 * qq, shr1 = 2 * qq;
     const int8_t* aql = aq + blk0 * 32 + 16 * h;            // + 256 per super-block; quarter qq+2 at +64
     const float* adl = ad + blk0;                           // + 8 per super-block; quarter qq+2 at +2
-    float acc = 0.0f;
+    const int nb = K / mq::QK;
+    float acc[MR];
+#pragma unroll
+    for (int m = 0; m < MR; ++m) acc[m] = 0.0f;
     int stg = 0;
     for (int c = 0; c < nc; ++c) {
         const int cn = c + kQ6Stages - 1;
@@ -280,35 +303,45 @@ __global__ void __launch_bounds__(32 * kQ6Rows) gemv_q6k_kernel(const uint8_t* _
                 const int sc1 = tc::lds_s8(blk + 192 + g1);
                 const float d = mq_f16_to_f32((uint16_t)tc::lds_u16(blk + 208));
                 const int sb = c * kQ6Chunk + j;
-                const int4 a0 = __ldg(reinterpret_cast<const int4*>(aql + sb * 256));
-                const int4 a1 = __ldg(reinterpret_cast<const int4*>(aql + sb * 256 + 64));
-                const int a0w[4] = {a0.x, a0.y, a0.z, a0.w};
-                const int a1w[4] = {a1.x, a1.y, a1.z, a1.w};
-                int L0 = 0, L1 = 0, H0 = 0, H1 = 0, S0 = 0, S1 = 0;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    L0 = dp4a_us(ql[i] & 0x0F0F0F0Fu, a0w[i], L0);
-                    L1 = dp4a_us(ql[i] & 0xF0F0F0F0u, a1w[i], L1);
-                    H0 = dp4a_us(qh[i] & mh0, a0w[i], H0);
-                    H1 = dp4a_us(qh[i] & mh1, a1w[i], H1);
-                    S0 = __dp4a(0x01010101, a0w[i], S0);
-                    S1 = __dp4a(0x01010101, a1w[i], S1);
+                for (int m = 0; m < MR; ++m) {
+                    if (m >= M) break;   // uniform
+                    const int8_t* am = aql + (size_t)m * K + sb * 256;
+                    const int4 a0 = __ldg(reinterpret_cast<const int4*>(am));
+                    const int4 a1 = __ldg(reinterpret_cast<const int4*>(am + 64));
+                    const int a0w[4] = {a0.x, a0.y, a0.z, a0.w};
+                    const int a1w[4] = {a1.x, a1.y, a1.z, a1.w};
+                    int L0 = 0, L1 = 0, H0 = 0, H1 = 0, S0 = 0, S1 = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        L0 = dp4a_us(ql[i] & 0x0F0F0F0Fu, a0w[i], L0);
+                        L1 = dp4a_us(ql[i] & 0xF0F0F0F0u, a1w[i], L1);
+                        H0 = dp4a_us(qh[i] & mh0, a0w[i], H0);
+                        H1 = dp4a_us(qh[i] & mh1, a1w[i], H1);
+                        S0 = __dp4a(0x01010101, a0w[i], S0);
+                        S1 = __dp4a(0x01010101, a1w[i], S1);
+                    }
+                    const int I0 = L0 + (H0 << shl0) - (S0 << 5);
+                    const int I1 = (L1 >> 4) + (H1 >> shr1) - (S1 << 5);
+                    const float* adm = adl + (size_t)m * nb + sb * 8;
+                    acc[m] += d * (__ldg(adm) * (float)(sc0 * I0) + __ldg(adm + 2) * (float)(sc1 * I1));
                 }
-                const int I0 = L0 + (H0 << shl0) - (S0 << 5);
-                const int I1 = (L1 >> 4) + (H1 >> shr1) - (S1 << 5);
-                acc += d * (__ldg(adl + sb * 8) * (float)(sc0 * I0) + __ldg(adl + sb * 8 + 2) * (float)(sc1 * I1));
             }
         }
         __syncwarp();   // buffer stg is read by every lane before it is refilled
         stg = stg == kQ6Stages - 1 ? 0 : stg + 1;
     }
-    acc = warp_sum(acc);
-    if (lane == 0) out[row] = acc;
+#pragma unroll
+    for (int m = 0; m < MR; ++m) {
+        if (m >= M) break;
+        const float v = warp_sum(acc[m]);
+        if (lane == 0) out[(size_t)m * N + row] = v;
+    }
 }
 
 int check_gemv(const mq_q8_plane* a, const void* w, int N, const float* out) {
     if (!a) return MQ_ERR_NULL;
-    if (N < 0 || a->M != 1 || !mq::valid_k(a->K)) return MQ_ERR_SHAPE;
+    if (N < 0 || a->M < 1 || a->M > MQ_GEMV_MAX_ROWS || !mq::valid_k(a->K)) return MQ_ERR_SHAPE;
     int rc = mq::check_plane(a, a->M, a->K);
     if (rc != MQ_OK || N == 0) return rc;
     if (!mq::has_q8(a) || !w || !out) return MQ_ERR_NULL;
@@ -347,15 +380,26 @@ int take_gemv_device_error(cudaStream_t, unsigned* code) {
 extern "C" int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     int rc = check_gemv(a, w, N, out);
     if (rc != MQ_OK || N == 0) return rc;
-    return mq::launch_plain(gemv_q4k_kernel, dim3(gemv_grid((N + 1) / 2, gemv_q4k_kernel)), dim3(kThreads), 0, stream,
-                          static_cast<const uint8_t*>(w), a->qs, a->d, a->s, out, N, a->K);
+    auto go = [&](auto kern) {
+        return mq::launch_plain(kern, dim3(gemv_grid((N + 1) / 2, kern)), dim3(kThreads), 0,
+                                stream, static_cast<const uint8_t*>(w), a->qs, a->d, a->s, out, N, a->K, a->M);
+    };
+    const int M = a->M;
+    return M == 1 ? go(gemv_q4k_kernel<1>) : M == 2 ? go(gemv_q4k_kernel<2>) : M <= 4 ? go(gemv_q4k_kernel<4>)
+                                                                                  : go(gemv_q4k_kernel<8>);
 }
 
 extern "C" int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     int rc = check_gemv(a, w, N, out);
     if (rc != MQ_OK || N == 0) return rc;
     const int chunks = (a->K / mq::QK_K + kQ6Chunk - 1) / kQ6Chunk;
-    return mq::launch_plain(chunks <= 3 ? gemv_q6k_kernel<4> : gemv_q6k_kernel<3>, dim3((N + kQ6Rows - 1) / kQ6Rows),
-                          dim3(32 * kQ6Rows), 0, stream,
-                          static_cast<const uint8_t*>(w), a->qs, a->d, out, N, a->K);
+    auto go = [&](auto k4, auto k3) {
+        return mq::launch_plain(chunks <= 3 ? k4 : k3, dim3((N + kQ6Rows - 1) / kQ6Rows), dim3(32 * kQ6Rows), 0,
+                                stream, static_cast<const uint8_t*>(w), a->qs, a->d, out, N, a->K, a->M);
+    };
+    const int M = a->M;
+    return M == 1   ? go(gemv_q6k_kernel<4, 1>, gemv_q6k_kernel<3, 1>)
+           : M == 2 ? go(gemv_q6k_kernel<4, 2>, gemv_q6k_kernel<3, 2>)
+           : M <= 4 ? go(gemv_q6k_kernel<4, 4>, gemv_q6k_kernel<3, 4>)
+                    : go(gemv_q6k_kernel<4, 8>, gemv_q6k_kernel<3, 8>);
 }

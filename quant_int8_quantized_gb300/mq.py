@@ -17,6 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libmq.so")
 
 MQ_OK, MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_ARCH, MQ_ERR_LAUNCH, MQ_ERR_DEVICE = range(7)
+MQ_GEMV_MAX_ROWS = 8   # include/mq.h
 
 EXPORTED = ["mq_plane_bytes", "mq_q4k_row_bytes", "mq_q6k_row_bytes", "mq_q6k_packed_row_bytes", "mq_prepack_q6k",
             "mq_quantize_q8", "mq_rms_quant",
@@ -210,6 +211,8 @@ def mq_swiglu_quant(g: torch.Tensor, u: torch.Tensor, out: Plane, stream=None) -
 def _matmul(fn_name: str, a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream):
     _dev_tensor(w, torch.uint8, "w")
     _dev_tensor(out, torch.float32, "out")
+    if out.numel() < a.M * N:
+        raise ValueError(f"{fn_name}: out holds {out.numel()} floats, needs M * N = {a.M * N}")
     cp = a.c()
     _check(getattr(lib(), fn_name)(ctypes.byref(cp), _ptr(w), int(N), _ptr(out), _stream(stream)), fn_name)
     return out

@@ -92,9 +92,10 @@ def test_validation_before_any_cuda_call(L):
 
 def test_matmul_validation_before_any_cuda_call(L):
     null = None
-    p = _plane(2, 512, 16, 16, 16)
+    p = _plane(mq.MQ_GEMV_MAX_ROWS + 1, 512, 16, 16, 16)
     for fn in (L.mq_gemv_q4k, L.mq_gemv_q6k):
-        assert fn(ctypes.byref(p), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE  # M != 1
+        assert fn(ctypes.byref(p), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE  # M > 8
+        assert fn(ctypes.byref(_plane(0, 512, 16, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE
     p1 = _plane(1, 512, 16, 16, 16, 16, 16, 16)
     for fn in (L.mq_gemm_q4k, L.mq_gemm_q6k, L.mq_gemv_q4k, L.mq_gemv_q6k):
         assert fn(None, ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL

@@ -142,6 +142,40 @@ GEMV_SHAPES = [(256, 512), (1024, 5120), (100, 768), (5120, 13824), (1, 256), (7
 
 
 @pytest.mark.parametrize("kind", ["q4k", "q6k"])
+@pytest.mark.parametrize("M", [2, 3, 5, 8])
+def test_gemv_small_batch_every_element(kind, M):
+    """The GEMV with M activation rows (each weight super-block decoded once, dotted with every
+    row): every element within the bound, and each row bit-identical to a one-row call on it
+    (the per-row summation order does not depend on M)."""
+    N, K = 1000, 3584
+    x = synth.with_outliers(synth.normal((M, K), 0, f"vbx{M}"), 0, f"vbo{M}")
+    out, p, w = _run(kind, x, N, K, mq.gemv)
+    _check(out, p, w, kind, N, K)
+    wd = w.cuda()
+    for m in range(M):
+        pm = mq.Plane(p.qs[m:m + 1], p.d[m:m + 1], p.s[m:m + 1])
+        om = torch.empty(N, device="cuda")
+        mq.gemv(kind, pm, wd, N, om)
+        assert torch.equal(om, out[m]), f"row {m}"
+
+
+@pytest.mark.parametrize("kind,N,K", [("q4k", 13824, 5120), ("q6k", 5120, 13824)])
+def test_gemv_small_batch_full_size(kind, N, K):
+    """M = 8 (the largest GEMV batch) on the 14B FFN shapes, every element checked."""
+    M = 8
+    x = synth.normal((M, K), 0, f"vbf{K}", device="cuda")
+    w = synth.weights(kind, N, K, 0, f"vbfw{kind}{N}", device="cuda")
+    p = mq.Plane.empty(M, K, op=False)
+    mq.mq_quantize_q8(x, p)
+    g = Guarded((M, N), torch.float32)
+    mq.gemv(kind, p, w, N, g.t)
+    torch.cuda.synchronize()
+    g.check()
+    assert g.untouched() == 0, "unwritten outputs"
+    _check(g.t, p, w, kind, N, K)
+
+
+@pytest.mark.parametrize("kind", ["q4k", "q6k"])
 @pytest.mark.parametrize("N,K", GEMV_SHAPES)
 def test_gemv_parity(kind, N, K):
     x = synth.normal((1, K), 0, f"vx{K}")
@@ -211,10 +245,11 @@ def test_gemv_matches_gemm_at_one_row(kind):
     assert np.all(np.abs(a.cpu().numpy() - b.cpu().numpy()) <= 2 * bound)
 
 
-def test_gemv_rejects_multi_row_plane():
-    p = mq.Plane.empty(2, 256)
+def test_gemv_rejects_more_rows_than_it_takes():
+    M = mq.MQ_GEMV_MAX_ROWS + 1
+    p = mq.Plane.empty(M, 256)
     w = torch.zeros((8, 144), dtype=torch.uint8, device="cuda")
-    out = torch.empty(8, device="cuda")
+    out = torch.empty((M, 8), device="cuda")
     with pytest.raises(mq.MQError) as e:
         mq.mq_gemv_q4k(p, w, 8, out)
     assert e.value.status == mq.MQ_ERR_SHAPE
