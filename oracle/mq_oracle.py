@@ -39,15 +39,29 @@ Readings taken where the pages are silent:
   R11 the GEMM/GEMV error bound is per output element:
       |gpu - oracle| <= 1e-3 * sum_k |a[m,k]| * |w[n,k]|, a the dequantized q8
       activation.
+  R21 q5_K super-block byte order (the pages name the type only, in the decode
+      dispatch): the GGUF block of that name, 176 bytes: d (f16), dmin (f16),
+      the 12-byte scale/min field packed as in q4_K, 32 bytes qh of fifth bits,
+      128 bytes of nibbles. Element e = 64j + l (l < 32) takes the low nibble of
+      byte 32j + l and bit 2j of qh[l]; element 64j + 32 + l the high nibble and
+      bit 2j + 1. w = d * sc[e/32] * q - dmin * m[e/32], q in 0..31.
+  R22 q4_0 block byte order (the pages name the type only, in the prefill
+      dispatch list): 18 bytes per 32 elements, d (f16) then 16 bytes; element l
+      (l < 16) is the low nibble of byte l, element 16 + l the high nibble;
+      w = d * (q - 8).
+  R23 q4_1 block byte order: 20 bytes per 32 elements, d (f16), m (f16), then
+      16 bytes of nibbles placed as in q4_0; w = d * q + m.
   R20 the prefill GEMM reads the activations in an operand form derived from
       the plane (operand_form): each row's super-block of dequantized values
       d * q, scaled by a power of two and rounded to binary16, with its exact
       per-block sums and the power of two. The pages' GEMM consumes the int8
       plane directly; this form is what the f16 tensor pipe multiplies.
 
-Parity pins live in tests/test_oracle.py (closed forms, hand-built blocks,
-invariants, brute force). Parity unpinned: whether R1/R2 match the byte order
-of real GGUF files (no such file is available).
+Parity pins live in tests/test_oracle.py, tests/test_oracle_order_pins.py,
+tests/test_oracle_operand_form.py and tests/test_oracle_block_types.py (closed
+forms, hand-built blocks, invariants, brute force). Parity unpinned: whether
+R1/R2/R21-R23 match the byte order of real GGUF files (no such file is
+available).
 """
 from __future__ import annotations
 
@@ -59,6 +73,9 @@ QK = 32            # activation block length (q8)
 QK_K = 256         # weight super-block length
 Q4K_BYTES = 144    # d (f16), dmin (f16), 12 bytes of packed 6-bit scales/mins, 128 bytes of nibbles
 Q6K_BYTES = 210    # 128 bytes low nibbles, 64 bytes high 2-bit pairs, 16 int8 scales, d (f16)
+Q5K_BYTES = 176    # d, dmin (f16), 12 bytes of packed 6-bit scales/mins, 32 bytes of fifth bits, 128 of nibbles
+Q4_0_BYTES = 18    # per 32 elements: d (f16), 16 bytes of nibbles
+Q4_1_BYTES = 20    # per 32 elements: d (f16), m (f16), 16 bytes of nibbles
 
 
 # --------------------------------------------------------------------------- f16
@@ -153,8 +170,61 @@ def dequant_q6k(w: np.ndarray, N: int, K: int) -> np.ndarray:
     return out.reshape(N, K)
 
 
+# --------------------------------------------------------------------------- q5_K (R21)
+
+def q5k_fields(w: np.ndarray, N: int, K: int):
+    """Split raw q5_K bytes [N, K/256*176] into d, dmin [N,S], sc, mn [N,S,8], q [N,S,256]."""
+    S = K // QK_K
+    blk = np.asarray(w, np.uint8).reshape(N, S, Q5K_BYTES)
+    d = f16_bits_to_f64(_u16_le(blk[..., 0], blk[..., 1]))
+    dmin = f16_bits_to_f64(_u16_le(blk[..., 2], blk[..., 3]))
+    sc, mn = q4k_scales_mins(blk[..., 4:16])
+    qh = blk[..., 16:48].astype(np.int64)
+    qs = blk[..., 48:176].astype(np.int64)
+    q = np.zeros((N, S, QK_K), np.int64)
+    for j in range(4):
+        nib = qs[..., 32 * j:32 * j + 32]
+        q[..., 64 * j:64 * j + 32] = (nib & 15) | (((qh >> (2 * j)) & 1) << 4)
+        q[..., 64 * j + 32:64 * j + 64] = (nib >> 4) | (((qh >> (2 * j + 1)) & 1) << 4)
+    return d, dmin, sc, mn, q
+
+
+def dequant_q5k(w: np.ndarray, N: int, K: int) -> np.ndarray:
+    """w[n,k] = d * sc[j] * q - dmin * m[j], j = (k mod 256) / 32, q in 0..31. f64 [N, K]."""
+    d, dmin, sc, mn, q = q5k_fields(w, N, K)
+    j = np.arange(QK_K) // QK
+    out = d[..., None] * sc[..., j] * q - dmin[..., None] * mn[..., j]
+    return out.reshape(N, K)
+
+
+# --------------------------------------------------------------------------- q4_0, q4_1 (R22, R23)
+
+def _nibbles32(qs: np.ndarray) -> np.ndarray:
+    """16 bytes -> 32 four-bit values: low nibbles first (elements 0..15), then high."""
+    q = qs.astype(np.int64)
+    return np.concatenate([q & 15, q >> 4], axis=-1)
+
+
+def dequant_q4_0(w: np.ndarray, N: int, K: int) -> np.ndarray:
+    """w[n,k] = d * (q - 8) per block of 32. f64 [N, K]."""
+    blk = np.asarray(w, np.uint8).reshape(N, K // QK, Q4_0_BYTES)
+    d = f16_bits_to_f64(_u16_le(blk[..., 0], blk[..., 1]))
+    q = _nibbles32(blk[..., 2:18])
+    return (d[..., None] * (q - 8)).reshape(N, K)
+
+
+def dequant_q4_1(w: np.ndarray, N: int, K: int) -> np.ndarray:
+    """w[n,k] = d * q + m per block of 32. f64 [N, K]."""
+    blk = np.asarray(w, np.uint8).reshape(N, K // QK, Q4_1_BYTES)
+    d = f16_bits_to_f64(_u16_le(blk[..., 0], blk[..., 1]))
+    m = f16_bits_to_f64(_u16_le(blk[..., 2], blk[..., 3]))
+    q = _nibbles32(blk[..., 4:20])
+    return (d[..., None] * q + m[..., None]).reshape(N, K)
+
+
 def dequant(kind: str, w: np.ndarray, N: int, K: int) -> np.ndarray:
-    return {"q4k": dequant_q4k, "q6k": dequant_q6k}[kind](w, N, K)
+    return {"q4k": dequant_q4k, "q6k": dequant_q6k, "q5k": dequant_q5k, "q4_0": dequant_q4_0,
+            "q4_1": dequant_q4_1}[kind](w, N, K)
 
 
 # --------------------------------------------------------------------------- q8 activations

@@ -3,7 +3,7 @@
 This module is shared by the CUDA-path tests, the bench and the CPU oracle's
 callers. It holds none of the method's arithmetic: it only draws seeded random
 numbers and places them into the input layouts (f32 activations, raw q4_K /
-q6_K super-block bytes).
+q6_K / q5_K super-block bytes, raw q4_0 / q4_1 block bytes).
 
 Every tensor is drawn from its own stream, seeded by (seed, name), so a tensor
 does not depend on which other tensors were drawn before it.
@@ -18,6 +18,13 @@ tensors of the same shapes stand in for them):
   * q6_K super-block (210 B): every byte uniform, so the 6-bit quants are
     uniform in 0..63 and the int8 sub-block scales uniform in -128..127; then
     bytes 208..209 (d) are overwritten with f16 |N(0, 0.01)|;
+  * q5_K super-block (176 B): every byte uniform (nibbles and fifth bits, so q
+    is uniform in 0..31; scales and mins as in q4_K); bytes 0..1 (d) and 2..3
+    (dmin) overwritten with f16 |N(0, 0.01)|;
+  * q4_0 block (18 B per 32): nibbles uniform; d (bytes 0..1) f16 N(0, 0.01)
+    (signed, as a q4_0 quantizer emits);
+  * q4_1 block (20 B per 32): nibbles uniform; d f16 |N(0, 0.01)|, m f16
+    N(0, 0.08);
   * "outlier" activations: each entry independently multiplied by 50 with
     probability 0.01.
 """
@@ -29,6 +36,9 @@ import torch
 
 Q4K_BLOCK_BYTES = 144
 Q6K_BLOCK_BYTES = 210
+Q5K_BLOCK_BYTES = 176
+Q4_0_BLOCK_BYTES = 18
+Q4_1_BLOCK_BYTES = 20
 QK_K = 256
 
 
@@ -64,6 +74,11 @@ def _f16_abs_normal(n: int, std: float, g: torch.Generator, device) -> torch.Ten
     return v.to(torch.float16).view(torch.uint8).view(n, 2)
 
 
+def _f16_normal(n: int, std: float, g: torch.Generator, device) -> torch.Tensor:
+    v = torch.randn((n,), generator=g, dtype=torch.float32, device=device).mul_(std)
+    return v.to(torch.float16).view(torch.uint8).view(n, 2)
+
+
 def _random_bytes(n: int, g: torch.Generator, device) -> torch.Tensor:
     return torch.randint(0, 256, (n,), generator=g, dtype=torch.uint8, device=device)
 
@@ -89,9 +104,41 @@ def q6k_weights(N: int, K: int, seed: int, name: str, device="cpu") -> torch.Ten
     return w.view(N, S * Q6K_BLOCK_BYTES)
 
 
+def q5k_weights(N: int, K: int, seed: int, name: str, device="cpu") -> torch.Tensor:
+    """Raw q5_K bytes for an N x K weight, shape [N, K/256*176], uint8."""
+    assert K % QK_K == 0
+    S = K // QK_K
+    g = _generator(seed, name, device)
+    w = _random_bytes(N * S * Q5K_BLOCK_BYTES, g, device).view(N * S, Q5K_BLOCK_BYTES)
+    w[:, 0:2] = _f16_abs_normal(N * S, 0.01, g, device)
+    w[:, 2:4] = _f16_abs_normal(N * S, 0.01, g, device)
+    return w.view(N, S * Q5K_BLOCK_BYTES)
+
+
+def q4_0_weights(N: int, K: int, seed: int, name: str, device="cpu") -> torch.Tensor:
+    """Raw q4_0 bytes for an N x K weight, shape [N, K/32*18], uint8."""
+    assert K % 32 == 0
+    B = K // 32
+    g = _generator(seed, name, device)
+    w = _random_bytes(N * B * Q4_0_BLOCK_BYTES, g, device).view(N * B, Q4_0_BLOCK_BYTES)
+    w[:, 0:2] = _f16_normal(N * B, 0.01, g, device)
+    return w.view(N, B * Q4_0_BLOCK_BYTES)
+
+
+def q4_1_weights(N: int, K: int, seed: int, name: str, device="cpu") -> torch.Tensor:
+    """Raw q4_1 bytes for an N x K weight, shape [N, K/32*20], uint8."""
+    assert K % 32 == 0
+    B = K // 32
+    g = _generator(seed, name, device)
+    w = _random_bytes(N * B * Q4_1_BLOCK_BYTES, g, device).view(N * B, Q4_1_BLOCK_BYTES)
+    w[:, 0:2] = _f16_abs_normal(N * B, 0.01, g, device)
+    w[:, 2:4] = _f16_normal(N * B, 0.08, g, device)
+    return w.view(N, B * Q4_1_BLOCK_BYTES)
+
+
 def weights(kind: str, N: int, K: int, seed: int, name: str, device="cpu") -> torch.Tensor:
-    if kind == "q4k":
-        return q4k_weights(N, K, seed, name, device)
-    if kind == "q6k":
-        return q6k_weights(N, K, seed, name, device)
-    raise ValueError(kind)
+    gen = {"q4k": q4k_weights, "q6k": q6k_weights, "q5k": q5k_weights, "q4_0": q4_0_weights,
+           "q4_1": q4_1_weights}
+    if kind not in gen:
+        raise ValueError(kind)
+    return gen[kind](N, K, seed, name, device)
