@@ -55,7 +55,7 @@ DECODE_MATS = [("q", "q4k", D_HID, D_HID), ("k", "q6k", D_KV, D_HID), ("v", "q6k
 # Decode storage: projections that read the same plane and share a quant type are stored as one
 # stacked matrix and run as one GEMV (k|v, gate|up); the rows, bytes and products are the same.
 DECODE_STACKS = [("q", ("q",)), ("kv", ("k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")), ("down", ("down",))]
-BYTES_PER_SB = {"q4k": 144, "q6k": 210}
+BYTES_PER_SB = {"q4k": 144, "q6k": 210, "q5k": 176, "q4_0": 8 * 18, "q4_1": 8 * 20}   # bytes per 256 weights
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one gemm_kernel<q4_K> launch at
 # 3314 x 18944 x 3584, from one ncu capture (summary under profiles/). It describes the device code
@@ -542,6 +542,33 @@ def run_sweep(steps: int, warmup: int):
                             "frac": max(t_tensor, t_stream) / t}
                     print(json.dumps(line))
                 del x, p, out
+    # the other block types (GEMV only) on the 14B decode shapes
+    for kind in ("q5k", "q4_0", "q4_1"):
+        for N, K in [(5120, 5120), (1024, 5120), (13824, 5120), (5120, 13824)]:
+            w = S.weights(kind, N, K, 0, f"sweep.{kind}.{N}x{K}", device=dev)
+            for M in (1, 2, 8):
+                x = S.normal((M, K), 0, f"sweep.x.{M}x{K}", device=dev)
+                p = mq.Plane.empty(M, K, dev, op=False)
+                mq.mq_quantize_q8(x, p)
+                out = torch.empty((M, N), dtype=torch.float32, device=dev)
+                fn = lambda: mq.gemv(kind, p, w, N, out)
+                nbytes = wbytes(kind, N, K) + M * plane_bytes(1, K, op=False) + 4 * M * N
+                for _ in range(max(1, warmup)):
+                    fn()
+                ts = []
+                for _ in range(steps):
+                    flush.sum()
+                    torch.cuda._sleep(GPU_HOLD_CYCLES)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    fn()
+                    b.record()
+                    torch.cuda.synchronize()
+                    ts.append(a.elapsed_time(b) * 1e-3)
+                t = statistics.median(ts)
+                print(json.dumps({"case": f"gemv_{kind}:{M}x{N}x{K}", "us": t * 1e6, "GBps": nbytes / t / 1e9,
+                                  "bound": "hbm", "frac": nbytes / (hbm * 1e9) / t}))
+                del x, p, out
     if mq.mq_device_status() != mq.MQ_OK:
         raise RuntimeError("device status")
     return 0
@@ -562,7 +589,7 @@ def run_case(spec: str, steps: int, warmup: int):
     peak_sus, peak_burst, hbm, peak_kind = load_peaks()
     if kind.startswith("gemm") or kind.startswith("gemv"):
         M, N, K = dims
-        wk = kind[-3:]
+        wk = kind.split("_", 1)[1]
         x = S.normal((M, K), 0, "case.x", device=dev)
         w = S.weights(wk, N, K, 0, "case.w", device=dev)
         p = mq.Plane.empty(M, K, dev)
@@ -571,7 +598,7 @@ def run_case(spec: str, steps: int, warmup: int):
         wg = mq.gemm_weights(wk, w, N, K) if kind.startswith("gemm") else w
         fn = (lambda: mq.gemm(wk, p, wg, N, out)) if kind.startswith("gemm") else (lambda: mq.gemv(wk, p, w, N, out))
         flops = 2.0 * M * N * K
-        act = gemm_act_bytes(wk, M, K) if kind.startswith("gemm") else plane_bytes(M, K) - (0 if wk == "q4k" else M * (K // 32) * 4)
+        act = gemm_act_bytes(wk, M, K) if kind.startswith("gemm") else plane_bytes(M, K) - (0 if wk != "q6k" else M * (K // 32) * 4)
         nbytes = wbytes(wk, N, K) + act + 4 * M * N
     else:
         M, K = dims

@@ -228,6 +228,32 @@ int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
 int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 
 /*
+ * mq_gemv_q5k / mq_gemv_q4_0 / mq_gemv_q4_1 — the same decode / small-batch
+ * product for the other block types the pages dispatch: q5_K in the decode
+ * arm ([D3-7] Excerpt B), Q4_0 / Q4_1 in the matmul dispatch list ([r60]
+ * §3.2). The pages name these types but print no layout; the library reads the
+ * GGUF blocks of those names:
+ *   q5_K : 176 bytes per 256 elements — d (f16), dmin (f16), the 12-byte
+ *          scale/min field packed as in q4_K, 32 bytes qh, 128 bytes of
+ *          nibbles. Element 64j + l (l < 32) is the low nibble of byte 32j + l
+ *          plus 16 * (bit 2j of qh[l]); element 64j + 32 + l the high nibble plus
+ *          16 * (bit 2j + 1 of qh[l]). w = d * sc * q - dmin * m.
+ *   q4_0 : 18 bytes per 32 elements — d (f16), 16 bytes; element l < 16 is the
+ *          low nibble of byte l, element 16 + l its high nibble. w = d * (q - 8).
+ *   q4_1 : 20 bytes per 32 elements — d (f16), m (f16), 16 bytes as q4_0.
+ *          w = d * q + m.
+ * Row bytes: mq_q5k_row_bytes(K) = K/256 * 176, mq_q4_0_row_bytes(K) = K/32 * 18,
+ * mq_q4_1_row_bytes(K) = K/32 * 20. Arguments, errors and the 1..8 rows of `a`
+ * as for mq_gemv_q4k; out f32 [M][N]; within the same bound.
+ */
+size_t mq_q5k_row_bytes(int K);
+size_t mq_q4_0_row_bytes(int K);
+size_t mq_q4_1_row_bytes(int K);
+int mq_gemv_q5k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+int mq_gemv_q4_0(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+int mq_gemv_q4_1(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+
+/*
  * mq_device_status — synchronizes `stream`, then returns MQ_OK if no kernel of
  * this library launched so far on the current device has given up on a
  * bounded wait, else MQ_ERR_DEVICE, and clears the record. Returns

@@ -35,25 +35,15 @@
 // (q6_K), plus 4 B per output.
 
 #include "mq_internal.cuh"
+#include "gemv_common.cuh"
 #include "tc.cuh"
 
 namespace {
 
-constexpr int kThreads = 128;        // q4_K: 4 warps (row pairs) per block; measured faster than 256 and 512
-constexpr int kRowsPerBlock = kThreads / 32;   // q4_K: warps (row pairs) per block
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    return v;
-}
-
-// dp4a of unsigned bytes (a) with signed bytes (b).
-__device__ __forceinline__ int dp4a_us(uint32_t a, int b, int c) {
-    int d;
-    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-    return d;
-}
+using gemv::dp4a_us;
+using gemv::kThreads;   // q4_K: 4 warps (row pairs) per block; measured faster than 256 and 512
+using gemv::warp_sum;
+constexpr int kRowsPerBlock = gemv::kWarpsPerBlock;   // q4_K: warps (row pairs) per block
 
 // Lane = 4*g + p: in each 8-super-block step, super-block g of the step and its
 // 32-byte quant group p, i.e. sub-blocks 2p (low nibbles) and 2p+1 (high
@@ -339,34 +329,6 @@ __global__ void __launch_bounds__(32 * kQ6Rows) gemv_q6k_kernel(const uint8_t* _
     }
 }
 
-int check_gemv(const mq_q8_plane* a, const void* w, int N, const float* out) {
-    if (!a) return MQ_ERR_NULL;
-    if (N < 0 || a->M < 1 || a->M > MQ_GEMV_MAX_ROWS || !mq::valid_k(a->K)) return MQ_ERR_SHAPE;
-    int rc = mq::check_plane(a, a->M, a->K);
-    if (rc != MQ_OK || N == 0) return rc;
-    if (!mq::has_q8(a) || !w || !out) return MQ_ERR_NULL;
-    if (!mq::aligned16(w) || !mq::aligned16(out)) return MQ_ERR_ALIGN;
-    return mq::check_arch();
-}
-
-// Persistent grid: as many blocks as are resident at once (queried once per kernel
-// and device), never more than there are rows for.
-template <typename Kern>
-int gemv_grid(int N, Kern kern) {
-    constexpr int kMaxDevices = 64;
-    static int per_sm[kMaxDevices];   // 0: not queried yet on that device
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = -1;
-    int b = dev >= 0 ? __atomic_load_n(&per_sm[dev], __ATOMIC_ACQUIRE) : 0;
-    if (b == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kThreads, 0) != cudaSuccess || b < 1) b = 1;
-        if (dev >= 0) __atomic_store_n(&per_sm[dev], b, __ATOMIC_RELEASE);
-    }
-    const long long need = ((long long)N + kRowsPerBlock - 1) / kRowsPerBlock;
-    const long long cap = (long long)mq::num_sms() * b;
-    return (int)(need < cap ? need : cap);
-}
-
 }  // namespace
 
 namespace mq {
@@ -378,10 +340,10 @@ int take_gemv_device_error(cudaStream_t, unsigned* code) {
 }  // namespace mq
 
 extern "C" int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
-    int rc = check_gemv(a, w, N, out);
+    int rc = gemv::check(a, w, N, out);
     if (rc != MQ_OK || N == 0) return rc;
     auto go = [&](auto kern) {
-        return mq::launch_plain(kern, dim3(gemv_grid((N + 1) / 2, kern)), dim3(kThreads), 0,
+        return mq::launch_plain(kern, dim3(gemv::grid_for((N + 1) / 2, kern)), dim3(kThreads), 0,
                                 stream, static_cast<const uint8_t*>(w), a->qs, a->d, a->s, out, N, a->K, a->M);
     };
     const int M = a->M;
@@ -390,7 +352,7 @@ extern "C" int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* ou
 }
 
 extern "C" int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
-    int rc = check_gemv(a, w, N, out);
+    int rc = gemv::check(a, w, N, out);
     if (rc != MQ_OK || N == 0) return rc;
     const int chunks = (a->K / mq::QK_K + kQ6Chunk - 1) / kQ6Chunk;
     auto go = [&](auto k4, auto k3) {

@@ -22,7 +22,8 @@ MQ_GEMV_MAX_ROWS = 8   # include/mq.h
 EXPORTED = ["mq_plane_bytes", "mq_q4k_row_bytes", "mq_q6k_row_bytes", "mq_q6k_packed_row_bytes", "mq_prepack_q6k",
             "mq_quantize_q8", "mq_rms_quant",
             "mq_swiglu_quant", "mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k",
-            "mq_device_status", "mq_status_str"]
+            "mq_q5k_row_bytes", "mq_q4_0_row_bytes", "mq_q4_1_row_bytes", "mq_gemv_q5k", "mq_gemv_q4_0",
+            "mq_gemv_q4_1", "mq_device_status", "mq_status_str"]
 
 
 class MQError(RuntimeError):
@@ -63,6 +64,12 @@ def lib() -> ctypes.CDLL:
             "mq_gemm_q6k": (i, [pp, vp, i, vp, vp]),
             "mq_gemv_q4k": (i, [pp, vp, i, vp, vp]),
             "mq_gemv_q6k": (i, [pp, vp, i, vp, vp]),
+            "mq_q5k_row_bytes": (sz, [i]),
+            "mq_q4_0_row_bytes": (sz, [i]),
+            "mq_q4_1_row_bytes": (sz, [i]),
+            "mq_gemv_q5k": (i, [pp, vp, i, vp, vp]),
+            "mq_gemv_q4_0": (i, [pp, vp, i, vp, vp]),
+            "mq_gemv_q4_1": (i, [pp, vp, i, vp, vp]),
             "mq_device_status": (i, [vp]),
             "mq_status_str": (ctypes.c_char_p, [i]),
         }
@@ -234,6 +241,30 @@ def mq_gemv_q6k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=Non
     return _matmul("mq_gemv_q6k", a, w, N, out, stream)
 
 
+def mq_gemv_q5k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return _matmul("mq_gemv_q5k", a, w, N, out, stream)
+
+
+def mq_gemv_q4_0(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return _matmul("mq_gemv_q4_0", a, w, N, out, stream)
+
+
+def mq_gemv_q4_1(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return _matmul("mq_gemv_q4_1", a, w, N, out, stream)
+
+
+def mq_q5k_row_bytes(K: int) -> int:
+    return int(lib().mq_q5k_row_bytes(K))
+
+
+def mq_q4_0_row_bytes(K: int) -> int:
+    return int(lib().mq_q4_0_row_bytes(K))
+
+
+def mq_q4_1_row_bytes(K: int) -> int:
+    return int(lib().mq_q4_1_row_bytes(K))
+
+
 def mq_device_status(stream=None) -> int:
     return int(lib().mq_device_status(_stream(stream)))
 
@@ -248,4 +279,5 @@ def gemm(kind: str, a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream
 
 
 def gemv(kind: str, a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
-    return {"q4k": mq_gemv_q4k, "q6k": mq_gemv_q6k}[kind](a, w, N, out, stream)
+    return {"q4k": mq_gemv_q4k, "q6k": mq_gemv_q6k, "q5k": mq_gemv_q5k, "q4_0": mq_gemv_q4_0,
+            "q4_1": mq_gemv_q4_1}[kind](a, w, N, out, stream)

@@ -49,6 +49,9 @@ def test_size_helpers(L):
     assert tot == qs + d + s + ah + ax + af
     assert mq.mq_q4k_row_bytes(3584) == 14 * 144
     assert mq.mq_q6k_row_bytes(18944) == 74 * 210
+    assert mq.mq_q5k_row_bytes(5120) == 20 * 176
+    assert mq.mq_q4_0_row_bytes(5120) == 160 * 18
+    assert mq.mq_q4_1_row_bytes(5120) == 160 * 20
 
 
 def test_status_strings(L):
@@ -93,11 +96,12 @@ def test_validation_before_any_cuda_call(L):
 def test_matmul_validation_before_any_cuda_call(L):
     null = None
     p = _plane(mq.MQ_GEMV_MAX_ROWS + 1, 512, 16, 16, 16)
-    for fn in (L.mq_gemv_q4k, L.mq_gemv_q6k):
+    gemvs = (L.mq_gemv_q4k, L.mq_gemv_q6k, L.mq_gemv_q5k, L.mq_gemv_q4_0, L.mq_gemv_q4_1)
+    for fn in gemvs:
         assert fn(ctypes.byref(p), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE  # M > 8
         assert fn(ctypes.byref(_plane(0, 512, 16, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE
     p1 = _plane(1, 512, 16, 16, 16, 16, 16, 16)
-    for fn in (L.mq_gemm_q4k, L.mq_gemm_q6k, L.mq_gemv_q4k, L.mq_gemv_q6k):
+    for fn in (L.mq_gemm_q4k, L.mq_gemm_q6k) + gemvs:
         assert fn(None, ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
         assert fn(ctypes.byref(p1), None, 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
         assert fn(ctypes.byref(p1), ctypes.c_void_p(16), 8, None, null) == mq.MQ_ERR_NULL
@@ -112,7 +116,7 @@ def test_matmul_validation_before_any_cuda_call(L):
         assert fn(ctypes.byref(_plane(4, 512, 16, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
         assert fn(ctypes.byref(_plane(4, 512, 16, 16, 16, 40, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_ALIGN
         assert fn(ctypes.byref(_plane(4, 512, 16, 16, 16, 16, None, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
-    for fn in (L.mq_gemv_q4k, L.mq_gemv_q6k):
+    for fn in gemvs:
         assert fn(ctypes.byref(_plane(1, 512, None, None, None, 16, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
     p8 = _plane(4, 256, 16, 16, 16, 16, 16, 24)
     assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 256, ctypes.byref(p8), null) == mq.MQ_ERR_ALIGN
