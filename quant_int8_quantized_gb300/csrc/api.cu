@@ -1,7 +1,9 @@
 // Host-side helpers of the C ABI: sizes, status strings, architecture check,
 // device-status query.
 
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "mq_internal.cuh"
 
@@ -39,6 +41,24 @@ int num_sms() {
     if (dev < 0 || dev >= kMaxDevices) return 152;
     if (__atomic_load_n(&g_arch_ok[dev], __ATOMIC_ACQUIRE) == 0) check_arch();
     return g_sms[dev] > 0 ? g_sms[dev] : 152;
+}
+
+int resident_blocks(const void* kern, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<const void*, int, int, size_t>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(kern, dev, threads, smem);
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, threads, smem) != cudaSuccess || b < 1) {
+        cudaGetLastError();
+        b = 1;
+    }
+    cache.emplace(key, b);
+    return b;
 }
 
 }  // namespace mq

@@ -34,19 +34,11 @@ inline int check(const mq_q8_plane* a, const void* w, int N, const float* out) {
 }
 
 // Persistent grid for a kernel of kThreads-thread blocks whose warps take `units`
-// units of work grid-stride: as many blocks as are resident at once (queried once
-// per kernel instantiation and device), never more than the work needs.
+// units of work grid-stride: as many blocks as are resident at once, never more than
+// the work needs.
 template <typename Kern>
 int grid_for(long long units, Kern kern) {
-    constexpr int kMaxDevices = 64;
-    static int per_sm[kMaxDevices];   // 0: not queried yet on that device
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = -1;
-    int b = dev >= 0 ? __atomic_load_n(&per_sm[dev], __ATOMIC_ACQUIRE) : 0;
-    if (b == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kThreads, 0) != cudaSuccess || b < 1) b = 1;
-        if (dev >= 0) __atomic_store_n(&per_sm[dev], b, __ATOMIC_RELEASE);
-    }
+    const int b = mq::resident_blocks(reinterpret_cast<const void*>(kern), kThreads, 0);
     const long long need = (units + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const long long cap = (long long)mq::num_sms() * b;
     return (int)(need < cap ? need : cap);

@@ -52,6 +52,11 @@ inline int launch_status() {
 
 int num_sms();      // SM count of the current device (cached)
 
+// Blocks of `kern` (launched with `threads` threads and `smem` bytes of dynamic shared
+// memory) resident per SM on the current device; queried once per kernel, device and
+// launch shape, then cached. At least 1.
+int resident_blocks(const void* kern, int threads, size_t smem);
+
 // Launch with programmatic stream serialization: the kernel may start while the
 // previous kernel on the stream is finishing. Kernels launched this way call
 // mq_grid_wait() before reading anything an earlier kernel writes and before
@@ -120,10 +125,12 @@ __device__ __forceinline__ float mq_f16_to_f32(uint16_t h) {
 }
 
 // rint(v / d) with v / d the correctly rounded f32 quotient, computed as
-// rint(v * (1/d)) unless that product lies within 6.2e-5 of a rounding boundary
-// (n + 1/2), where the exact quotient is taken instead. For |v / d| <= 128 the
-// product is within 2e-5 of the rounded quotient (two roundings of 2^-24
-// relative each), so both round to the same integer outside that band.
+// rint(v * inv) with inv an approximate 1/d (rcp.approx: at most 1 ulp off)
+// unless that product lies within 6.2e-5 of a rounding boundary (n + 1/2), where
+// the exact quotient is taken instead. For |v / d| <= 128 the product is within
+// 128 * (2^-23 + 2^-24 + 2^-24) = 3.1e-5 of the rounded quotient (the reciprocal's
+// error, the product's rounding and the quotient's), so both round to the same
+// integer outside that band.
 __device__ __forceinline__ int mq_rint_div(float v, float d, float inv) {
     const float t = v * inv;
     const float r = rintf(t);
@@ -145,13 +152,14 @@ __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v
     const float d = __fdiv_rn(am, 127.0f);
     int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
     if (d != 0.0f) {
-        const float inv = __frcp_rn(d);
+        float inv;
+        asm("rcp.approx.f32 %0, %1;" : "=f"(inv) : "f"(d));
         if (isfinite(inv)) {
             q0 = mq_rint_div(v0, d, inv);
             q1 = mq_rint_div(v1, d, inv);
             q2 = mq_rint_div(v2, d, inv);
             q3 = mq_rint_div(v3, d, inv);
-        } else {   // d subnormal: 1/d overflows
+        } else {   // d subnormal: 1/d overflows (rcp.approx keeps subnormal inputs)
             q0 = __float2int_rn(__fdiv_rn(v0, d));
             q1 = __float2int_rn(__fdiv_rn(v1, d));
             q2 = __float2int_rn(__fdiv_rn(v2, d));

@@ -77,7 +77,9 @@ __device__ __forceinline__ void quant_pair(const Out& o, long long pair, int lan
         D = fmaxf(D, __shfl_xor_sync(0xffffffffu, D, 8));
         D = fmaxf(D, __shfl_xor_sync(0xffffffffu, D, 16));
         int e = 0;
-        if (D != 0.0f) {
+        if (D >= 0x1p-126f) {   // normal: D = 1.m 2^(b - 127) = 0.1m 2^(b - 126)
+            e = min(126, max(-126, 3 - (((int)(__float_as_uint(D) >> 23) & 0xff) - 126)));
+        } else if (D != 0.0f) {
             int E;
             frexpf(D, &E);
             e = min(126, max(-126, 3 - E));
@@ -189,7 +191,7 @@ __device__ __forceinline__ float4 silu_mul4(float4 g, float4 u) {
 }
 
 template <int R>
-__global__ void __launch_bounds__(kThreads) swiglu_quant_kernel(const float4* __restrict__ g,
+__global__ void __launch_bounds__(kThreads, 4) swiglu_quant_kernel(const float4* __restrict__ g,
                                                                 const float4* __restrict__ u, Out o,
                                                                 long long rounds) {
     mq_grid_release();
@@ -364,10 +366,13 @@ __global__ void __launch_bounds__(1024) rms_quant_wide_kernel(const float4* __re
 // rounds' latencies then overlap across warps instead of queueing inside one.
 bool few_rounds(long long rounds) { return rounds < 2LL * mq::num_sms() * (kThreads / 32) * kRoundsPerIter; }
 
-int flat_grid(long long rounds, int rounds_per_iter) {
+// One wave: as many blocks as are resident at once (the warps stride over the rounds),
+// never more than the rounds need.
+template <typename Kern>
+int flat_grid(long long rounds, int rounds_per_iter, Kern kern) {
     const long long per_block = (kThreads / 32) * rounds_per_iter;
     long long blocks = (rounds + per_block - 1) / per_block;
-    const long long cap = (long long)mq::num_sms() * 8;
+    const long long cap = (long long)mq::num_sms() * mq::resident_blocks(reinterpret_cast<const void*>(kern), kThreads, 0);
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return (int)blocks;
@@ -401,7 +406,7 @@ extern "C" int mq_quantize_q8(const float* x, int M, int K, const mq_q8_plane* o
     const long long rounds = (long long)M * K / 128;
     const int R = flat_rounds(rounds, out);
     auto kern = R == 1 ? quantize_q8_kernel<1> : R == 2 ? quantize_q8_kernel<2> : quantize_q8_kernel<kRoundsPerIter>;
-    return mq::launch_pdl(kern, dim3(flat_grid(rounds, R)), dim3(kThreads), 0, stream,
+    return mq::launch_pdl(kern, dim3(flat_grid(rounds, R, kern)), dim3(kThreads), 0, stream,
                           reinterpret_cast<const float4*>(x), out_of(out), rounds);
 }
 
@@ -412,7 +417,7 @@ extern "C" int mq_swiglu_quant(const float* g, const float* u, int M, int K, con
     const long long rounds = (long long)M * K / 128;
     const int R = flat_rounds(rounds, out);
     auto kern = R == 1 ? swiglu_quant_kernel<1> : R == 2 ? swiglu_quant_kernel<2> : swiglu_quant_kernel<kRoundsPerIter>;
-    return mq::launch_pdl(kern, dim3(flat_grid(rounds, R)), dim3(kThreads), 0, stream,
+    return mq::launch_pdl(kern, dim3(flat_grid(rounds, R, kern)), dim3(kThreads), 0, stream,
                           reinterpret_cast<const float4*>(g), reinterpret_cast<const float4*>(u), out_of(out), rounds);
 }
 
