@@ -199,6 +199,23 @@ int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
 int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 
 /*
+ * mq_gemm_q4_0 / mq_gemm_q4_1 — the same prefill matmul for the Q4_0 / Q4_1 types
+ * of the matmul dispatch list ([r60] §3.2), with w in the raw layouts given at
+ * mq_gemv_q4_0 below (18 / 20 bytes per 32 weights, rows 16-byte aligned since K
+ * is a multiple of 256). Arguments, output, split-K and errors as for mq_gemm_q4k.
+ * Arithmetic: per 256-wide super-block and weight row, a power of two c; block b's
+ * scale d_b = g_b 2^E_b (g_b its 11-bit integer significand) is split
+ * g_b = 64 Dh + Dl, and each weight d_b (q - o) / c enters the f16 tensor pipe as
+ * the two exact binary16 parts (q - o) Dh 2^(E_b+6) / c and (q - o) Dl 2^E_b / c
+ * (o = 8 for q4_0, 0 for q4_1), two MMAs per K step; q4_1's m_b / c multiplies the
+ * plane's exact block sums like q4_K's min term. The weight operand is exact
+ * while a super-block's block scales lie within a factor 2^24 of each other;
+ * accuracy within 1e-3 * sum_k |a||w| per element.
+ */
+int mq_gemm_q4_0(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+int mq_gemm_q4_1(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+
+/*
  * mq_gemv_q4k / mq_gemv_q6k — decode (M == 1) and small-batch
  * (1 <= M <= MQ_GEMV_MAX_ROWS) matrix products ([D3-7] §2 (2b) and Excerpt
  * A/A2, the MMVQ decode path): the same result as the GEMM, within the same

@@ -70,7 +70,6 @@ constexpr int RA = 5;                   // activation slots (q6_K; q4_K: one per
 constexpr int RX = 3;                   // per-super-block stages (block sums, 2^-e, weight scales c)
 constexpr int kActBytes = BT * KS * 2;  // 24576
 constexpr int kAxBytes = BT * 32;       // 16 binary16 block-sum parts per token
-constexpr int kAfBytes = BT * 4;
 constexpr int kConvWarps = 8;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + 32 * kConvWarps + 32 * kEpiWarps;
@@ -84,15 +83,25 @@ constexpr uint32_t kSCol0 = 0, kSCol1 = BT, kACol = 2 * BT;   // accumulators, t
 constexpr int kMTile = BW * 16 * 2;                           // q4_K min-term operand: 128 rows x K 16, f16
 static_assert(kACol + 128 <= kTmemCols, "tensor memory");
 
-template <bool Q6>
+// Weight types of the GEMM.
+enum : int { kQ4K = 0, kQ6K = 1, kQ40 = 2, kQ41 = 3 };
+
+template <int WT>
 struct Cfg {
-    // q4_K: raw 144-byte super-blocks. q6_K: the 224-byte prepacked form (mq.h), staged
-    // with a 240-byte pitch (the box reads 16 bytes past the block) so that one 16-byte
-    // load per thread and row hits 8 distinct bank groups per 8 rows.
-    static constexpr int kSB = Q6 ? mq::Q6K_PACKED_BYTES : mq::Q4K_BYTES;
-    static constexpr int kRowBytes = Q6 ? 240 : 144;   // staged bytes per weight row (the TMA box)
+    // q4_K: one exact binary16 operand per weight, K chunks of 64 (slot j = chunk j).
+    // q6_K, q4_0, q4_1: two exact binary16 parts per weight, 32-wide quarters, two MMAs
+    // per K = 16 step. q4_K and q4_1 add the min-term MMAs.
+    static constexpr bool kQuarters = WT != kQ4K;
+    static constexpr bool kMin = WT == kQ4K || WT == kQ41;
+    // Bytes per 256 weights in global memory, and staged bytes per weight row (the TMA
+    // box). q4_K, q4_0: raw 144-byte super-blocks (8 x 18 B for q4_0). q6_K: the 224-byte
+    // prepacked form (mq.h), staged with a 240-byte pitch (the box reads 16 bytes past the
+    // block) so that one 16-byte load per thread and row hits 8 distinct bank groups per 8
+    // rows; q4_1: 8 x 20 B, staged with a 176-byte pitch for the same reason.
+    static constexpr int kSB = WT == kQ6K ? mq::Q6K_PACKED_BYTES : WT == kQ41 ? 160 : mq::Q4K_BYTES;
+    static constexpr int kRowBytes = WT == kQ6K ? 240 : WT == kQ41 ? 176 : 144;
     static constexpr int kStage = BW * kRowBytes;
-    static constexpr int kRB = Q6 ? 2 : 3;             // weight stages
+    static constexpr int kRB = kQuarters ? 2 : 3;      // weight stages
     // Weight-operand slots in tensor memory, 32 columns each. q4_K: slot j holds K chunk j
     // (64 wide) of every super-block and is written by one converter half only. q6_K: slot
     // t holds quarter t of a super-block half (32 wide, both exact parts), written
@@ -104,21 +113,22 @@ struct Cfg {
     // barrier pair per chunk covers both (the TMA and the 4 converter warps of its half
     // arrive on "full", the MMAs' commit on "empty"), and the min-term operand joins
     // the per-super-block block-sum stage the same way: half the issuer's waits.
-    static constexpr bool kJoint = !Q6;
-    static constexpr int kRA = Q6 ? RA : 4;
+    static constexpr bool kJoint = !kQuarters;
+    static constexpr int kRA = WT == kQ4K ? 4 : RA;
 };
 
-template <bool Q6>
+template <int WT>
 struct Smem {
-    alignas(1024) uint8_t act[Cfg<Q6>::kRA][kActBytes];
+    static constexpr bool kMin = Cfg<WT>::kMin;
+    alignas(1024) uint8_t act[Cfg<WT>::kRA][kActBytes];
     alignas(256) uint8_t ax[RX][kAxBytes];
     alignas(16) float af[RX][BT];
     float cvec[RX][BW];
-    alignas(128) uint8_t braw[Cfg<Q6>::kRB][Cfg<Q6>::kStage];
-    alignas(128) uint8_t mop[Q6 ? 1 : RX][Q6 ? 16 : 2 * kMTile];   // q4_K min-term operand (hi, lo) per stage
-    uint64_t act_full[Cfg<Q6>::kRA], act_empty[Cfg<Q6>::kRA], ax_full[RX], ax_empty[RX], c_full[RX], c_empty[RX];
-    uint64_t b_full[Cfg<Q6>::kRB], b_empty[Cfg<Q6>::kRB];
-    uint64_t a_full[Cfg<Q6>::kRF], a_empty[Cfg<Q6>::kRF][2];
+    alignas(128) uint8_t braw[Cfg<WT>::kRB][Cfg<WT>::kStage];
+    alignas(128) uint8_t mop[kMin ? RX : 1][kMin ? 2 * kMTile : 16];   // min-term operand (hi, lo) per stage
+    uint64_t act_full[Cfg<WT>::kRA], act_empty[Cfg<WT>::kRA], ax_full[RX], ax_empty[RX], c_full[RX], c_empty[RX];
+    uint64_t b_full[Cfg<WT>::kRB], b_empty[Cfg<WT>::kRB];
+    uint64_t a_full[Cfg<WT>::kRF], a_empty[Cfg<WT>::kRF][2];
     uint64_t t_full[2], t_empty[2], mma_done;
     uint32_t tmem;
     int abort;
@@ -148,23 +158,23 @@ __device__ __forceinline__ bool mbar_ready(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-template <bool Q6>
-__device__ __forceinline__ bool wait1(Smem<Q6>& sm, uint64_t* bar, uint32_t parity) {
+template <int WT>
+__device__ __forceinline__ bool wait1(Smem<WT>& sm, uint64_t* bar, uint32_t parity) {
     if (mbar_ready(bar, parity) || tc::mbar_wait(bar, parity, kWaitLimitNs)) return true;
     atomicOr(&g_gemm_error, 1u);
     *(volatile int*)&sm.abort = 1;
     return false;
 }
 
-template <bool Q6>
-__device__ __forceinline__ bool aborted(Smem<Q6>& sm) {
+template <int WT>
+__device__ __forceinline__ bool aborted(Smem<WT>& sm) {
     return *(volatile int*)&sm.abort != 0;
 }
 
 // Whole-warp variants: every lane waits, and the outcome is made warp-uniform so
 // that the warp never diverges in front of a warp-collective operation.
-template <bool Q6>
-__device__ __forceinline__ bool wwait(Smem<Q6>& sm, uint64_t* bar, uint32_t parity) {
+template <int WT>
+__device__ __forceinline__ bool wwait(Smem<WT>& sm, uint64_t* bar, uint32_t parity) {
     const bool ok = __all_sync(0xffffffffu, mbar_ready(bar, parity) || tc::mbar_wait(bar, parity, kWaitLimitNs));
     if (!ok) {
         if ((threadIdx.x & 31) == 0) atomicOr(&g_gemm_error, 1u);
@@ -173,8 +183,8 @@ __device__ __forceinline__ bool wwait(Smem<Q6>& sm, uint64_t* bar, uint32_t pari
     return ok;
 }
 
-template <bool Q6>
-__device__ __forceinline__ bool waborted(Smem<Q6>& sm) {
+template <int WT>
+__device__ __forceinline__ bool waborted(Smem<WT>& sm) {
     return __any_sync(0xffffffffu, aborted(sm));
 }
 
@@ -210,17 +220,29 @@ __device__ __forceinline__ uint32_t byte_of(uint32_t y, uint32_t z, uint32_t w, 
     return (v >> (8 * (i & 3))) & 0xffu;
 }
 
-template <bool Q6>
+// A binary16 bit pattern as m * 2^E with m its integer significand (< 2048, 0 for zero).
+__device__ __forceinline__ void f16_split(uint32_t hb, int& m, int& E) {
+    const int e = (int)((hb >> 10) & 31u);
+    m = e ? (int)(1024u | (hb & 1023u)) : (int)(hb & 1023u);
+    E = (e ? e : 1) - 25;
+}
+
+// A 32-bit word from a 2-byte-aligned shared-memory address.
+__device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
+    return (uint32_t)*reinterpret_cast<const uint16_t*>(p) | ((uint32_t)*reinterpret_cast<const uint16_t*>(p + 2) << 16);
+}
+
+template <int WT>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmAct,
                                                            const __grid_constant__ CUtensorMap tmAx,
                                                            const __grid_constant__ CUtensorMap tmAf,
                                                            const __grid_constant__ CUtensorMap tmW,
                                                            float* __restrict__ out, int M, int N, int K, int splits,
                                                            int nfast, int bt) {
-    using C = Cfg<Q6>;
+    using C = Cfg<WT>;
     constexpr int kRB = C::kRB, kRF = C::kRF;
     extern __shared__ uint8_t smem_raw[];
-    Smem<Q6>& sm = *reinterpret_cast<Smem<Q6>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    Smem<WT>& sm = *reinterpret_cast<Smem<WT>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = K / mq::QK_K;
     const int num_mt = (M + bt - 1) / bt, num_nt = (N + BW - 1) / BW;
@@ -232,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc::mbar_init(&sm.act_empty[i], 1);
         }
         for (int i = 0; i < RX; ++i) {
-            tc::mbar_init(&sm.ax_full[i], C::kJoint ? 5 : 1);
+            tc::mbar_init(&sm.ax_full[i], C::kMin ? 5 : 1);   // + the 4 warps writing the min operand
             tc::mbar_init(&sm.ax_empty[i], 1 + kEpiWarps);   // the MMAs (block sums) and the epilogue (2^-e)
             tc::mbar_init(&sm.c_full[i], 4);
             tc::mbar_init(&sm.c_empty[i], kEpiWarps);
@@ -337,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 for (int j = 0; j < 4; ++j) {
                     const int a = (ga + j) % C::kRA;
                     const uint32_t sa = tc::smem_u32(sm.act[a]);
-                    if constexpr (!Q6) {
+                    if constexpr (!C::kQuarters) {
                         const uint32_t fa = tbase + kACol + C::kFCols * j;
 #pragma unroll
                         for (int k = 0; k < 2; ++k)
@@ -376,13 +398,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 if (!ok) break;
                 ga += 4;
-                if constexpr (!Q6) {
+                if constexpr (C::kMin) {
+                    if constexpr (C::kQuarters) {   // q4_1: the block sums and the min operand (q4_K waited at chunk 3)
+                        if (!wait1(sm, &sm.ax_full[x], (sbc / RX) & 1)) break;
+                        tc::tc_fence_after();
+                    }
                     const uint64_t bd = tc::smem_desc_sw32(tc::smem_u32(sm.ax[x]));
                     const uint32_t ma = tc::smem_u32(sm.mop[x]);
                     tc::mma_f16(dcol, tc::smem_desc_noswizzle(ma, 128, 256), bd, idesc, 1u);
                     tc::mma_f16(dcol, tc::smem_desc_noswizzle(ma + kMTile, 128, 256), bd, idesc, 1u);
                 }
-                tc::mma_commit(&sm.ax_empty[x]);   // q6_K: a token arrival (the block sums are the epilogue's)
+                tc::mma_commit(&sm.ax_empty[x]);   // q6_K, q4_0: a token arrival (the block sums are the epilogue's)
                 tc::mma_commit(&sm.t_full[s]);
                 if (sbc + 1 < total) {
                     ok = sb_ready(sbc + 1, ga);
@@ -410,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const int b = sbc % kRB, x = sbc % RX;
                 if (!wwait(sm, &sm.b_full[b], (sbc / kRB) & 1)) break;
                 const uint8_t* row = sm.braw[b] + r * C::kRowBytes;
-                if constexpr (!Q6) {
+                if constexpr (WT == kQ4K) {
                     // ---- q4_K: scales and the power of two k; the main operand, then (h == 0) the
                     //      min-term operand and the epilogue's scale c
                     const uint4 hdr = *reinterpret_cast<const uint4*>(row);
@@ -494,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&sm.c_full[x]);
                     }
-                } else {
+                } else if constexpr (WT == kQ6K) {
                     // ---- q6_K (prepacked): half h of the block is 112 bytes at 112 h: ql (64), qh (32),
                     //      the half's 8 scales, d. Slot j = 2h + jj covers quarters t = 2jj + i, i = 0, 1:
                     //      low bits from ql bytes 32i.. (high nibble when jj = 1), high bits from qh
@@ -538,6 +564,102 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (h == 0) {
                         if (!wwait(sm, &sm.c_empty[x], ((sbc / RX) & 1) ^ 1)) break;
                         sm.cvec[x][r] = n < N ? __half2float(__ushort_as_half((unsigned short)(c6.z & 0xffffu))) : 0.0f;
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&sm.c_full[x]);
+                    }
+                } else {
+                    // ---- q4_0 / q4_1: eight 32-blocks of kB bytes. Block b's scale is d_b = g_b 2^E_b
+                    //      (g_b its 11-bit integer significand) and g_b = 64 Dh + Dl (Dh < 32, Dl < 64),
+                    //      so that with c = 2^Ec a power of two per row and super-block,
+                    //          d_b (q - o) / c = (q - o) Dh 2^(E_b + 6 - Ec) + (q - o) Dl 2^(E_b - Ec),
+                    //      two parts of at most 9 and 10 significant bits: exact in binary16 (o = 8 for
+                    //      q4_0, 0 for q4_1). Ec is the largest E_b (and, q4_1, large enough that every
+                    //      m_b / c stays below 2^15), so the parts stay below 2^14 and are exact while the
+                    //      super-block's block scales lie within 2^24 of each other. Quarter t of half h
+                    //      is block 4h + t, in operand slot t (both parts), as q6_K's quarters.
+                    constexpr bool Q41 = WT == kQ41;
+                    constexpr int kB = Q41 ? 20 : 18;
+                    int ec = -1000;
+                    uint32_t dm[8];   // bit patterns: d_b (low half), q4_1: m_b (high half)
+#pragma unroll
+                    for (int bb = 0; bb < 8; ++bb) {
+                        dm[bb] = Q41 ? *reinterpret_cast<const uint32_t*>(row + kB * bb)
+                                     : (uint32_t)*reinterpret_cast<const uint16_t*>(row + kB * bb);
+                        int g, E;
+                        f16_split(dm[bb] & 0xffffu, g, E);
+                        if (g) ec = max(ec, E);
+                        if (Q41) {
+                            f16_split(dm[bb] >> 16, g, E);
+                            if (g) ec = max(ec, E - 4);   // |m_b| < 2^(E + 11) <= 2^15 c
+                        }
+                    }
+                    if (ec == -1000) ec = 0;
+                    bool ok = true;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        if (!wwait(sm, &sm.a_empty[t][h], h ? (sbc & 1) : ((sbc & 1) ^ 1))) { ok = false; break; }
+                        tc::tc_fence_after();   // the stores below come after the MMAs that read the slot
+                        const int bb = 4 * h + t;
+                        const uint8_t* blk = row + kB * bb;
+                        int g, E;
+                        f16_split(dm[bb] & 0xffffu, g, E);
+                        const float sgn = (dm[bb] & 0x8000u) ? -1.0f : 1.0f;
+                        const float m1 = sgn * ldexpf((float)(g >> 6), E + 6 - ec);
+                        const float m2 = sgn * ldexpf((float)(g & 63), E - ec);
+                        const float off = Q41 ? 16.0f : 24.0f;   // (1 + v/16) 16 mul - off mul = (v - o) mul
+                        const uint32_t mul1 = h2_of(16.0f * m1), add1 = h2_of(-off * m1);
+                        const uint32_t mul2 = h2_of(16.0f * m2), add2 = h2_of(-off * m2);
+                        uint32_t qw[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            qw[i] = Q41 ? *reinterpret_cast<const uint32_t*>(blk + 4 + 4 * i) : ld_u32_a2(blk + 2 + 4 * i);
+                        uint32_t p1[16], p2[16];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t lo = qw[i] & 0x0F0F0F0Fu, hi = (qw[i] >> 4) & 0x0F0F0F0Fu;
+                            nib4_one(lo, mul1, add1, p1[2 * i], p1[2 * i + 1]);          // K 4i .. 4i + 3
+                            nib4_one(hi, mul1, add1, p1[8 + 2 * i], p1[9 + 2 * i]);      // K 16 + 4i ..
+                            nib4_one(lo, mul2, add2, p2[2 * i], p2[2 * i + 1]);
+                            nib4_one(hi, mul2, add2, p2[8 + 2 * i], p2[9 + 2 * i]);
+                        }
+                        const uint32_t fa = tbase + lane_bits + kACol + C::kFCols * t;
+                        tc::tmem_st16(fa, p1);
+                        tc::tmem_st16(fa + 16, p2);
+                        tc::tmem_st_wait();
+                        tc::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&sm.a_full[t]);
+                    }
+                    if (!ok) break;
+                    if (h == 0) {
+                        if constexpr (Q41) {   // the min operand: m_b / c as hi + lo binary16 parts
+                            if (!wwait(sm, &sm.ax_empty[x], ((sbc / RX) & 1) ^ 1)) break;
+                            uint32_t mh[8];
+#pragma unroll
+                            for (int j = 0; j < 8; j += 2) {
+                                float v[2];
+#pragma unroll
+                                for (int e = 0; e < 2; ++e) {
+                                    const float mb = __half2float(__ushort_as_half((unsigned short)(dm[j + e] >> 16)));
+                                    v[e] = ldexpf(mb, -ec);
+                                }
+                                const float hi0 = __half2float(__float2half_rn(v[0]));
+                                const float hi1 = __half2float(__float2half_rn(v[1]));
+                                mh[j / 2] = h2_pack(v[0], v[1]);
+                                mh[4 + j / 2] = h2_pack(__fsub_rn(v[0], hi0), __fsub_rn(v[1], hi1));
+                            }
+                            uint8_t* mt = sm.mop[x] + (r >> 3) * 256 + (r & 7) * 16;
+                            const uint4 vh = make_uint4(mh[0], mh[1], mh[2], mh[3]), vl = make_uint4(mh[4], mh[5], mh[6], mh[7]);
+                            *reinterpret_cast<uint4*>(mt) = vh;
+                            *reinterpret_cast<uint4*>(mt + 128) = vh;
+                            *reinterpret_cast<uint4*>(mt + kMTile) = vl;
+                            *reinterpret_cast<uint4*>(mt + kMTile + 128) = vl;
+                            tc::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) tc::mbar_arrive(&sm.ax_full[x]);
+                        }
+                        if (!wwait(sm, &sm.c_empty[x], ((sbc / RX) & 1) ^ 1)) break;
+                        sm.cvec[x][r] = n < N ? ldexpf(1.0f, ec) : 0.0f;
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&sm.c_full[x]);
                     }
@@ -679,7 +801,7 @@ int check_gemm(const mq_q8_plane* a, const void* w, int N, const float* out) {
 // Once per device: the register split between warpgroups assumes the launch register
 // count, and the kernel's shared-memory size is set. Later calls make no attribute
 // calls, so a sequence of entry points can be captured in a graph.
-template <bool Q6>
+template <int WT>
 bool gemm_ready(size_t smem) {
     constexpr int kMaxDevices = 64;
     static int state[kMaxDevices];   // 0 unknown, 1 ready, 2 failed
@@ -692,8 +814,8 @@ bool gemm_ready(size_t smem) {
         v = state[dev];
         if (v == 0) {
             cudaFuncAttributes fa;
-            v = (cudaFuncGetAttributes(&fa, gemm_kernel<Q6>) == cudaSuccess && fa.numRegs == kLaunchRegs &&
-                 cudaFuncSetAttribute(gemm_kernel<Q6>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+            v = (cudaFuncGetAttributes(&fa, gemm_kernel<WT>) == cudaSuccess && fa.numRegs == kLaunchRegs &&
+                 cudaFuncSetAttribute(gemm_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
                      cudaSuccess)
                     ? 1
                     : 2;
@@ -710,16 +832,16 @@ bool gemm_ready(size_t smem) {
 // weight stream and its conversion rather than by work on empty columns.
 int token_tile(int M) { return M >= BT ? BT : ((M + 15) / 16) * 16; }
 
-template <bool Q6>
+template <int WT>
 int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     int rc = check_gemm(a, w, N, out);
     if (rc != MQ_OK || N == 0 || a->M == 0) return rc;
     const int M = a->M, K = a->K, S = K / mq::QK_K;
-    const size_t smem = sizeof(Smem<Q6>) + 1024;
-    if (!gemm_ready<Q6>(smem)) return MQ_ERR_LAUNCH;
-    const unsigned long long row = (unsigned long long)S * Cfg<Q6>::kSB;
+    const size_t smem = sizeof(Smem<WT>) + 1024;
+    if (!gemm_ready<WT>(smem)) return MQ_ERR_LAUNCH;
+    const unsigned long long row = (unsigned long long)S * Cfg<WT>::kSB;
     CUtensorMap tmAct, tmAx, tmAf, tmW;
-    if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row, (uint64_t)N, row, Cfg<Q6>::kRowBytes, BW))
+    if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row, (uint64_t)N, row, Cfg<WT>::kRowBytes, BW))
         return MQ_ERR_LAUNCH;
     const int mp = mq::af_stride(M);
     const int bt = token_tile(M);
@@ -738,7 +860,7 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
     const int grid = (int)(units < sms ? units : sms);
     // weight-row tiles fastest when the activations outweigh the weights
     const int nfast = (double)M * K * 2 > (double)N * row ? 1 : 0;
-    gemm_kernel<Q6><<<grid, kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits, nfast, bt);
+    gemm_kernel<WT><<<grid, kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits, nfast, bt);
     return mq::launch_status();
 }
 
@@ -759,9 +881,17 @@ int take_gemm_device_error(cudaStream_t stream, unsigned* code) {
 }  // namespace mq
 
 extern "C" int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
-    return launch_gemm<false>(a, w, N, out, stream);
+    return launch_gemm<kQ4K>(a, w, N, out, stream);
 }
 
 extern "C" int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
-    return launch_gemm<true>(a, w, N, out, stream);
+    return launch_gemm<kQ6K>(a, w, N, out, stream);
+}
+
+extern "C" int mq_gemm_q4_0(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
+    return launch_gemm<kQ40>(a, w, N, out, stream);
+}
+
+extern "C" int mq_gemm_q4_1(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
+    return launch_gemm<kQ41>(a, w, N, out, stream);
 }

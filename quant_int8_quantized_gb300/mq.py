@@ -23,7 +23,7 @@ EXPORTED = ["mq_plane_bytes", "mq_q4k_row_bytes", "mq_q6k_row_bytes", "mq_q6k_pa
             "mq_quantize_q8", "mq_rms_quant",
             "mq_swiglu_quant", "mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k",
             "mq_q5k_row_bytes", "mq_q4_0_row_bytes", "mq_q4_1_row_bytes", "mq_gemv_q5k", "mq_gemv_q4_0",
-            "mq_gemv_q4_1", "mq_device_status", "mq_status_str"]
+            "mq_gemv_q4_1", "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_device_status", "mq_status_str"]
 
 
 class MQError(RuntimeError):
@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
             "mq_gemv_q5k": (i, [pp, vp, i, vp, vp]),
             "mq_gemv_q4_0": (i, [pp, vp, i, vp, vp]),
             "mq_gemv_q4_1": (i, [pp, vp, i, vp, vp]),
+            "mq_gemm_q4_0": (i, [pp, vp, i, vp, vp]),
+            "mq_gemm_q4_1": (i, [pp, vp, i, vp, vp]),
             "mq_device_status": (i, [vp]),
             "mq_status_str": (ctypes.c_char_p, [i]),
         }
@@ -241,6 +243,14 @@ def mq_gemv_q6k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=Non
     return _matmul("mq_gemv_q6k", a, w, N, out, stream)
 
 
+def mq_gemm_q4_0(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return _matmul("mq_gemm_q4_0", a, w, N, out, stream)
+
+
+def mq_gemm_q4_1(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    return _matmul("mq_gemm_q4_1", a, w, N, out, stream)
+
+
 def mq_gemv_q5k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
     return _matmul("mq_gemv_q5k", a, w, N, out, stream)
 
@@ -270,12 +280,13 @@ def mq_device_status(stream=None) -> int:
 
 
 def gemm_weights(kind: str, w: torch.Tensor, N: int, K: int, stream=None) -> torch.Tensor:
-    """The weight form the GEMM reads: q4_K rows as they are, q6_K rows prepacked."""
+    """The weight form the GEMM reads: q6_K rows prepacked, every other type as it is."""
     return mq_prepack_q6k(w, N, K, stream=stream) if kind == "q6k" else w
 
 
 def gemm(kind: str, a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
-    return {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k}[kind](a, w, N, out, stream)
+    return {"q4k": mq_gemm_q4k, "q6k": mq_gemm_q6k, "q4_0": mq_gemm_q4_0, "q4_1": mq_gemm_q4_1}[kind](a, w, N, out,
+                                                                                                 stream)
 
 
 def gemv(kind: str, a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:

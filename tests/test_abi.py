@@ -101,7 +101,8 @@ def test_matmul_validation_before_any_cuda_call(L):
         assert fn(ctypes.byref(p), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE  # M > 8
         assert fn(ctypes.byref(_plane(0, 512, 16, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE
     p1 = _plane(1, 512, 16, 16, 16, 16, 16, 16)
-    for fn in (L.mq_gemm_q4k, L.mq_gemm_q6k) + gemvs:
+    gemms = (L.mq_gemm_q4k, L.mq_gemm_q6k, L.mq_gemm_q4_0, L.mq_gemm_q4_1)
+    for fn in gemms + gemvs:
         assert fn(None, ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
         assert fn(ctypes.byref(p1), None, 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
         assert fn(ctypes.byref(p1), ctypes.c_void_p(16), 8, None, null) == mq.MQ_ERR_NULL
@@ -112,7 +113,7 @@ def test_matmul_validation_before_any_cuda_call(L):
     assert L.mq_gemm_q4k(ctypes.byref(bad), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE
     # the GEMM needs the operand arrays, the GEMV the q8 arrays; a group is all present or all
     # absent, and a misaligned array is rejected everywhere
-    for fn in (L.mq_gemm_q4k, L.mq_gemm_q6k):
+    for fn in gemms:
         assert fn(ctypes.byref(_plane(4, 512, 16, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL
         assert fn(ctypes.byref(_plane(4, 512, 16, 16, 16, 40, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_ALIGN
         assert fn(ctypes.byref(_plane(4, 512, 16, 16, 16, 16, None, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_NULL

@@ -130,3 +130,69 @@ def test_full_size_every_element(kind, N, K):
     g.check()
     _check(g.t, p, w, kind, N, K)
     assert mq.mq_device_status() == mq.MQ_OK
+
+
+# ----------------------------------------------------------------- q4_0 / q4_1 prefill GEMM
+
+GEMM_KINDS = ["q4_0", "q4_1"]
+
+
+def _op_plane(x):
+    M, K = x.shape
+    p = mq.Plane.empty(M, K)
+    mq.mq_quantize_q8(x.cuda(), p)
+    return p
+
+
+@pytest.mark.parametrize("kind", GEMM_KINDS)
+@pytest.mark.parametrize("M,N,K", [(16, 256, 512), (2, 1000, 3584), (130, 300, 768), (257, 129, 1280), (1, 8, 256)])
+def test_gemm_parity_every_element(kind, M, N, K):
+    x = synth.with_outliers(synth.normal((M, K), 0, f"bg.x{M}x{K}"), 0, f"bg.o{M}x{K}")
+    w = synth.weights(kind, N, K, 0, f"bg.{kind}.{N}x{K}")
+    p = _op_plane(x)
+    g = Guarded((M, N), torch.float32)
+    mq.gemm(kind, p, mq.gemm_weights(kind, w.cuda(), N, K), N, g.t)
+    torch.cuda.synchronize()
+    g.check()
+    assert g.untouched() == 0, "unwritten outputs"
+    _check(g.t, p, w, kind, N, K)
+    assert mq.mq_device_status() == mq.MQ_OK
+
+
+@pytest.mark.parametrize("kind", GEMM_KINDS)
+@pytest.mark.parametrize("M", [16, 130])
+def test_gemm_exact_integer_dots(kind, M):
+    """d = 1 (q4_1: m = -3) and d_a = 1: every partial sum is an integer below 2^24, so the
+    GEMM's two exact weight parts and the min term must give the f64 oracle bit for bit."""
+    rng = np.random.default_rng(23 + M)
+    N, K = 300, 1280
+    w = torch.from_numpy(np.ascontiguousarray(_exact_weights(kind, rng, N, K))).cuda()
+    p = _op_plane(_unit_activations(rng, M, K))
+    assert np.all(p.d.cpu().numpy() == 1.0)
+    out = torch.empty((M, N), device="cuda")
+    mq.gemm(kind, p, w, N, out)
+    ref, _ = O.gemm_rows(p.qs.cpu().numpy(), p.d.cpu().numpy(), w.cpu().numpy(), kind, N, K)
+    assert np.all(np.abs(ref) < 2 ** 22)
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, ref), f"max diff {np.max(np.abs(got - ref))}"
+
+
+@pytest.mark.parametrize("kind", GEMM_KINDS)
+def test_gemm_full_size_sampled_rows(kind):
+    """The 7B FFN up shape at M = 3314, every output written, 16 sampled rows against the oracle."""
+    M, N, K = 3314, 18944, 3584
+    x = synth.normal((M, K), 0, "bg.full.x", device="cuda")
+    w = synth.weights(kind, N, K, 0, f"bg.full.{kind}", device="cuda")
+    p = mq.Plane.empty(M, K)
+    mq.mq_quantize_q8(x, p)
+    g = Guarded((M, N), torch.float32)
+    mq.gemm(kind, p, w, N, g.t)
+    torch.cuda.synchronize()
+    g.check()
+    assert g.untouched() == 0, "unwritten outputs"
+    rows = np.sort(np.random.default_rng(3).choice(M, 16, replace=False))
+    rows[-1] = M - 1
+    ref, bound = O.gemm_rows(p.qs.cpu().numpy(), p.d.cpu().numpy(), w.cpu().numpy(), kind, N, K, rows=rows)
+    got = g.t.cpu().numpy().astype(np.float64)[rows]
+    assert np.all(np.abs(got - ref) <= bound)
+    assert mq.mq_device_status() == mq.MQ_OK
