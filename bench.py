@@ -97,8 +97,9 @@ def plane_bytes(M, K, q8=True, op=False):
 
 
 def gemm_act_bytes(kind, M, K):
-    """Activation bytes a GEMM reads: the operand arrays ah, af and (q4_K's min term) ax."""
-    return 2 * M * K + M * (K // 256) * (36 if kind == "q4k" else 4)
+    """Activation bytes a GEMM reads: the operand arrays ah, af and (the min terms of q4_K and
+    q4_1) ax."""
+    return 2 * M * K + M * (K // 256) * (36 if kind in ("q4k", "q4_1") else 4)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -542,17 +543,23 @@ def run_sweep(steps: int, warmup: int):
                             "frac": max(t_tensor, t_stream) / t}
                     print(json.dumps(line))
                 del x, p, out
-    # the other block types (GEMV only) on the 14B decode shapes
+    # the other block types on the 14B decode shapes: the GEMV at M = 1, 2, 8; q4_0 / q4_1 also
+    # through the GEMM at M = 16 and 3314
     for kind in ("q5k", "q4_0", "q4_1"):
         for N, K in [(5120, 5120), (1024, 5120), (13824, 5120), (5120, 13824)]:
             w = S.weights(kind, N, K, 0, f"sweep.{kind}.{N}x{K}", device=dev)
-            for M in (1, 2, 8):
+            cases = [("gemv", M) for M in (1, 2, 8)] + ([("gemm", M) for M in (16, 3314)] if kind != "q5k" else [])
+            for path, M in cases:
                 x = S.normal((M, K), 0, f"sweep.x.{M}x{K}", device=dev)
-                p = mq.Plane.empty(M, K, dev, op=False)
+                p = mq.Plane.empty(M, K, dev, op=path == "gemm")
                 mq.mq_quantize_q8(x, p)
                 out = torch.empty((M, N), dtype=torch.float32, device=dev)
-                fn = lambda: mq.gemv(kind, p, w, N, out)
-                nbytes = wbytes(kind, N, K) + M * plane_bytes(1, K, op=False) + 4 * M * N
+                if path == "gemv":
+                    fn = lambda: mq.gemv(kind, p, w, N, out)
+                    nbytes = wbytes(kind, N, K) + M * plane_bytes(1, K, op=False) + 4 * M * N
+                else:
+                    fn = lambda: mq.gemm(kind, p, w, N, out)
+                    nbytes = wbytes(kind, N, K) + gemm_act_bytes(kind, M, K) + 4 * M * N
                 for _ in range(max(1, warmup)):
                     fn()
                 ts = []
@@ -566,8 +573,12 @@ def run_sweep(steps: int, warmup: int):
                     torch.cuda.synchronize()
                     ts.append(a.elapsed_time(b) * 1e-3)
                 t = statistics.median(ts)
-                print(json.dumps({"case": f"gemv_{kind}:{M}x{N}x{K}", "us": t * 1e6, "GBps": nbytes / t / 1e9,
-                                  "bound": "hbm", "frac": nbytes / (hbm * 1e9) / t}))
+                t_tensor = 2.0 * M * N * K / (peak_burst * 1e12)
+                t_stream = nbytes / (hbm * 1e9)
+                print(json.dumps({"case": f"{path}_{kind}:{M}x{N}x{K}", "us": t * 1e6, "GBps": nbytes / t / 1e9,
+                                  "TFLOPs": 2.0 * M * N * K / t / 1e12,
+                                  "bound": "tensor" if t_tensor >= t_stream else "hbm",
+                                  "frac": max(t_tensor, t_stream) / t}))
                 del x, p, out
     if mq.mq_device_status() != mq.MQ_OK:
         raise RuntimeError("device status")
