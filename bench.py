@@ -585,6 +585,34 @@ def run_sweep(steps: int, warmup: int):
     return 0
 
 
+# ----------------------------------------------------------------------------- decode alone
+
+def run_decode_only(steps: int, warmup: int):
+    """The 14B decode token launched eagerly: `warmup` tokens, then `steps` timed ones (384
+    launches each). Without graph replay the host's launch cost shows in the time; the mode
+    exists for launch lists (ncu -s 384*warmup -c 384)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    from quant_int8_quantized_gb300 import mq
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = Stack(dev)
+    for _ in range(warmup):
+        st.decode_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        st.decode_step()
+    b.record()
+    torch.cuda.synchronize()
+    if mq.mq_device_status() != mq.MQ_OK:
+        raise RuntimeError("device status")
+    t = a.elapsed_time(b) * 1e-3 / max(1, steps)
+    print(json.dumps({"decode_eager_ms_per_token": t * 1e3, "GBps": Stack.decode_bytes() / t / 1e9}))
+    return 0
+
+
 # ----------------------------------------------------------------------------- single-kernel cases
 
 def run_case(spec: str, steps: int, warmup: int):
@@ -663,6 +691,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--case", default=None, help="time one kernel, e.g. gemm_q4k:3314x18944x3584")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="run the decode token alone, eagerly (W warm-up tokens, then K timed), for launch lists")
     ap.add_argument("--sweep", action="store_true",
                     help="time the 60-case shape/token sweep; one JSON line per case with its roofline fraction")
     args = ap.parse_args()
@@ -670,6 +700,8 @@ def main():
         return run_case(args.case, args.steps, args.warmup)
     if args.sweep:
         return run_sweep(args.steps, args.warmup)
+    if args.decode_only:
+        return run_decode_only(args.steps, args.warmup)
     if args.impl == "reference":
         return run_reference(args)
     ws, rank, local = dist_setup()
