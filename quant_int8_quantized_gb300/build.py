@@ -50,14 +50,26 @@ def up_to_date() -> bool:
 
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile every CUDA translation unit and link libmq.so. Returns the library path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(LIBDIR, exist_ok=True)
+    return _build(LIB, [], force, verbose, ptxas_info)
+
+
+def build_variant(name: str, defines, force: bool = False) -> str:
+    """A separately named copy of the library compiled with extra -D definitions (test
+    builds: a short wait limit, failure injection), at _lib/<name>/libmq.so. The product
+    library is never built with them."""
+    return _build(os.path.join(LIBDIR, name, "libmq.so"), [f"-D{d}" for d in defines], force, False, False)
+
+
+def _build(lib: str, defines, force: bool, verbose: bool, ptxas_info: bool) -> str:
+    if not force and os.path.exists(lib) and all(os.path.getmtime(p) <= os.path.getmtime(lib) for p in _deps()):
+        return lib
+    libdir = os.path.dirname(lib)
+    os.makedirs(libdir, exist_ok=True)
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + list(defines)
 
     def compile_one(src):
-        obj = os.path.join(LIBDIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(libdir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -70,13 +82,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, log in results:
             if log.strip():
                 print(log)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

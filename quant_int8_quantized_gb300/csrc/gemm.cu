@@ -77,7 +77,15 @@ constexpr int kLaunchRegs = 96;         // 65536 / 640, rounded down to the allo
 constexpr int kRegsWG0 = 64, kRegsConv = 64, kRegsEpi = 144;
 static_assert(128 * kRegsWG0 + 32 * kConvWarps * kRegsConv + 32 * kEpiWarps * kRegsEpi <= kThreads * kLaunchRegs,
               "register split");
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+#ifndef MQ_WAIT_LIMIT_NS
+#define MQ_WAIT_LIMIT_NS 2000000000ull   // test builds may shorten it
+#endif
+constexpr uint64_t kWaitLimitNs = MQ_WAIT_LIMIT_NS;
+#ifdef MQ_TEST_INJECT
+// Test builds only: when set, CTA 0's TMA producer skips its first activation copy, so that
+// chunk's barrier never completes and the kernel's bounded waits run out (abort path).
+__device__ int g_test_skip_first_act;
+#endif
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol0 = 0, kSCol1 = BT, kACol = 2 * BT;   // accumulators, then the weight ring
 constexpr int kMTile = BW * 16 * 2;                           // q4_K min-term operand: 128 rows x K 16, f16
@@ -311,6 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         const int a = ga % C::kRA;
                         const uint32_t pa = (ga / C::kRA) & 1;
                         if (!wait1(sm, &sm.act_empty[a], pa ^ 1)) { ok = false; break; }
+#ifdef MQ_TEST_INJECT
+                        if (g_test_skip_first_act && blockIdx.x == 0 && ga == 0) continue;
+#endif
                         tc::mbar_arrive_expect_tx(&sm.act_full[a], (uint32_t)bt * KS * 2);
                         tc::tma_load_2d(sm.act[a], &tmAct, sb * 256 + KS * j, wk.m0, &sm.act_full[a]);
                         issA |= 1u << a;
@@ -879,6 +890,13 @@ int take_gemm_device_error(cudaStream_t stream, unsigned* code) {
     return MQ_OK;
 }
 }  // namespace mq
+
+#ifdef MQ_TEST_INJECT
+// Test builds only: switch the injected missing copy on or off.
+extern "C" int mq_test_inject(int on) {
+    return cudaMemcpyToSymbol(g_test_skip_first_act, &on, sizeof(on)) == cudaSuccess ? MQ_OK : MQ_ERR_LAUNCH;
+}
+#endif
 
 extern "C" int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     return launch_gemm<kQ4K>(a, w, N, out, stream);
