@@ -68,15 +68,7 @@ constexpr int BT = 192;                 // tokens per tile (MMA N)
 constexpr int KS = 64;                  // K per activation slot and weight-operand slot
 constexpr int RA = 5;                   // activation slots (q6_K; q4_K: one per K chunk, see Cfg)
 constexpr int RX = 3;                   // per-super-block stages (block sums, 2^-e, weight scales c)
-constexpr int kActBytes = BT * KS * 2;  // 24576
 constexpr int kAxBytes = BT * 32;       // 16 binary16 block-sum parts per token
-constexpr int kConvWarps = 8;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 128 + 32 * kConvWarps + 32 * kEpiWarps;
-constexpr int kLaunchRegs = 96;         // 65536 / 640, rounded down to the allocation unit
-constexpr int kRegsWG0 = 64, kRegsConv = 64, kRegsEpi = 144;
-static_assert(128 * kRegsWG0 + 32 * kConvWarps * kRegsConv + 32 * kEpiWarps * kRegsEpi <= kThreads * kLaunchRegs,
-              "register split");
 #ifndef MQ_WAIT_LIMIT_NS
 #define MQ_WAIT_LIMIT_NS 2000000000ull   // test builds may shorten it
 #endif
@@ -87,14 +79,13 @@ constexpr uint64_t kWaitLimitNs = MQ_WAIT_LIMIT_NS;
 __device__ int g_test_skip_first_act;
 #endif
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol0 = 0, kSCol1 = BT, kACol = 2 * BT;   // accumulators, then the weight ring
-constexpr int kMTile = BW * 16 * 2;                           // q4_K min-term operand: 128 rows x K 16, f16
-static_assert(kACol + 128 <= kTmemCols, "tensor memory");
+constexpr int kShortTok = 64;           // token tiles up to this take the short-tile form (q4_K)
+constexpr int kMTile = BW * 16 * 2;     // q4_K min-term operand: 128 rows x K 16, f16
 
 // Weight types of the GEMM.
 enum : int { kQ4K = 0, kQ6K = 1, kQ40 = 2, kQ41 = 3 };
 
-template <int WT>
+template <int WT, bool SH = false>
 struct Cfg {
     // q4_K: one exact binary16 operand per weight, K chunks of 64 (slot j = chunk j).
     // q6_K, q4_0, q4_1: two exact binary16 parts per weight, 32-wide quarters, two MMAs
@@ -123,20 +114,51 @@ struct Cfg {
     // the per-super-block block-sum stage the same way: half the issuer's waits.
     static constexpr bool kJoint = !kQuarters;
     static constexpr int kRA = WT == kQ4K ? 4 : RA;
+    // Tensor memory: two accumulators of kTok columns, then the weight-operand slots (32
+    // columns each, one K = 64 chunk of q4_K). A full tile (192 tokens) leaves room for one
+    // super-block's 4 slots: each chunk's operand is rewritten only after the previous
+    // super-block's MMAs of that chunk have completed. A short tile (SH, q4_K, at most 64
+    // tokens) keeps the operands of kD = 3 super-blocks and the activation ring as many (12
+    // slots of 64 tokens), so that the converters and the copies run up to three
+    // super-blocks ahead of the MMAs. There every K = 16 MMA costs a fixed ~96 cycles
+    // whatever its N (measured for N = 16 to 128, A from tensor or shared memory, one or
+    // several accumulators), so the MMAs, not the weight stream, set the pace; keeping them
+    // fed is what the deeper rings do. Activation slot a and operand slot a both hold K chunk
+    // a % 4 of a super-block, under one barrier pair.
+    static constexpr int kD = SH ? 3 : 1;
+    static constexpr int kNA = SH ? 4 * kD : kRA;      // activation slots
+    static constexpr int kTok = SH ? kShortTok : BT;   // tokens per tile at most
+    static constexpr int kActSlot = kTok * KS * 2;     // bytes per activation slot
+    static constexpr uint32_t kSCol1 = kTok, kACol = 2 * kTok;
+    // Warps: 4 (TMA producer, MMA issuer, TMEM allocator, idle), 8 weight converters (two per
+    // TMEM lane quarter, one K half each), 8 epilogue warps (two per lane quarter, kEpiCols
+    // token columns each). Registers: the launch's share per thread, redistributed by setmaxnreg.
+    static constexpr int kConvWarps = 8;
+    static constexpr int kEpiWarps = 8;
+    static constexpr int kThreads = 128 + 32 * (kConvWarps + kEpiWarps);
+    static constexpr int kLaunchRegs = 96;             // 65536 / kThreads, rounded down to 8
+    static constexpr int kRegsWG0 = 64, kRegsConv = 64, kRegsEpi = 144;
+    static_assert(128 * kRegsWG0 + 32 * kConvWarps * kRegsConv + 32 * kEpiWarps * kRegsEpi <= kThreads * kLaunchRegs,
+                  "register split");
+    static constexpr int kMinWarps = 4;                // warps writing the q4_K / q4_1 min-term operand
+    static constexpr int kEpiCols = kTok / 2;          // accumulator columns per epilogue thread
+    static_assert(!SH || WT == kQ4K, "short tiles: q4_K");
+    static_assert(kACol + kFCols * kRF * kD <= kTmemCols, "tensor memory");
 };
 
-template <int WT>
+template <int WT, bool SH = false>
 struct Smem {
-    static constexpr bool kMin = Cfg<WT>::kMin;
-    alignas(1024) uint8_t act[Cfg<WT>::kRA][kActBytes];
+    using C = Cfg<WT, SH>;
+    static constexpr bool kMin = C::kMin;
+    alignas(1024) uint8_t act[C::kNA][C::kActSlot];
     alignas(256) uint8_t ax[RX][kAxBytes];
     alignas(16) float af[RX][BT];
     float cvec[RX][BW];
-    alignas(128) uint8_t braw[Cfg<WT>::kRB][Cfg<WT>::kStage];
+    alignas(128) uint8_t braw[C::kRB][C::kStage];
     alignas(128) uint8_t mop[kMin ? RX : 1][kMin ? 2 * kMTile : 16];   // min-term operand (hi, lo) per stage
-    uint64_t act_full[Cfg<WT>::kRA], act_empty[Cfg<WT>::kRA], ax_full[RX], ax_empty[RX], c_full[RX], c_empty[RX];
-    uint64_t b_full[Cfg<WT>::kRB], b_empty[Cfg<WT>::kRB];
-    uint64_t a_full[Cfg<WT>::kRF], a_empty[Cfg<WT>::kRF][2];
+    uint64_t act_full[C::kNA], act_empty[C::kNA], ax_full[RX], ax_empty[RX], c_full[RX], c_empty[RX];
+    uint64_t b_full[C::kRB], b_empty[C::kRB];
+    uint64_t a_full[C::kRF], a_empty[C::kRF][2];
     uint64_t t_full[2], t_empty[2], mma_done;
     uint32_t tmem;
     int abort;
@@ -166,23 +188,23 @@ __device__ __forceinline__ bool mbar_ready(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-template <int WT>
-__device__ __forceinline__ bool wait1(Smem<WT>& sm, uint64_t* bar, uint32_t parity) {
+template <class SM>
+__device__ __forceinline__ bool wait1(SM& sm, uint64_t* bar, uint32_t parity) {
     if (mbar_ready(bar, parity) || tc::mbar_wait(bar, parity, kWaitLimitNs)) return true;
     atomicOr(&g_gemm_error, 1u);
     *(volatile int*)&sm.abort = 1;
     return false;
 }
 
-template <int WT>
-__device__ __forceinline__ bool aborted(Smem<WT>& sm) {
+template <class SM>
+__device__ __forceinline__ bool aborted(SM& sm) {
     return *(volatile int*)&sm.abort != 0;
 }
 
 // Whole-warp variants: every lane waits, and the outcome is made warp-uniform so
 // that the warp never diverges in front of a warp-collective operation.
-template <int WT>
-__device__ __forceinline__ bool wwait(Smem<WT>& sm, uint64_t* bar, uint32_t parity) {
+template <class SM>
+__device__ __forceinline__ bool wwait(SM& sm, uint64_t* bar, uint32_t parity) {
     const bool ok = __all_sync(0xffffffffu, mbar_ready(bar, parity) || tc::mbar_wait(bar, parity, kWaitLimitNs));
     if (!ok) {
         if ((threadIdx.x & 31) == 0) atomicOr(&g_gemm_error, 1u);
@@ -191,8 +213,8 @@ __device__ __forceinline__ bool wwait(Smem<WT>& sm, uint64_t* bar, uint32_t pari
     return ok;
 }
 
-template <int WT>
-__device__ __forceinline__ bool waborted(Smem<WT>& sm) {
+template <class SM>
+__device__ __forceinline__ bool waborted(SM& sm) {
     return __any_sync(0xffffffffu, aborted(sm));
 }
 
@@ -235,41 +257,72 @@ __device__ __forceinline__ void f16_split(uint32_t hb, int& m, int& E) {
     E = (e ? e : 1) - 25;
 }
 
+// q4_K super-block header (the word holding f16 d and dmin): k, the least power of two in
+// [0, 24] with |d| 2^k >= |dmin| (0 when d or dmin is 0; from the exponents and the
+// significands, as the doubling loop it replaces would find it), sk = 2^-k, c = d 2^k (dmin
+// when d = 0; exact) and rr = dmin / c.
+struct Q4KHead {
+    float d, c, rr, sk;
+};
+__device__ __forceinline__ Q4KHead q4k_head(uint32_t w) {
+    Q4KHead h;
+    h.d = __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+    const float dmin = __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+    int k = 0;
+    h.c = dmin;
+    h.rr = 1.0f;
+    if (h.d != 0.0f) {
+        const uint32_t bd = __float_as_uint(h.d) & 0x7fffffffu, bm = __float_as_uint(dmin) & 0x7fffffffu;
+        if (bm != 0u) {   // both normal in f32 (binary16 inputs): compare exponents, then significands
+            const int kk = (int)(bm >> 23) - (int)(bd >> 23) + ((bm & 0x7fffffu) > (bd & 0x7fffffu) ? 1 : 0);
+            k = min(24, max(0, kk));
+        }
+        h.c = __int_as_float(__float_as_int(h.d) + (k << 23));
+        h.rr = __fdiv_rn(dmin, h.c);
+    }
+    h.sk = __int_as_float((127 - k) << 23);
+    return h;
+}
+
 // A 32-bit word from a 2-byte-aligned shared-memory address.
 __device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
     return (uint32_t)*reinterpret_cast<const uint16_t*>(p) | ((uint32_t)*reinterpret_cast<const uint16_t*>(p + 2) << 16);
 }
 
-template <int WT>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmAct,
+template <int WT, bool SH>
+__global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmAct,
                                                            const __grid_constant__ CUtensorMap tmAx,
                                                            const __grid_constant__ CUtensorMap tmAf,
                                                            const __grid_constant__ CUtensorMap tmW,
                                                            float* __restrict__ out, int M, int N, int K, int splits,
                                                            int nfast, int bt) {
-    using C = Cfg<WT>;
+    using C = Cfg<WT, SH>;
     constexpr int kRB = C::kRB, kRF = C::kRF;
     extern __shared__ uint8_t smem_raw[];
-    Smem<WT>& sm = *reinterpret_cast<Smem<WT>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    Smem<WT, SH>& sm = *reinterpret_cast<Smem<WT, SH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int S = K / mq::QK_K;
     const int num_mt = (M + bt - 1) / bt, num_nt = (N + BW - 1) / BW;
     const int units = num_mt * num_nt * splits;
 
     if (tid == 0) {
-        for (int i = 0; i < C::kRA; ++i) {
+        tc::prefetch_tensormap(&tmW);
+        tc::prefetch_tensormap(&tmAct);
+        tc::prefetch_tensormap(&tmAx);
+        tc::prefetch_tensormap(&tmAf);
+        for (int i = 0; i < C::kNA; ++i) {
             tc::mbar_init(&sm.act_full[i], C::kJoint ? 5 : 1);
             tc::mbar_init(&sm.act_empty[i], 1);
         }
         for (int i = 0; i < RX; ++i) {
-            tc::mbar_init(&sm.ax_full[i], C::kMin ? 5 : 1);   // + the 4 warps writing the min operand
-            tc::mbar_init(&sm.ax_empty[i], 1 + kEpiWarps);   // the MMAs (block sums) and the epilogue (2^-e)
+            tc::mbar_init(&sm.ax_full[i], C::kMin ? 1 + C::kMinWarps : 1);   // + the warps writing the min operand
+            tc::mbar_init(&sm.ax_empty[i], 1 + C::kEpiWarps);   // the MMAs (block sums) and the epilogue (2^-e)
             tc::mbar_init(&sm.c_full[i], 4);
-            tc::mbar_init(&sm.c_empty[i], kEpiWarps);
+            tc::mbar_init(&sm.c_empty[i], C::kEpiWarps);
         }
         for (int i = 0; i < kRB; ++i) {
             tc::mbar_init(&sm.b_full[i], 1);
-            tc::mbar_init(&sm.b_empty[i], kConvWarps);
+            tc::mbar_init(&sm.b_empty[i], C::kConvWarps);
         }
         for (int i = 0; i < kRF; ++i) {
             tc::mbar_init(&sm.a_full[i], 4);
@@ -278,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&sm.t_full[i], 1);
-            tc::mbar_init(&sm.t_empty[i], kEpiWarps);
+            tc::mbar_init(&sm.t_empty[i], C::kEpiWarps);
         }
         tc::mbar_init(&sm.mma_done, 1);
         sm.abort = 0;
@@ -291,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     if (warp < 4) {
         // ============================================================ warpgroup 0
-        tc::setmaxnreg_dec<kRegsWG0>();
+        tc::setmaxnreg_dec<C::kRegsWG0>();
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------- TMA producer
             uint32_t issA = 0, phA = 0, issX = 0, phX = 0, issB = 0, phB = 0;   // copies in flight (for an abort)
@@ -316,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     }
                     bool ok = true;
                     for (int j = 0; j < 4; ++j, ++ga) {
-                        const int a = ga % C::kRA;
-                        const uint32_t pa = (ga / C::kRA) & 1;
+                        const int a = ga % C::kNA;
+                        const uint32_t pa = (ga / C::kNA) & 1;
                         if (!wait1(sm, &sm.act_empty[a], pa ^ 1)) { ok = false; break; }
 #ifdef MQ_TEST_INJECT
                         if (g_test_skip_first_act && blockIdx.x == 0 && ga == 0) continue;
@@ -331,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
             }
             if (aborted(sm)) {   // let every copy already issued land before the CTA exits
-                for (int i = 0; i < C::kRA; ++i) if (issA >> i & 1u) tc::mbar_wait(&sm.act_full[i], phA >> i & 1u, kWaitLimitNs);
+                for (int i = 0; i < C::kNA; ++i) if (issA >> i & 1u) tc::mbar_wait(&sm.act_full[i], phA >> i & 1u, kWaitLimitNs);
                 for (int i = 0; i < RX; ++i) if (issX >> i & 1u) tc::mbar_wait(&sm.ax_full[i], phX >> i & 1u, kWaitLimitNs);
                 for (int i = 0; i < kRB; ++i) if (issB >> i & 1u) tc::mbar_wait(&sm.b_full[i], phB >> i & 1u, kWaitLimitNs);
             }
@@ -353,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             // slot and its first quarter's operand (the second quarter is waited for between
             // the first quarter's MMAs)
             auto chunk_ready = [&](int sbc_, int j_, int ga_) {
-                if constexpr (C::kJoint) return wait1(sm, &sm.act_full[j_], sbc_ & 1);
-                return wait1(sm, &sm.act_full[ga_ % C::kRA], (ga_ / C::kRA) & 1) &&
+                if constexpr (C::kJoint) return wait1(sm, &sm.act_full[ga_ % C::kNA], (ga_ / C::kNA) & 1);
+                return wait1(sm, &sm.act_full[ga_ % C::kNA], (ga_ / C::kNA) & 1) &&
                        wait1(sm, &sm.a_full[(2 * j_) & 3], (uint32_t)(j_ >> 1));
             };
             auto sb_ready = [&](int sbc_, int ga_) {   // accumulator slot free, first chunk ready
@@ -365,13 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             int ga = 0;
             for (int sbc = 0; sbc < total && ok; ++sbc) {
                 const int s = sbc & 1, x = sbc % RX;
-                const uint32_t dcol = tbase + (s ? kSCol1 : kSCol0);
+                const uint32_t dcol = tbase + (s ? C::kSCol1 : 0u);
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const int a = (ga + j) % C::kRA;
+                    const int a = (ga + j) % C::kNA;
                     const uint32_t sa = tc::smem_u32(sm.act[a]);
                     if constexpr (!C::kQuarters) {
-                        const uint32_t fa = tbase + kACol + C::kFCols * j;
+                        const uint32_t fa = tbase + C::kACol + C::kFCols * a;   // operand slot a
 #pragma unroll
                         for (int k = 0; k < 2; ++k)
                             tc::mma_f16_ts(dcol, fa + 8 * k, tc::smem_desc_sw128(sa + 32 * k), idesc, (j | k) ? 1u : 0u);
@@ -389,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
                             const int qq = (2 * j + i) & 3;
-                            const uint32_t fa = tbase + kACol + C::kFCols * qq;
+                            const uint32_t fa = tbase + C::kACol + C::kFCols * qq;
 #pragma unroll
                             for (int k = 0; k < 2; ++k) {
                                 const uint64_t bd = tc::smem_desc_sw128(sa + 64 * i + 32 * k);
@@ -433,9 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc::tc_fence_before();
         }
         __syncwarp();
-    } else if (warp < 4 + kConvWarps) {
+    } else if (warp < 4 + C::kConvWarps) {
         // ============================================================ weight converters
-        tc::setmaxnreg_dec<kRegsConv>();
+        tc::setmaxnreg_dec<C::kRegsConv>();
         const int q = warp & 3, h = (warp - 4) >> 2;
         const int r = 32 * q + lane;                            // weight row within the tile
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
@@ -448,28 +501,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (!wwait(sm, &sm.b_full[b], (sbc / kRB) & 1)) break;
                 const uint8_t* row = sm.braw[b] + r * C::kRowBytes;
                 if constexpr (WT == kQ4K) {
-                    // ---- q4_K: scales and the power of two k; the main operand, then (h == 0) the
-                    //      min-term operand and the epilogue's scale c
+                    // ---- q4_K: scales and the power of two k; the main operand of chunks 2h, 2h + 1,
+                    //      then (h == 0) the min-term operand and the epilogue's scale c
                     const uint4 hdr = *reinterpret_cast<const uint4*>(row);
-                    const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
-                    const float dmin = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
-                    int k = 0;
-                    float c = dmin, rr = 1.0f;
-                    if (d != 0.0f) {
-                        float t = fabsf(d);
-                        while (t < fabsf(dmin) && k < 24) {
-                            t *= 2.0f;
-                            ++k;
-                        }
-                        c = ldexpf(d, k);
-                        rr = __fdiv_rn(dmin, c);
-                    }
-                    // ---- the main operand: slots j = 2h, 2h + 1 (sub-blocks 2j, 2j + 1)
-                    bool ok = true;
-#pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        const int j = 2 * h + jj, f = j;   // slot j: this half's own, one use a super-block
-                        if (!wwait(sm, &sm.act_empty[f], (sbc & 1) ^ 1)) { ok = false; break; }
+                    const Q4KHead hd = q4k_head(hdr.x);
+                    // chunk j of super-block sbc: operand (and activation) slot f, written by this
+                    // half only, once the MMAs of its previous use (kD super-blocks ago) completed
+                    auto main_chunk = [&](int j) -> bool {
+                        const int f = 4 * (sbc % C::kD) + j;
+                        if (!wwait(sm, &sm.act_empty[f], ((sbc / C::kD) & 1) ^ 1)) return false;
                         tc::tc_fence_after();   // the stores below come after the MMAs that read the slot
                         const int s0 = j < 2 ? (int)(byte_of(hdr.y, hdr.z, hdr.w, 2 * j) & 63u)
                                              : (int)((byte_of(hdr.y, hdr.z, hdr.w, 2 * j + 4) & 15u) |
@@ -477,8 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         const int s1 = j < 2 ? (int)(byte_of(hdr.y, hdr.z, hdr.w, 2 * j + 1) & 63u)
                                              : (int)((byte_of(hdr.y, hdr.z, hdr.w, 2 * j + 5) & 15u) |
                                                      ((byte_of(hdr.y, hdr.z, hdr.w, 2 * j - 3) >> 6) << 4));
-                        const float m0f = d != 0.0f ? ldexpf((float)s0, -k) : 0.0f;
-                        const float m1f = d != 0.0f ? ldexpf((float)s1, -k) : 0.0f;
+                        const float m0f = hd.d != 0.0f ? (float)s0 * hd.sk : 0.0f;   // sc 2^-k, exact
+                        const float m1f = hd.d != 0.0f ? (float)s1 * hd.sk : 0.0f;
                         const uint32_t mul0 = h2_of(m0f), add0 = h2_of(-1024.0f * m0f);
                         const uint32_t mul1 = h2_of(m1f), add1 = h2_of(-1024.0f * m1f);
                         const uint4 qa = *reinterpret_cast<const uint4*>(row + 16 + 32 * j);
@@ -490,34 +530,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             nib4_1024(wv[w] & 0x0F0F0F0Fu, mul0, add0, o[2 * w], o[2 * w + 1]);
                             nib4_1024((wv[w] >> 4) & 0x0F0F0F0Fu, mul1, add1, o[16 + 2 * w], o[16 + 2 * w + 1]);
                         }
-                        tc::tmem_st32(tbase + lane_bits + kACol + C::kFCols * f, o);
+                        tc::tmem_st32(tbase + lane_bits + C::kACol + C::kFCols * f, o);
                         tc::tmem_st_wait();
                         tc::tc_fence_before();
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&sm.act_full[f]);
-                    }
+                        return true;
+                    };
+                    // min-term operand of sub-blocks 2i, 2i + 1: -(dmin / c) m as exact hi + lo
+                    // binary16 parts, packed in pairs
+                    auto min_pair = [&](int i, uint32_t& hi, uint32_t& lo) {
+                        float v[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int jj = 2 * i + e;
+                            const uint32_t mn = jj < 4 ? (byte_of(hdr.y, hdr.z, hdr.w, jj + 4) & 63u)
+                                                       : ((byte_of(hdr.y, hdr.z, hdr.w, jj + 4) >> 4) |
+                                                          ((byte_of(hdr.y, hdr.z, hdr.w, jj) >> 6) << 4));
+                            v[e] = -__fmul_rn(hd.rr, (float)mn);
+                        }
+                        const float hi0 = __half2float(__float2half_rn(v[0])), hi1 = __half2float(__float2half_rn(v[1]));
+                        hi = h2_pack(v[0], v[1]);
+                        lo = h2_pack(__fsub_rn(v[0], hi0), __fsub_rn(v[1], hi1));
+                    };
+                    // row r of the hi tile [hi_0..hi_7, hi_0..hi_7] and of the lo tile, K-major
+                    // without swizzle: core matrices of 8 rows x 16 B, K-adjacent ones 128 B apart
+                    uint8_t* mt = sm.mop[x] + (r >> 3) * 256 + (r & 7) * 16;
+                    bool ok = true;
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj)
+                        if (!main_chunk(2 * h + jj)) { ok = false; break; }
                     if (!ok) break;
                     if (h == 0) {
                         if (!wwait(sm, &sm.ax_empty[x], ((sbc / RX) & 1) ^ 1)) break;
                         uint32_t mh[8];
 #pragma unroll
-                        for (int j = 0; j < 8; j += 2) {
-                            float v[2];
-#pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-                                const int jj = j + e;
-                                const uint32_t mn = jj < 4 ? (byte_of(hdr.y, hdr.z, hdr.w, jj + 4) & 63u)
-                                                           : ((byte_of(hdr.y, hdr.z, hdr.w, jj + 4) >> 4) |
-                                                              ((byte_of(hdr.y, hdr.z, hdr.w, jj) >> 6) << 4));
-                                v[e] = -__fmul_rn(rr, (float)mn);
-                            }
-                            const float hi0 = __half2float(__float2half_rn(v[0])), hi1 = __half2float(__float2half_rn(v[1]));
-                            mh[j / 2] = h2_pack(v[0], v[1]);
-                            mh[4 + j / 2] = h2_pack(__fsub_rn(v[0], hi0), __fsub_rn(v[1], hi1));
-                        }
-                        // row r of the hi tile [hi_0..hi_7, hi_0..hi_7] and of the lo tile, K-major
-                        // without swizzle: core matrices of 8 rows x 16 B, K-adjacent ones 128 B apart
-                        uint8_t* mt = sm.mop[x] + (r >> 3) * 256 + (r & 7) * 16;
+                        for (int i = 0; i < 4; ++i) min_pair(i, mh[i], mh[4 + i]);
                         const uint4 vh = make_uint4(mh[0], mh[1], mh[2], mh[3]), vl = make_uint4(mh[4], mh[5], mh[6], mh[7]);
                         *reinterpret_cast<uint4*>(mt) = vh;
                         *reinterpret_cast<uint4*>(mt + 128) = vh;
@@ -527,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&sm.ax_full[x]);
                         if (!wwait(sm, &sm.c_empty[x], ((sbc / RX) & 1) ^ 1)) break;
-                        sm.cvec[x][r] = n < N ? c : 0.0f;
+                        sm.cvec[x][r] = n < N ? hd.c : 0.0f;
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&sm.c_full[x]);
                     }
@@ -549,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     for (int t = 0; t < 4; ++t) {
                         if (!wwait(sm, &sm.a_empty[t][h], h ? (sbc & 1) : ((sbc & 1) ^ 1))) { ok = false; break; }
                         tc::tc_fence_after();   // the stores below come after the MMAs that read the slot
-                        const uint32_t fa = tbase + lane_bits + kACol + C::kFCols * t;
+                        const uint32_t fa = tbase + lane_bits + C::kACol + C::kFCols * t;
                         const uint32_t scw = (t < 2) ? c6.x : c6.y;     // scale bytes 2t, 2t + 1 of the half
                         const uint4 l0 = *reinterpret_cast<const uint4*>(half + 32 * (t & 1));
                         const uint4 l1 = *reinterpret_cast<const uint4*>(half + 32 * (t & 1) + 16);
@@ -633,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                             nib4_one(lo, mul2, add2, p2[2 * i], p2[2 * i + 1]);
                             nib4_one(hi, mul2, add2, p2[8 + 2 * i], p2[9 + 2 * i]);
                         }
-                        const uint32_t fa = tbase + lane_bits + kACol + C::kFCols * t;
+                        const uint32_t fa = tbase + lane_bits + C::kACol + C::kFCols * t;
                         tc::tmem_st16(fa, p1);
                         tc::tmem_st16(fa + 16, p2);
                         tc::tmem_st_wait();
@@ -681,17 +729,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
     } else {
         // ============================================================ epilogue
-        tc::setmaxnreg_inc<kRegsEpi>();
-        const int ew = warp - 4 - kConvWarps;
-        const int q = warp & 3, ch = ew >> 2;         // lane quarter, column half (96 tokens)
+        tc::setmaxnreg_inc<C::kRegsEpi>();
+        const int ew = warp - 4 - C::kConvWarps;
+        const int q = warp & 3, ch = ew >> 2;         // lane quarter, column half (kEpiCols tokens)
         const int r = 32 * q + lane;
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         int sbc = 0;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
             const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt);
-            float acc[96];
+            float acc[C::kEpiCols];
 #pragma unroll
-            for (int i = 0; i < 96; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0.0f;
             bool ok = true;
             for (int sb = wk.sb0; sb < wk.sb1; ++sb, ++sbc) {
                 const int s = sbc & 1, x = sbc % RX;
@@ -702,21 +750,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 tc::tc_fence_after();
                 const float c = sm.cvec[x][r];
-                const uint32_t ta = tbase + lane_bits + (s ? kSCol1 : kSCol0) + 96 * ch;
+                const uint32_t ta = tbase + lane_bits + (s ? C::kSCol1 : 0u) + C::kEpiCols * ch;
+                // 16 columns at a time (32 at a time, the accumulators no longer all fit in registers)
 #pragma unroll
-                for (int cc = 0; cc < 3; ++cc) {
-                    if (96 * ch + 32 * cc >= bt) break;   // no token of the tile in these columns
-                    uint32_t v[32];
-                    tc::tmem_ld32(ta + 32 * cc, v);
+                for (int cc = 0; cc < C::kEpiCols / 16; ++cc) {
+                    if (C::kEpiCols * ch + 16 * cc >= bt) break;   // no token of the tile in these columns
+                    uint32_t v[16];
+                    tc::tmem_ld16(ta + 16 * cc, v);
                     tc::tmem_ld_wait();
-                    const float4* fp = reinterpret_cast<const float4*>(&sm.af[x][96 * ch + 32 * cc]);
+                    const float4* fp = reinterpret_cast<const float4*>(&sm.af[x][C::kEpiCols * ch + 16 * cc]);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int i = 0; i < 4; ++i) {
                         const float4 f4 = fp[i];
                         float g0, g1, g2, g3;
                         tc::fmul2(g0, g1, c, c, f4.x, f4.y);
                         tc::fmul2(g2, g3, c, c, f4.z, f4.w);
-                        float* a = &acc[32 * cc + 4 * i];
+                        float* a = &acc[16 * cc + 4 * i];
                         tc::ffma2(a[0], a[1], g0, g1, __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]));
                         tc::ffma2(a[2], a[3], g2, g3, __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
                     }
@@ -732,10 +781,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             if (!ok) break;
             const int n = wk.n0 + r;
             if (n < N) {
-                const int t0 = wk.m0 + 96 * ch;
+                const int t0 = wk.m0 + C::kEpiCols * ch;
                 float* op = out + (size_t)t0 * N + n;
 #pragma unroll
-                for (int i = 0; i < 96; ++i) {
+                for (int i = 0; i < C::kEpiCols; ++i) {
                     if (t0 + i < M) {
                         if (splits > 1) atomicAdd(op + (size_t)i * N, acc[i]);
                         else op[(size_t)i * N] = acc[i];
@@ -812,7 +861,7 @@ int check_gemm(const mq_q8_plane* a, const void* w, int N, const float* out) {
 // Once per device: the register split between warpgroups assumes the launch register
 // count, and the kernel's shared-memory size is set. Later calls make no attribute
 // calls, so a sequence of entry points can be captured in a graph.
-template <int WT>
+template <int WT, bool SH>
 bool gemm_ready(size_t smem) {
     constexpr int kMaxDevices = 64;
     static int state[kMaxDevices];   // 0 unknown, 1 ready, 2 failed
@@ -825,8 +874,8 @@ bool gemm_ready(size_t smem) {
         v = state[dev];
         if (v == 0) {
             cudaFuncAttributes fa;
-            v = (cudaFuncGetAttributes(&fa, gemm_kernel<WT>) == cudaSuccess && fa.numRegs == kLaunchRegs &&
-                 cudaFuncSetAttribute(gemm_kernel<WT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+            v = (cudaFuncGetAttributes(&fa, gemm_kernel<WT, SH>) == cudaSuccess && fa.numRegs == Cfg<WT, SH>::kLaunchRegs &&
+                 cudaFuncSetAttribute(gemm_kernel<WT, SH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
                      cudaSuccess)
                     ? 1
                     : 2;
@@ -848,14 +897,16 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
     int rc = check_gemm(a, w, N, out);
     if (rc != MQ_OK || N == 0 || a->M == 0) return rc;
     const int M = a->M, K = a->K, S = K / mq::QK_K;
-    const size_t smem = sizeof(Smem<WT>) + 1024;
-    if (!gemm_ready<WT>(smem)) return MQ_ERR_LAUNCH;
+    const int bt = token_tile(M);
+    constexpr bool kS = WT == kQ4K;   // the short-tile form exists for q4_K
+    const bool sh = kS && bt <= kShortTok;
+    const size_t smem = sh ? sizeof(Smem<WT, kS>) + 1024 : sizeof(Smem<WT, false>) + 1024;
+    if (!(sh ? gemm_ready<WT, kS>(smem) : gemm_ready<WT, false>(smem))) return MQ_ERR_LAUNCH;
     const unsigned long long row = (unsigned long long)S * Cfg<WT>::kSB;
     CUtensorMap tmAct, tmAx, tmAf, tmW;
     if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row, (uint64_t)N, row, Cfg<WT>::kRowBytes, BW))
         return MQ_ERR_LAUNCH;
     const int mp = mq::af_stride(M);
-    const int bt = token_tile(M);
     if (!make_map(&tmAct, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ah, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, KS, bt,
                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tmAx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ax, (uint64_t)S * 16, (uint64_t)M, (uint64_t)S * 32, 16,
@@ -871,7 +922,10 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
     const int grid = (int)(units < sms ? units : sms);
     // weight-row tiles fastest when the activations outweigh the weights
     const int nfast = (double)M * K * 2 > (double)N * row ? 1 : 0;
-    gemm_kernel<WT><<<grid, kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits, nfast, bt);
+    if (sh)
+        gemm_kernel<WT, kS><<<grid, Cfg<WT, kS>::kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits, nfast, bt);
+    else
+        gemm_kernel<WT, false><<<grid, Cfg<WT, false>::kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits, nfast, bt);
     return mq::launch_status();
 }
 

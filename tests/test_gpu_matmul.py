@@ -89,10 +89,12 @@ def test_gemm_partial_last_wave_every_element(kind, M, N, K):
 
 
 @pytest.mark.parametrize("kind", ["q4k", "q6k"])
-@pytest.mark.parametrize("M", [2, 3, 8, 15])
+@pytest.mark.parametrize("M", [2, 3, 8, 15, 24, 40, 64, 65])
 def test_gemm_small_batch_every_element(kind, M):
-    """Small batches, M in [2, 16): one 16-token tile (MMA N = 16), the weight rows split along
-    K across the SMs. Every element of a ragged, several-tile product within the bound."""
+    """Small batches: one token tile of round_up(M, 16) (MMA N = 16 for M in [2, 16)), the weight
+    rows split along K across the SMs; q4_K tiles of up to 64 tokens take the short-tile form
+    (M = 65 is the first full-form tile). Every element of a ragged, several-tile product
+    within the bound."""
     N, K = 1000, 3584
     x = synth.with_outliers(synth.normal((M, K), 0, f"sbx{M}"), 0, f"sbo{M}")
     out, p, w = _run(kind, x, N, K, mq.gemm)
@@ -289,16 +291,20 @@ def _unit_activations(rng, M, K, small_first_half=False):
     return torch.from_numpy(x)
 
 
-@pytest.mark.parametrize("M,N,K", [(16, 256, 512), (130, 200, 768), (300, 1100, 1280), (3, 300, 768), (8, 200, 1280)])
-def test_gemm_q4k_exact_integer_dots(M, N, K):
-    """Unit super-block scales (d = dmin = 1), sub-block scales 0 or 1, mins 0..7 and d_a = 1:
-    the operand form is exact (ah = 4q, block sums 4s, dmin/d = 1), every product and partial
-    sum is an integer below 2^24, so the GEMM must equal the f64 oracle bit for bit."""
+@pytest.mark.parametrize("d,dmin", [(1.0, 1.0), (1.0, 4.0), (1.0, 3.0), (0.5, 3.0), (2.0, 0.5)])
+@pytest.mark.parametrize("M,N,K", [(16, 256, 512), (130, 200, 768), (300, 1100, 1280), (3, 300, 768), (8, 200, 1280),
+                                   (48, 300, 768)])
+def test_gemm_q4k_exact_integer_dots(M, N, K, d, dmin):
+    """Super-block scales d, dmin chosen so that the kernel's power of two k (the least k >= 0
+    with d 2^k >= dmin: 0, 2, 2, 3, 0 here) and its operands are exact: sub-block scales 0 or
+    1, mins 0..7, d_a = 1, so ah = 4q, the weight operand sc q 2^-k and dmin / (d 2^k) are exact
+    binary16 values and every partial sum is a multiple of 2^-3 far below 2^21. The GEMM (short
+    tiles for M <= 64, full tiles above) must then equal the f64 oracle bit for bit."""
     rng = np.random.default_rng(M + N + K)
     S = K // 256
     blk = np.zeros((N, S, 144), np.uint8)
-    blk[..., 0:2] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
-    blk[..., 2:4] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+    blk[..., 0:2] = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+    blk[..., 2:4] = np.frombuffer(np.float16(dmin).tobytes(), np.uint8)
     sc = rng.integers(0, 2, size=(N, S, 8))
     mn = rng.integers(0, 8, size=(N, S, 8))
     # 6-bit fields < 16: bytes 0..3 scales 0..3, 4..7 mins 0..3, 8..11 scale | min << 4 of 4..7
