@@ -36,9 +36,10 @@ def _gemm(L, p, w, N, out):
     return L.mq_gemm_q4k(ctypes.byref(cp), ctypes.c_void_p(w.data_ptr()), N, ctypes.c_void_p(out.data_ptr()), stream)
 
 
-def test_gemm_wait_runs_out_and_is_reported_then_recovers(L):
-    M, N, K = 384, 640, 1024
-    x = synth.normal((M, K), 0, "ab.x", device="cuda")
+@pytest.mark.parametrize("M", [384, 16])   # full tiles; the short-tile form (16 tokens)
+def test_gemm_wait_runs_out_and_is_reported_then_recovers(L, M):
+    N, K = 640, 1024
+    x = synth.normal((M, K), 0, f"ab.x{M}", device="cuda")
     w = synth.weights("q4k", N, K, 0, "ab.w", device="cuda")
     p = mq.Plane.empty(M, K)
     cp = p.c()
