@@ -143,6 +143,10 @@ __device__ __forceinline__ int mq_rint_div(float v, float d, float inv) {
 // shuffles at offsets 4, 2, 1 (max and integer sums are exact in any order).
 // q = rint(v / d) with the correctly rounded quotient (see mq_rint_div).
 // Returns the packed int8 quants; d and s are valid in every lane of the group.
+// kUniform: the band test is one warp vote for the warp's 128 values (the whole warp must call
+// it together); the fused SwiGLU producer, whose long per-value arithmetic comes before,
+// runs faster with the per-value test (kUniform = false).
+template <bool kUniform = true>
 __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v2, float v3,
                                                      float& d_out, int& s_out, int (&q)[4]) {
     float am = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
@@ -150,10 +154,24 @@ __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
     am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
     const float d = __fdiv_rn(am, 127.0f);
+    float inv;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(inv) : "f"(d));
     int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
-    if (d != 0.0f) {
-        float inv;
-        asm("rcp.approx.f32 %0, %1;" : "=f"(inv) : "f"(d));
+    // Common case, one warp-uniform test for all four values of every lane: each product lies
+    // outside the band around n + 1/2 (or the block is all zero), so rint of the product is
+    // rint of the quotient (see mq_rint_div). Otherwise the lanes take the per-value path.
+    const float t0 = v0 * inv, t1 = v1 * inv, t2 = v2 * inv, t3 = v3 * inv;
+    const float r0 = rintf(t0), r1 = rintf(t1), r2 = rintf(t2), r3 = rintf(t3);
+    constexpr float kIn = 0.5f - 6.2e-5f;
+    const bool clear = fabsf(t0 - r0) < kIn && fabsf(t1 - r1) < kIn && fabsf(t2 - r2) < kIn && fabsf(t3 - r3) < kIn;
+    if (kUniform && __all_sync(0xffffffffu, d == 0.0f || (isfinite(inv) && clear))) {
+        if (d != 0.0f) {
+            q0 = max(-127, min(127, (int)r0));
+            q1 = max(-127, min(127, (int)r1));
+            q2 = max(-127, min(127, (int)r2));
+            q3 = max(-127, min(127, (int)r3));
+        }
+    } else if (d != 0.0f) {
         if (isfinite(inv)) {
             q0 = mq_rint_div(v0, d, inv);
             q1 = mq_rint_div(v1, d, inv);
