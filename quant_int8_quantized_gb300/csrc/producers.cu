@@ -130,7 +130,7 @@ __device__ __forceinline__ void quant_pair(const Out& o, long long pair, int lan
 // super-block (required when the plane holds the operand form). R == 1 writes the q8
 // arrays only.
 template <int R>
-__global__ void __launch_bounds__(kThreads) quantize_q8_kernel(const float4* __restrict__ x, Out o, long long rounds) {
+__global__ void __launch_bounds__(kThreads, 4) quantize_q8_kernel(const float4* __restrict__ x, Out o, long long rounds) {
     mq_grid_release();
     mq_grid_wait();
     const int lane = threadIdx.x & 31;
