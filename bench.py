@@ -177,7 +177,7 @@ class Stack:
         # q6_K weights are prepacked once, as at weight registration (the GEMM's weight form)
         self.W = [{n: mq.gemm_weights(kind, S.weights(kind, N, K, seed, f"L{l}.{n}", device=dev), N, K)
                    for n, kind, N, K, _ in PREFILL_MATS} for l in range(LAYERS)]
-        self.lm_head = S.q6k_weights(VOCAB, HID, seed, "lm_head", device=dev)
+        self.lm_head = mq.mq_prepack_q6k(S.q6k_weights(VOCAB, HID, seed, "lm_head", device=dev), VOCAB, HID)
         f32 = dict(dtype=torch.float32, device=dev)
         self.out = {n: torch.empty((M_TOK, N), **f32) for n, _, N, _, _ in PREFILL_MATS}
         # prefill planes feed only GEMMs: the producers write the operand arrays alone
@@ -200,7 +200,8 @@ class Stack:
                 kinds, Ks = {mats[p][0] for p in parts}, {mats[p][2] for p in parts}
                 assert len(kinds) == 1 and len(Ks) == 1
                 self.dstack[name] = (kinds.pop(), sum(mats[p][1] for p in parts), Ks.pop())
-            self.DW = [{n: S.weights(kind, N, K, seed, f"D{l}.{n}", device=dev)
+            # q6_K matrices prepacked, as for the prefill GEMM: one registered form serves both
+            self.DW = [{n: mq.gemm_weights(kind, S.weights(kind, N, K, seed, f"D{l}.{n}", device=dev), N, K)
                         for n, (kind, N, K) in self.dstack.items()} for l in range(D_LAYERS)]
             self.dout = {n: torch.empty((N,), **f32) for n, (_, N, _) in self.dstack.items()}
             self.dp_h = mq.Plane.empty(1, D_HID, dev, op=False)
@@ -236,7 +237,7 @@ class Stack:
                 else:
                     mq.gemm(kind, planes[src], W[name], N, self.out[name])
         mq.mq_rms_quant(self.out["down"][-1:], self.final_w, EPS, self.p_last)
-        mq.mq_gemv_q6k(self.p_last, self.lm_head, VOCAB, self.logits)
+        mq.mq_gemv_q6k_packed(self.p_last, self.lm_head, VOCAB, self.logits)
 
     def decode_step(self):
         mq = self.mq
@@ -246,7 +247,7 @@ class Stack:
             mq.mq_rms_quant(self.dx, self.drms[l], EPS, self.dp_h)
             self.ev_h.record(main)
             self.side.wait_event(self.ev_h)
-            mq.mq_gemv_q6k(self.dp_h, W["kv"], 2 * D_KV, self.dout["kv"], stream=self.side)
+            mq.mq_gemv_q6k_packed(self.dp_h, W["kv"], 2 * D_KV, self.dout["kv"], stream=self.side)
             self.ev_kv.record(self.side)
             mq.mq_gemv_q4k(self.dp_h, W["q"], D_HID, self.dout["q"])
             main.wait_event(self.ev_kv)
@@ -254,7 +255,7 @@ class Stack:
             mq.mq_gemv_q4k(self.dp_a, W["o"], D_HID, self.dout["o"])
             mq.mq_gemv_q4k(self.dp_h, W["gate_up"], 2 * D_FFN, self.dout["gate_up"])
             mq.mq_swiglu_quant(self.dg, self.du, self.dp_f)
-            mq.mq_gemv_q6k(self.dp_f, W["down"], D_HID, self.dout["down"])
+            mq.mq_gemv_q6k_packed(self.dp_f, W["down"], D_HID, self.dout["down"])
 
     @staticmethod
     def prefill_flops():
@@ -271,14 +272,14 @@ class Stack:
             W = self.DW[l]
             mq.mq_rms_quant(self.dx, self.drms[l], EPS, self.dp_h)
             mq.mq_gemv_q4k(self.dp_h, W["q"], D_HID, self.dout["q"])
-            mq.mq_gemv_q6k(self.dp_h, W["kv"][:D_KV], D_KV, self.dout["kv"][:D_KV])
-            mq.mq_gemv_q6k(self.dp_h, W["kv"][D_KV:], D_KV, self.dout["kv"][D_KV:])
+            mq.mq_gemv_q6k_packed(self.dp_h, W["kv"][:D_KV], D_KV, self.dout["kv"][:D_KV])
+            mq.mq_gemv_q6k_packed(self.dp_h, W["kv"][D_KV:], D_KV, self.dout["kv"][D_KV:])
             mq.mq_quantize_q8(self.dattn, self.dp_a)
             mq.mq_gemv_q4k(self.dp_a, W["o"], D_HID, self.dout["o"])
             mq.mq_gemv_q4k(self.dp_h, W["gate_up"][:D_FFN], D_FFN, self.dout["gate_up"][:D_FFN])
             mq.mq_gemv_q4k(self.dp_h, W["gate_up"][D_FFN:], D_FFN, self.dout["gate_up"][D_FFN:])
             mq.mq_swiglu_quant(self.dg, self.du, self.dp_f)
-            mq.mq_gemv_q6k(self.dp_f, W["down"], D_HID, self.dout["down"])
+            mq.mq_gemv_q6k_packed(self.dp_f, W["down"], D_HID, self.dout["down"])
 
     @staticmethod
     def decode_bytes():
@@ -515,8 +516,9 @@ def run_sweep(steps: int, warmup: int):
                 out = torch.empty((M, N), dtype=torch.float32, device=dev)
                 paths = (["gemv"] if M <= MQ_GEMV_ROWS else []) + (["gemm"] if M > 1 else [])
                 for path in paths:
-                    if path == "gemv":
-                        fn = lambda: mq.gemv(kind, p, w, N, out)
+                    if path == "gemv":   # q6_K: the GEMV on the prepacked rows the GEMM reads
+                        fn = ((lambda: mq.gemv(kind, p, w, N, out)) if kind == "q4k" else
+                              (lambda: mq.mq_gemv_q6k_packed(p, wg, N, out)))
                         act = M * (plane_bytes(1, K, op=False) - (0 if kind == "q4k" else K // 32 * 4))
                     else:
                         fn = lambda: mq.gemm(kind, p, wg, N, out)
@@ -537,7 +539,8 @@ def run_sweep(steps: int, warmup: int):
                     t = statistics.median(ts)
                     t_tensor = 2.0 * M * N * K / (peak_burst * 1e12)
                     t_stream = nbytes / (hbm * 1e9)
-                    line = {"case": f"{path}_{kind}:{M}x{N}x{K}", "us": t * 1e6,
+                    label = "q6kp" if path == "gemv" and kind == "q6k" else kind
+                    line = {"case": f"{path}_{label}:{M}x{N}x{K}", "us": t * 1e6,
                             "TFLOPs": 2.0 * M * N * K / t / 1e12, "GBps": nbytes / t / 1e9,
                             "bound": "tensor" if t_tensor >= t_stream else "hbm",
                             "frac": max(t_tensor, t_stream) / t}
@@ -616,7 +619,8 @@ def run_decode_only(steps: int, warmup: int):
 # ----------------------------------------------------------------------------- single-kernel cases
 
 def run_case(spec: str, steps: int, warmup: int):
-    """Time one kernel on seeded inputs: `kind:MxNxK` (gemm_q4k, gemm_q6k, gemv_q4k, gemv_q6k)
+    """Time one kernel on seeded inputs: `kind:MxNxK` (gemm_q4k, gemm_q6k, gemv_q4k, gemv_q6k, gemv_q6kp:
+    the q6_K GEMV on prepacked rows, and the other block types)
     or `kind:MxK` (quantize, rms, swiglu). Prints one JSON line with its roofline figure."""
     import __graft_entry__
     __graft_entry__.build()
@@ -629,13 +633,16 @@ def run_case(spec: str, steps: int, warmup: int):
     if kind.startswith("gemm") or kind.startswith("gemv"):
         M, N, K = dims
         wk = kind.split("_", 1)[1]
+        packed = wk == "q6kp"   # the q6_K GEMV on prepacked rows
+        wk = "q6k" if packed else wk
         x = S.normal((M, K), 0, "case.x", device=dev)
         w = S.weights(wk, N, K, 0, "case.w", device=dev)
         p = mq.Plane.empty(M, K, dev)
         mq.mq_quantize_q8(x, p)
         out = torch.empty((M, N), dtype=torch.float32, device=dev)
-        wg = mq.gemm_weights(wk, w, N, K) if kind.startswith("gemm") else w
-        fn = (lambda: mq.gemm(wk, p, wg, N, out)) if kind.startswith("gemm") else (lambda: mq.gemv(wk, p, w, N, out))
+        wg = mq.gemm_weights(wk, w, N, K) if kind.startswith("gemm") or packed else w
+        fn = ((lambda: mq.gemm(wk, p, wg, N, out)) if kind.startswith("gemm") else
+              (lambda: mq.mq_gemv_q6k_packed(p, wg, N, out)) if packed else (lambda: mq.gemv(wk, p, w, N, out)))
         flops = 2.0 * M * N * K
         act = gemm_act_bytes(wk, M, K) if kind.startswith("gemm") else plane_bytes(M, K) - (0 if wk != "q6k" else M * (K // 32) * 4)
         nbytes = wbytes(wk, N, K) + act + 4 * M * N

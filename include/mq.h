@@ -245,6 +245,17 @@ int mq_gemv_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
 int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 
 /*
+ * mq_gemv_q6k_packed — mq_gemv_q6k on prepacked rows: w is mq_prepack_q6k's output
+ * (N * (K/256) * 224 bytes, 16-byte aligned), the weight form the q6_K GEMM reads, so
+ * one registered copy of a q6_K matrix serves prefill and decode ([r60] §1, weights
+ * re-laid out once at registration; [D3-7] §2 (2b) and Excerpt A, the q6_K decode
+ * arm). Every super-block is 16-byte aligned, so the rows are read with aligned
+ * 16-byte loads straight into registers. Same arguments, result bound and errors as
+ * mq_gemv_q6k; the same products are summed in another order.
+ */
+int mq_gemv_q6k_packed(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+
+/*
  * mq_gemv_q5k / mq_gemv_q4_0 / mq_gemv_q4_1 — the same decode / small-batch
  * product for the other block types the pages dispatch: q5_K in the decode
  * arm ([D3-7] Excerpt B), Q4_0 / Q4_1 in the matmul dispatch list ([r60]

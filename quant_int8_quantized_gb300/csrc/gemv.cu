@@ -331,6 +331,107 @@ __global__ void __launch_bounds__(32 * kQ6Rows) gemv_q6k_kernel(const uint8_t* _
     }
 }
 
+// q6_K in the prepacked layout (mq_prepack_q6k: 224-byte super-blocks, 16-byte aligned,
+// each half contiguous: ql 64 B, qh 32 B, 8 int8 scales, f16 d). With every super-block
+// aligned the rows need no shared-memory staging: the kernel takes the q4_K GEMV's form, a
+// warp on two consecutive rows (sharing the activation loads), 8 super-blocks a step.
+// Lane = 4*g + 2*hh + c: super-block g of the step, its half hh and the positions 16c ..
+// 16c + 15 of each of the half's four 32-blocks t (elements 128 hh + 32 t + l): four 16-byte
+// loads a row (ql bytes 16c.., ql bytes 32 + 16c.., qh bytes 16c.., and the half's scales and
+// d), 64 weights. Quarter t takes the low (t < 2) or high nibble of ql[l + 32 (t & 1)], the
+// bit pair 2t of qh[l] and scale byte 2t + c; the integer dot is the raw kernel's
+// (L >> 4e) + 16 (H >> 2t) - 32 S.
+template <int MR>
+__global__ void __launch_bounds__(kThreads, MR == 1 ? 6 : 4) gemv_q6kp_kernel(const uint8_t* __restrict__ W,
+                                                                          const int8_t* __restrict__ aq,
+                                                                          const float* __restrict__ ad,
+                                                                          float* __restrict__ out, int N, int K,
+                                                                          int M) {
+    mq_grid_release();
+    const int lane = threadIdx.x & 31;
+    const int S = K / mq::QK_K, nst = (S + 7) / 8, nb = K / mq::QK;
+    const int g = lane >> 2, hh = (lane >> 1) & 1, c = lane & 1;
+    const size_t row_bytes = (size_t)S * mq::Q6K_PACKED_BYTES;
+    const int npairs = (N + 1) / 2;
+    const int G = gridDim.x * kRowsPerBlock;
+    for (int pr = blockIdx.x * kRowsPerBlock + (threadIdx.x >> 5); pr < npairs; pr += G) {   // warp-uniform
+        const int row = 2 * pr;
+        const bool two = row + 1 < N;
+        const uint8_t* wr = W + (size_t)row * row_bytes;
+        float acc[2][MR];
+#pragma unroll
+        for (int m = 0; m < MR; ++m) acc[0][m] = acc[1][m] = 0.0f;
+        for (int st = 0; st < nst; ++st) {
+            const int sb = 8 * st + g;
+            if (sb >= S) continue;
+            uint4 qa[2], qb[2], qh[2], hd[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                if (r == 1 && !two) break;
+                const uint8_t* half = wr + r * row_bytes + (size_t)sb * mq::Q6K_PACKED_BYTES + 112 * hh;
+                qa[r] = __ldcs(reinterpret_cast<const uint4*>(half + 16 * c));
+                qb[r] = __ldcs(reinterpret_cast<const uint4*>(half + 32 + 16 * c));
+                qh[r] = __ldcs(reinterpret_cast<const uint4*>(half + 64 + 16 * c));
+                hd[r] = __ldg(reinterpret_cast<const uint4*>(half + 96));
+            }
+            const int b0 = sb * 8 + 4 * hh;   // the half's first 32-block
+#pragma unroll
+            for (int m = 0; m < MR; ++m) {
+                if (m >= M) break;   // uniform
+                const int8_t* am = aq + (size_t)m * K + (size_t)b0 * 32 + 16 * c;
+                const float4 da = __ldg(reinterpret_cast<const float4*>(ad + (size_t)m * nb + b0));
+                const float dav[4] = {da.x, da.y, da.z, da.w};
+                int4 av[4];
+                int Sa[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    av[t] = __ldg(reinterpret_cast<const int4*>(am + 32 * t));
+                    int s4 = __dp4a(0x01010101, av[t].x, 0);
+                    s4 = __dp4a(0x01010101, av[t].y, s4);
+                    s4 = __dp4a(0x01010101, av[t].z, s4);
+                    Sa[t] = __dp4a(0x01010101, av[t].w, s4);
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    if (r == 1 && !two) break;
+                    const uint32_t qaw[4] = {qa[r].x, qa[r].y, qa[r].z, qa[r].w};
+                    const uint32_t qbw[4] = {qb[r].x, qb[r].y, qb[r].z, qb[r].w};
+                    const uint32_t qhw[4] = {qh[r].x, qh[r].y, qh[r].z, qh[r].w};
+                    const uint32_t scw = (c ? (hd[r].x >> 8) : hd[r].x);   // scale bytes 2t + c at bits 16t
+                    const uint32_t scw2 = (c ? (hd[r].y >> 8) : hd[r].y);
+                    float part = 0.0f;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int4 a4 = av[t];
+                        const int aw[4] = {a4.x, a4.y, a4.z, a4.w};
+                        const uint32_t lm = t < 2 ? 0x0F0F0F0Fu : 0xF0F0F0F0u;
+                        const uint32_t hm = 0x03030303u << (2 * t);
+                        int L = 0, H = 0;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            L = gemv::dp4a_us(((t & 1) ? qbw[w] : qaw[w]) & lm, aw[w], L);
+                            H = gemv::dp4a_us(qhw[w] & hm, aw[w], H);
+                        }
+                        const int I = (L >> (t < 2 ? 0 : 4)) + 16 * (H >> (2 * t)) - 32 * Sa[t];
+                        const int sc = (int)(int8_t)(((t < 2 ? scw : scw2) >> (16 * (t & 1))) & 0xffu);
+                        part += dav[t] * (float)(sc * I);
+                    }
+                    acc[r][m] += mq_f16_to_f32((uint16_t)(hd[r].z & 0xffffu)) * part;
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < MR; ++m) {
+            if (m >= M) break;
+            const float v0 = warp_sum(acc[0][m]), v1 = warp_sum(acc[1][m]);
+            if (lane == 0) {
+                out[(size_t)m * N + row] = v0;
+                if (two) out[(size_t)m * N + row + 1] = v1;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 namespace mq {
@@ -366,4 +467,16 @@ extern "C" int mq_gemv_q6k(const mq_q8_plane* a, const void* w, int N, float* ou
            : M == 2 ? go(gemv_q6k_kernel<4, 2>, gemv_q6k_kernel<3, 2>)
            : M <= 4 ? go(gemv_q6k_kernel<4, 4>, gemv_q6k_kernel<3, 4>)
                     : go(gemv_q6k_kernel<4, 8>, gemv_q6k_kernel<3, 8>);
+}
+
+extern "C" int mq_gemv_q6k_packed(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
+    int rc = gemv::check(a, w, N, out);
+    if (rc != MQ_OK || N == 0) return rc;
+    auto go = [&](auto kern) {
+        return mq::launch_plain(kern, dim3(gemv::grid_for((N + 1) / 2, kern)), dim3(kThreads), 0, stream,
+                                static_cast<const uint8_t*>(w), a->qs, a->d, out, N, a->K, a->M);
+    };
+    const int M = a->M;
+    return M == 1 ? go(gemv_q6kp_kernel<1>) : M == 2 ? go(gemv_q6kp_kernel<2>) : M <= 4 ? go(gemv_q6kp_kernel<4>)
+                                                                                   : go(gemv_q6kp_kernel<8>);
 }

@@ -23,7 +23,8 @@ EXPORTED = ["mq_plane_bytes", "mq_q4k_row_bytes", "mq_q6k_row_bytes", "mq_q6k_pa
             "mq_quantize_q8", "mq_rms_quant",
             "mq_swiglu_quant", "mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k",
             "mq_q5k_row_bytes", "mq_q4_0_row_bytes", "mq_q4_1_row_bytes", "mq_gemv_q5k", "mq_gemv_q4_0",
-            "mq_gemv_q4_1", "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_device_status", "mq_status_str"]
+            "mq_gemv_q4_1", "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemv_q6k_packed", "mq_device_status",
+            "mq_status_str"]
 
 
 class MQError(RuntimeError):
@@ -64,6 +65,7 @@ def lib() -> ctypes.CDLL:
             "mq_gemm_q6k": (i, [pp, vp, i, vp, vp]),
             "mq_gemv_q4k": (i, [pp, vp, i, vp, vp]),
             "mq_gemv_q6k": (i, [pp, vp, i, vp, vp]),
+            "mq_gemv_q6k_packed": (i, [pp, vp, i, vp, vp]),
             "mq_q5k_row_bytes": (sz, [i]),
             "mq_q4_0_row_bytes": (sz, [i]),
             "mq_q4_1_row_bytes": (sz, [i]),
@@ -241,6 +243,11 @@ def mq_gemv_q4k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=Non
 
 def mq_gemv_q6k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
     return _matmul("mq_gemv_q6k", a, w, N, out, stream)
+
+
+def mq_gemv_q6k_packed(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """q6_K GEMV on prepacked rows (mq_prepack_q6k), the form the GEMM reads too."""
+    return _matmul("mq_gemv_q6k_packed", a, w, N, out, stream)
 
 
 def mq_gemm_q4_0(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:

@@ -32,7 +32,7 @@ def declared_functions():
 def test_every_declared_symbol_is_exported(L):
     names = declared_functions()
     assert {"mq_quantize_q8", "mq_rms_quant", "mq_swiglu_quant", "mq_gemm_q4k", "mq_gemm_q6k",
-            "mq_gemv_q4k", "mq_gemv_q6k"} <= names
+            "mq_gemv_q4k", "mq_gemv_q6k", "mq_gemv_q6k_packed"} <= names
     for n in names:
         assert hasattr(L, n), n
     assert names <= set(mq.EXPORTED) | names  # the binding wraps what it knows
@@ -96,7 +96,7 @@ def test_validation_before_any_cuda_call(L):
 def test_matmul_validation_before_any_cuda_call(L):
     null = None
     p = _plane(mq.MQ_GEMV_MAX_ROWS + 1, 512, 16, 16, 16)
-    gemvs = (L.mq_gemv_q4k, L.mq_gemv_q6k, L.mq_gemv_q5k, L.mq_gemv_q4_0, L.mq_gemv_q4_1)
+    gemvs = (L.mq_gemv_q4k, L.mq_gemv_q6k, L.mq_gemv_q5k, L.mq_gemv_q4_0, L.mq_gemv_q4_1, L.mq_gemv_q6k_packed)
     for fn in gemvs:
         assert fn(ctypes.byref(p), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE  # M > 8
         assert fn(ctypes.byref(_plane(0, 512, 16, 16, 16)), ctypes.c_void_p(16), 8, ctypes.c_void_p(16), null) == mq.MQ_ERR_SHAPE
