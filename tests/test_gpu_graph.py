@@ -104,10 +104,12 @@ def test_prefill_gemm_graph_replay_matches_eager():
     assert mq.mq_device_status() == mq.MQ_OK
 
 
-def test_decode_layer_two_streams_matches_one_stream():
+@pytest.mark.parametrize("packed", [False, True])
+def test_decode_layer_two_streams_matches_one_stream(packed):
     """The decode step's schedule: the k|v GEMV on a second stream beside attn_q, joined before
     the next producer, captured into a graph. Replays equal one-stream eager execution bit for
-    bit, over two layers that reuse the planes."""
+    bit, over two layers that reuse the planes; the q6_K k|v GEMV on raw or prepacked rows (the
+    bench's decode uses the prepacked form)."""
     dev = torch.device("cuda")
     H, F, KV = 1024, 2048, 256
     x = synth.normal((1, H), 7, "s.x", device=dev)
@@ -115,6 +117,9 @@ def test_decode_layer_two_streams_matches_one_stream():
     w_rms = [synth.normal((H,), 7, f"s.rms{l}", 1.0, 0.1, device=dev) for l in range(2)]
     Wq = [synth.weights("q4k", H, H, 7, f"s.wq{l}", device=dev) for l in range(2)]
     Wkv = [synth.weights("q6k", 2 * KV, H, 7, f"s.wkv{l}", device=dev) for l in range(2)]
+    if packed:
+        Wkv = [mq.mq_prepack_q6k(w, 2 * KV, H) for w in Wkv]
+    gemv6 = mq.mq_gemv_q6k_packed if packed else mq.mq_gemv_q6k
     Wo = [synth.weights("q4k", H, H, 7, f"s.wo{l}", device=dev) for l in range(2)]
     ph, pa = mq.Plane.empty(1, H, dev, op=False), mq.Plane.empty(1, H, dev, op=False)
     oq = [torch.empty((H,), device=dev) for _ in range(2)]
@@ -129,7 +134,7 @@ def test_decode_layer_two_streams_matches_one_stream():
             mq.mq_rms_quant(x, w_rms[l], 1e-6, ph)
             ev_h.record(main)
             side.wait_event(ev_h)
-            mq.mq_gemv_q6k(ph, Wkv[l], 2 * KV, okv[l], stream=side)
+            gemv6(ph, Wkv[l], 2 * KV, okv[l], stream=side)
             ev_kv.record(side)
             mq.mq_gemv_q4k(ph, Wq[l], H, oq[l])
             main.wait_event(ev_kv)
@@ -140,7 +145,7 @@ def test_decode_layer_two_streams_matches_one_stream():
         for l in range(2):
             mq.mq_rms_quant(x, w_rms[l], 1e-6, ph)
             mq.mq_gemv_q4k(ph, Wq[l], H, oq[l])
-            mq.mq_gemv_q6k(ph, Wkv[l], 2 * KV, okv[l])
+            gemv6(ph, Wkv[l], 2 * KV, okv[l])
             mq.mq_quantize_q8(attn, pa)
             mq.mq_gemv_q4k(pa, Wo[l], H, oo[l])
 
