@@ -1,4 +1,4 @@
-// Decode (M == 1) matrix-vector products of a q8 plane by q4_K / q6_K weights.
+// Decode (M == 1) and small-batch matrix-vector products of a q8 plane by q4_K / q6_K weights.
 //
 // "72 · D3-7 — attn_v-q6K MMVQ routing (2b) + rms wide-block", §2 (2b) and
 // Excerpt A2: the decode matmul streams each weight row once and takes integer
@@ -14,7 +14,9 @@
 // occupancy than they gain.) Lane roles are fixed, so the byte positions of a
 // lane's scales are known once.
 //
-// q6_K: one warp per row; a lane task is 32 weights (16 positions of two
+// q6_K, prepacked rows (mq_prepack_q6k): the q4_K form (see gemv_q6kp_kernel below).
+//
+// q6_K, raw rows: one warp per row; a lane task is 32 weights (16 positions of two
 // quarters), 8 lanes per super-block, 4 super-blocks per step. The row is staged
 // through shared memory by cp.async copies of its 16-byte-aligned window, two
 // 8-super-block chunks in flight (three for rows of at most three chunks), so
@@ -32,7 +34,7 @@
 // scheduled as soon as it starts, which the producers use.
 //
 // HBM roofline: the weight stream, 0.5625 B/weight (q4_K) or 0.8203 B/weight
-// (q6_K), plus 4 B per output.
+// (q6_K; the prepacked rows read 0.875), plus 4 B per output.
 
 #include "mq_internal.cuh"
 #include "gemv_common.cuh"
