@@ -124,6 +124,35 @@ __device__ __forceinline__ float mq_f16_to_f32(uint16_t h) {
     return f;
 }
 
+// Packed pairs of f32 operations (the f32x2 instructions of sm_100 and later: one issue slot
+// for two results). Each half is the correctly rounded result of the scalar operation, so
+// packing changes no bit of any result; the compiler does not pair these by itself.
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{ .reg .b64 ra, rb, rc, rd;\n\t mov.b64 ra, {%2, %3};\n\t mov.b64 rb, {%4, %5};\n\t mov.b64 rc, {%6, %7};\n\t"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n\t mov.b64 {%0, %1}, rd; }"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+    float2 d;
+    asm("{ .reg .b64 ra, rb, rd;\n\t mov.b64 ra, {%2, %3};\n\t mov.b64 rb, {%4, %5};\n\t"
+        " mul.rn.f32x2 rd, ra, rb;\n\t mov.b64 {%0, %1}, rd; }"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+    float2 d;
+    asm("{ .reg .b64 ra, rb, rd;\n\t mov.b64 ra, {%2, %3};\n\t mov.b64 rb, {%4, %5};\n\t"
+        " add.rn.f32x2 rd, ra, rb;\n\t mov.b64 {%0, %1}, rd; }"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 f2_dup(float v) { return make_float2(v, v); }
+
 // rint(v / d) with v / d the correctly rounded f32 quotient, computed as
 // rint(v * inv) with inv an approximate 1/d (rcp.approx: at most 1 ulp off)
 // unless that product lies within 6.2e-5 of a rounding boundary (n + 1/2), where
@@ -160,10 +189,13 @@ __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v
     // Common case, one warp-uniform test for all four values of every lane: each product lies
     // outside the band around n + 1/2 (or the block is all zero), so rint of the product is
     // rint of the quotient (see mq_rint_div). Otherwise the lanes take the per-value path.
-    const float t0 = v0 * inv, t1 = v1 * inv, t2 = v2 * inv, t3 = v3 * inv;
-    const float r0 = rintf(t0), r1 = rintf(t1), r2 = rintf(t2), r3 = rintf(t3);
+    const float2 t01 = f2_mul(make_float2(v0, v1), f2_dup(inv)), t23 = f2_mul(make_float2(v2, v3), f2_dup(inv));
+    const float r0 = rintf(t01.x), r1 = rintf(t01.y), r2 = rintf(t23.x), r3 = rintf(t23.y);
+    // t - r, exact (r is the integer nearest t)
+    const float2 e01 = f2_fma(make_float2(r0, r1), f2_dup(-1.0f), t01);
+    const float2 e23 = f2_fma(make_float2(r2, r3), f2_dup(-1.0f), t23);
     constexpr float kIn = 0.5f - 6.2e-5f;
-    const bool clear = fabsf(t0 - r0) < kIn && fabsf(t1 - r1) < kIn && fabsf(t2 - r2) < kIn && fabsf(t3 - r3) < kIn;
+    const bool clear = fabsf(e01.x) < kIn && fabsf(e01.y) < kIn && fabsf(e23.x) < kIn && fabsf(e23.y) < kIn;
     if (kUniform && __all_sync(0xffffffffu, d == 0.0f || (isfinite(inv) && clear))) {
         if (d != 0.0f) {
             q0 = max(-127, min(127, (int)r0));

@@ -90,16 +90,16 @@ __device__ __forceinline__ void quant_pair(const Out& o, long long pair, int lan
         float sig[2];
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            unsigned short h[4];
-            float part = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const __half hv = __float2half_rn(__fmul_rn(__fmul_rn(dd[r], (float)q[r][i]), scale));
-                h[i] = __half_as_ushort(hv);
-                part = __fadd_rn(part, __half2float(hv));
-            }
-            o.ah[(r0 + r) * 32 + lane] = make_uint2((uint32_t)h[0] | ((uint32_t)h[1] << 16),
-                                                    (uint32_t)h[2] | ((uint32_t)h[3] << 16));
+            // f16(f32(d q) 2^e), two values per packed multiply; the block sum of these binary16
+            // values is exact in f32 in any order (see above), so it is taken pairwise
+            const float2 p01 = f2_mul(f2_mul(f2_dup(dd[r]), make_float2((float)q[r][0], (float)q[r][1])), f2_dup(scale));
+            const float2 p23 = f2_mul(f2_mul(f2_dup(dd[r]), make_float2((float)q[r][2], (float)q[r][3])), f2_dup(scale));
+            const __half2 h01 = __floats2half2_rn(p01.x, p01.y), h23 = __floats2half2_rn(p23.x, p23.y);
+            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+            const float2 pr = f2_add(f01, f23);
+            float part = __fadd_rn(pr.x, pr.y);
+            o.ah[(r0 + r) * 32 + lane] = make_uint2(*reinterpret_cast<const uint32_t*>(&h01),
+                                                    *reinterpret_cast<const uint32_t*>(&h23));
             part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 4));
             part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 2));
             part = __fadd_rn(part, __shfl_xor_sync(0xffffffffu, part, 1));
@@ -166,30 +166,38 @@ __global__ void __launch_bounds__(kThreads, 4) quantize_q8_kernel(const float4* 
 // 2^n and p * 2^n are normal and the scaling is exact. Below -86, e^x < 2^-124
 // vanishes next to 1 in 1 + e^x: 0 is returned; above 88, +inf. Within 0.91 ulp
 // of e^x on [-86, 88].
-__device__ __forceinline__ float exp_cw(float x) {
-    if (x < -86.0f) return 0.0f;
-    if (x > 88.0f) return __int_as_float(0x7f800000);
-    const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
-    const float r = __fmaf_rn(-n, 0x1.7f7d1cp-20f, __fmaf_rn(-n, 0x1.62e4p-1f, x));
-    float p = 0x1.a01a02p-13f;              // 1/7!
-    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);   // 1/6!
-    p = __fmaf_rn(p, r, 0x1.111112p-7f);    // 1/5!
-    p = __fmaf_rn(p, r, 0x1.555556p-5f);    // 1/4!
-    p = __fmaf_rn(p, r, 0x1.555556p-3f);    // 1/3!
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+__device__ __forceinline__ float2 exp_cw2(float2 x) {   // two values, packed arithmetic
+    const float2 t = f2_mul(x, f2_dup(0x1.715476p+0f));
+    const float2 n = make_float2(rintf(t.x), rintf(t.y));
+    const float2 r = f2_fma(n, f2_dup(-0x1.7f7d1cp-20f), f2_fma(n, f2_dup(-0x1.62e4p-1f), x));
+    float2 p = f2_dup(0x1.a01a02p-13f);                 // 1/7!
+    p = f2_fma(p, r, f2_dup(0x1.6c16c2p-10f));          // 1/6!
+    p = f2_fma(p, r, f2_dup(0x1.111112p-7f));           // 1/5!
+    p = f2_fma(p, r, f2_dup(0x1.555556p-5f));           // 1/4!
+    p = f2_fma(p, r, f2_dup(0x1.555556p-3f));           // 1/3!
+    p = f2_fma(p, r, f2_dup(0.5f));
+    p = f2_fma(p, r, f2_dup(1.0f));
+    p = f2_fma(p, r, f2_dup(1.0f));
+    // 2^n is formed for every x; outside [-86, 88] the result is replaced below
+    float2 e = f2_mul(p, make_float2(__int_as_float(((int)n.x + 127) << 23), __int_as_float(((int)n.y + 127) << 23)));
+    if (x.x < -86.0f) e.x = 0.0f;
+    if (x.x > 88.0f) e.x = __int_as_float(0x7f800000);
+    if (x.y < -86.0f) e.y = 0.0f;
+    if (x.y > 88.0f) e.y = __int_as_float(0x7f800000);
+    return e;
 }
 
 // (g / (1 + e^-g)) * u as the pages write it: an IEEE division and correctly
 // rounded f32 operations, with the exp above, so the plane is bit-exact.
-__device__ __forceinline__ float silu_mul(float g, float u) {
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, exp_cw(-g))), u);
+__device__ __forceinline__ float2 silu_mul2(float2 g, float2 u) {
+    const float2 den = f2_add(f2_dup(1.0f), exp_cw2(make_float2(-g.x, -g.y)));
+    return f2_mul(make_float2(__fdiv_rn(g.x, den.x), __fdiv_rn(g.y, den.y)), u);
 }
 
 __device__ __forceinline__ float4 silu_mul4(float4 g, float4 u) {
-    return make_float4(silu_mul(g.x, u.x), silu_mul(g.y, u.y), silu_mul(g.z, u.z), silu_mul(g.w, u.w));
+    const float2 a = silu_mul2(make_float2(g.x, g.y), make_float2(u.x, u.y));
+    const float2 b = silu_mul2(make_float2(g.z, g.w), make_float2(u.z, u.w));
+    return make_float4(a.x, a.y, b.x, b.y);
 }
 
 template <int R>
@@ -230,9 +238,9 @@ __global__ void __launch_bounds__(kThreads, 4) swiglu_quant_kernel(const float4*
 // rounded), then an xor butterfly 16, 8, 4, 2, 1; scale = 1 / sqrt(ss/K + eps)
 // ("55 · r52", §3.2 phase 1; "72 · D3-7", §2c(i) and Excerpt C).
 __device__ __forceinline__ float sum_sq4(float4 v) {
-    float t = __fadd_rn(__fmul_rn(v.x, v.x), __fmul_rn(v.y, v.y));
-    t = __fadd_rn(t, __fmul_rn(v.z, v.z));
-    return __fadd_rn(t, __fmul_rn(v.w, v.w));
+    const float2 a = f2_mul(make_float2(v.x, v.y), make_float2(v.x, v.y));
+    const float2 b = f2_mul(make_float2(v.z, v.w), make_float2(v.z, v.w));
+    return __fadd_rn(__fadd_rn(__fadd_rn(a.x, a.y), b.x), b.y);
 }
 
 __device__ __forceinline__ float rms_scale_finish(float ss, int K, float eps) {
@@ -249,9 +257,10 @@ __device__ __forceinline__ float rms_scale_warp(const float4* __restrict__ xr, i
     return rms_scale_finish(ss, K, eps);
 }
 
-__device__ __forceinline__ float4 rms_apply(float4 xv, float4 wv, float scale) {
-    return make_float4(__fmul_rn(__fmul_rn(xv.x, scale), wv.x), __fmul_rn(__fmul_rn(xv.y, scale), wv.y),
-                       __fmul_rn(__fmul_rn(xv.z, scale), wv.z), __fmul_rn(__fmul_rn(xv.w, scale), wv.w));
+__device__ __forceinline__ float4 rms_apply(float4 xv, float4 wv, float scale) {   // (x scale) w
+    const float2 a = f2_mul(f2_mul(make_float2(xv.x, xv.y), f2_dup(scale)), make_float2(wv.x, wv.y));
+    const float2 b = f2_mul(f2_mul(make_float2(xv.z, xv.w), f2_dup(scale)), make_float2(wv.z, wv.w));
+    return make_float4(a.x, a.y, b.x, b.y);
 }
 
 // Rows of at most 64 * kRegPairsMax rounds (K <= 16384): one block per row; pair p
