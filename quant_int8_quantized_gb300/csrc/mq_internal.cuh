@@ -172,10 +172,7 @@ __device__ __forceinline__ int mq_rint_div(float v, float d, float inv) {
 // shuffles at offsets 4, 2, 1 (max and integer sums are exact in any order).
 // q = rint(v / d) with the correctly rounded quotient (see mq_rint_div).
 // Returns the packed int8 quants; d and s are valid in every lane of the group.
-// kUniform: the band test is one warp vote for the warp's 128 values (the whole warp must call
-// it together); the fused SwiGLU producer, whose long per-value arithmetic comes before,
-// runs faster with the per-value test (kUniform = false).
-template <bool kUniform = true>
+// The band test is one warp vote for the warp's 128 values: the whole warp must call it together.
 __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v2, float v3,
                                                      float& d_out, int& s_out, int (&q)[4]) {
     float am = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
@@ -196,7 +193,7 @@ __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v
     const float2 e23 = f2_fma(make_float2(r2, r3), f2_dup(-1.0f), t23);
     constexpr float kIn = 0.5f - 6.2e-5f;
     const bool clear = fabsf(e01.x) < kIn && fabsf(e01.y) < kIn && fabsf(e23.x) < kIn && fabsf(e23.y) < kIn;
-    if (kUniform && __all_sync(0xffffffffu, d == 0.0f || (isfinite(inv) && clear))) {
+    if (__all_sync(0xffffffffu, d == 0.0f || (isfinite(inv) && clear))) {
         if (d != 0.0f) {
             q0 = max(-127, min(127, (int)r0));
             q1 = max(-127, min(127, (int)r1));

@@ -49,24 +49,22 @@ __device__ __forceinline__ void store_q8(const Out& o, long long round, int lane
 }
 
 // Quantize one round (q8 arrays only).
-template <bool kUniform = true>
 __device__ __forceinline__ void quant_round(const Out& o, long long round, int lane, float v0, float v1, float v2,
                                             float v3) {
     float dd;
     int ss, q[4];
-    const uint32_t pq = mq_quant4_group8<kUniform>(v0, v1, v2, v3, dd, ss, q);
+    const uint32_t pq = mq_quant4_group8(v0, v1, v2, v3, dd, ss, q);
     store_q8(o, round, lane, pq, dd, ss);
 }
 
 // Quantize the two rounds of super-block `pair` (rounds 2 pair, 2 pair + 1) and write
 // every array group the plane holds. v[r] is this lane's float4 of round r.
-template <bool kUniform = true>
 __device__ __forceinline__ void quant_pair(const Out& o, long long pair, int lane, const float4 (&v)[2]) {
     float dd[2];
     int ss[2], q[2][4];
     uint32_t pq[2];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) pq[r] = mq_quant4_group8<kUniform>(v[r].x, v[r].y, v[r].z, v[r].w, dd[r], ss[r], q[r]);
+    for (int r = 0; r < 2; ++r) pq[r] = mq_quant4_group8(v[r].x, v[r].y, v[r].z, v[r].w, dd[r], ss[r], q[r]);
     const long long r0 = 2 * pair;
     if (o.qs) {
         store_q8(o, r0, lane, pq[0], dd[0], ss[0]);
@@ -220,13 +218,13 @@ __global__ void __launch_bounds__(kThreads, 4) swiglu_quant_kernel(const float4*
         }
         if constexpr (R == 1) {
             const float4 v = silu_mul4(gv[0], uv[0]);
-            quant_round<false>(o, r0, lane, v.x, v.y, v.z, v.w);
+            quant_round(o, r0, lane, v.x, v.y, v.z, v.w);
         } else {
 #pragma unroll
             for (int k = 0; k < R; k += 2) {
                 if (r0 + k < rounds) {
                     const float4 pv[2] = {silu_mul4(gv[k], uv[k]), silu_mul4(gv[k + 1], uv[k + 1])};
-                    quant_pair<false>(o, (r0 + k) >> 1, lane, pv);
+                    quant_pair(o, (r0 + k) >> 1, lane, pv);
                 }
             }
         }
