@@ -194,11 +194,13 @@ __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v
     constexpr float kIn = 0.5f - 6.2e-5f;
     const bool clear = fabsf(e01.x) < kIn && fabsf(e01.y) < kIn && fabsf(e23.x) < kIn && fabsf(e23.y) < kIn;
     if (__all_sync(0xffffffffu, d == 0.0f || (isfinite(inv) && clear))) {
+        // no clamp needed: |v| <= amax and d = amax / 127 rounded, so |t| stays within
+        // 127 (1 + 2^-21) and its nearest integer within [-127, 127]
         if (d != 0.0f) {
-            q0 = max(-127, min(127, (int)r0));
-            q1 = max(-127, min(127, (int)r1));
-            q2 = max(-127, min(127, (int)r2));
-            q3 = max(-127, min(127, (int)r3));
+            q0 = (int)r0;
+            q1 = (int)r1;
+            q2 = (int)r2;
+            q3 = (int)r3;
         }
     } else if (d != 0.0f) {
         if (isfinite(inv)) {
@@ -217,7 +219,9 @@ __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v
         q2 = max(-127, min(127, q2));
         q3 = max(-127, min(127, q3));
     }
-    int s = (q0 + q1) + (q2 + q3);
+    const uint32_t packed = (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) | ((uint32_t)(q2 & 0xff) << 16) |
+                            ((uint32_t)(q3 & 0xff) << 24);
+    int s = __dp4a((int)packed, 0x01010101, 0);   // q0 + q1 + q2 + q3 from the signed bytes
     s += __shfl_xor_sync(0xffffffffu, s, 4);
     s += __shfl_xor_sync(0xffffffffu, s, 2);
     s += __shfl_xor_sync(0xffffffffu, s, 1);
@@ -227,6 +231,5 @@ __device__ __forceinline__ uint32_t mq_quant4_group8(float v0, float v1, float v
     q[1] = q1;
     q[2] = q2;
     q[3] = q3;
-    return (uint32_t)(q0 & 0xff) | ((uint32_t)(q1 & 0xff) << 8) | ((uint32_t)(q2 & 0xff) << 16) |
-           ((uint32_t)(q3 & 0xff) << 24);
+    return packed;
 }

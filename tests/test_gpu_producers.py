@@ -146,6 +146,34 @@ def test_swiglu_quant_bit_exact(M, K):
     assert_plane_equal(gp.numpy(), O.swiglu_quant(g.numpy(), u.numpy()), f"swiglu {M}x{K}")
 
 
+def test_swiglu_quant_exp_range_edges():
+    """SwiGLU at the edges of its exp's range (e^x is 0 below -86 and +inf above 88, so
+    g / (1 + e^-g) is g or -0 there), one ulp either side of each edge, subnormal and huge
+    gates (whose products with u stay finite), signed zeros: bit-exact. Each 32-block mixes edge
+    values with ordinary ones."""
+    f32 = np.float32
+    edges = []
+    for e in (86.0, 87.0, 88.0):
+        for sgn in (1.0, -1.0):
+            v = f32(sgn * e)
+            edges += [np.nextafter(v, f32(-np.inf), dtype=f32), v, np.nextafter(v, f32(np.inf), dtype=f32)]
+    edges += [f32(0.0), f32(-0.0), f32(1e-40), f32(-1e-40), f32(1e30), f32(-1e30), f32(1e37), f32(-1e37),
+              f32(0.5), f32(-0.5), f32(20.0), f32(-20.0)]
+    edges = np.array(edges, dtype=f32)
+    K = 512
+    g = np.resize(edges, (2, K)).astype(f32)
+    g[1] = np.roll(g[1], 7)
+    rng = np.random.default_rng(5)
+    g[:, ::3] = rng.normal(0.0, 4.0, size=g[:, ::3].shape).astype(f32)
+    u = rng.normal(0.0, 1.0, size=(2, K)).astype(f32)
+    u[:, ::5] *= f32(1e-3)
+    gp = GuardedPlane(2, K)
+    mq.mq_swiglu_quant(torch.from_numpy(g).cuda(), torch.from_numpy(u).cuda(), gp.plane)
+    torch.cuda.synchronize()
+    gp.check()
+    assert_plane_equal(gp.numpy(), O.swiglu_quant(g, u), "swiglu exp-range edges")
+
+
 def test_producers_full_size_sampled_rows():
     """7B FFN shapes (M = 3314; hidden 3584, ffn 18944) with the oracle on 64 sampled rows."""
     M, K, KF = 3314, 3584, 18944
