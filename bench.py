@@ -61,8 +61,8 @@ BYTES_PER_SB = {"q4k": 144, "q6k": 210, "q5k": 176, "q4_0": 8 * 18, "q4_1": 8 * 
 # 3314 x 18944 x 3584, from one ncu capture (summary under profiles/). It describes the device code
 # with these SHA-256 digests (gemm.cu up to its host-side section, and tc.cuh) and is reported as
 # null once either changes.
-GEMM_Q4K_TRAFFIC = {"bytes": 66430976 + 205331712,
-                    "sha256": {"gemm.cu": "7e170ba28470bbe44be804c878cfcc221b2483d62166211e2b2c136f6fba9bfd",
+GEMM_Q4K_TRAFFIC = {"bytes": 66732544 + 205647360,
+                    "sha256": {"gemm.cu": "e60cebd19c2058302766b03e735d7b042a7ffe05dcbb0c4a31ef95f3b97f24e5",
                                "tc.cuh": "77627d374b6dc4619249b40701e93050c782a7d46494b273d5b7a343462067e1"}}
 HOST_SECTION = b"// ------------------------------------------------------------------ host side"
 
@@ -79,6 +79,25 @@ def gemm_q4k_traffic():
         if device_code_digest(fn) != digest:
             return None
     return GEMM_Q4K_TRAFFIC["bytes"]
+
+
+def gemm_launches(kind, M, N, K, sms):
+    """Kernel launches one GEMM call makes: two for a q6_K GEMM whose output tiles (192 tokens x
+    128 rows) leave the persistent grid's last round partly idle and whose split pays (the library
+    then runs those tiles as ordered K slices in a second launch), else one. Mirrors the library's
+    rule (order_slices in csrc/gemm.cu); the launch list under profiles/ shows the count."""
+    if kind != "q6k" or M <= 64:
+        return 1
+    bt = 192 if M >= 192 else (M + 15) // 16 * 16
+    tiles = -(-M // bt) * -(-N // 128)
+    S = K // 256
+    if tiles <= sms or tiles % sms == 0:
+        return 1
+    rest = tiles % sms
+    best_cost = S
+    for ts in range(2, min(sms // rest, 15) + 1):
+        best_cost = min(best_cost, -(-S // ts) + 2 * (ts - 1) + 2)
+    return 2 if best_cost < S else 1
 
 
 def wbytes(kind, N, K):
@@ -213,8 +232,11 @@ class Stack:
             self.ev_h = torch.cuda.Event()
             self.ev_kv = torch.cuda.Event()
 
-    # launches per prefill step: 28 * (2 rms + 1 quantize + 1 swiglu + 7 gemm) + rms + gemv
-    LAUNCHES_PER_STEP = LAYERS * 11 + 2
+    # launches per prefill step: 28 * (2 rms + 1 quantize + 1 swiglu + the GEMMs' launches) + rms + gemv
+    @staticmethod
+    def launches_per_step(sms):
+        gemms = sum(gemm_launches(kind, M_TOK, N, K, sms) for _, kind, N, K, _ in PREFILL_MATS)
+        return LAYERS * (4 + gemms) + 2
     LAUNCHES_PER_DECODE = D_LAYERS * 8   # rms, q, k|v, quantize, o, gate|up, swiglu, down
 
     def step(self, time_q4=False):
@@ -841,7 +863,7 @@ def main():
                          "achieved": achieved, "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
                          "peak_kind": f"{peak_kind} bf16 sustained (f16 runs at the bf16 rate)",
                          "launches": q4_launches, "traffic": gemm_q4k_traffic(), "traffic_unit": "bytes per launch"},
-            "gpu_launches": Stack.LAUNCHES_PER_STEP * args.steps,
+            "gpu_launches": Stack.launches_per_step(torch.cuda.get_device_properties(dev).multi_processor_count) * args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }

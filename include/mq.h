@@ -194,6 +194,12 @@ int mq_swiglu_quant(const float* g, const float* u, int M, int K,
  * (small M or N), the K axis is split across several thread blocks, `out` is
  * zeroed on `stream` and the partial sums are added with f32 atomics: the result
  * is then within the same bound, but its last bits may differ from run to run.
+ * mq_gemm_q6k with more tiles than SMs but not a whole number of rounds of them
+ * may make two launches: the tiles of the complete rounds whole, then (a
+ * programmatic dependent launch on `stream`) the rest cut along K into slices
+ * that add into `out` in a fixed order; the result is the same on every run (on
+ * a GPU with the same SM count). The hand-over uses flags in the library's own
+ * device memory and bounded waits (mq_device_status reports a wait given up).
  */
 int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);

@@ -63,6 +63,10 @@
 namespace {
 
 __device__ unsigned int g_gemm_error;   // bit 0: a bounded wait gave up
+// Flags of ordered split launches (see Order): a ring shared by the launches of a device,
+// each taking its own range; every flag is back at 0 when its launch ends.
+constexpr int kOrderRing = 1 << 16;
+__device__ unsigned int g_order_flags[kOrderRing];
 
 constexpr int BW = 128;                 // weight rows per tile (MMA M)
 constexpr int BT = 192;                 // tokens per tile (MMA N)
@@ -165,22 +169,60 @@ struct Smem {
     uint64_t b_full[C::kRB], b_empty[C::kRB];
     uint64_t a_full[C::kRF], a_empty[C::kRF][2];
     uint64_t t_full[2], t_empty[2], mma_done;
+    uint64_t ord_go;   // ordered split: the tile's previous slice is in the output
     uint32_t tmem;
     int abort;
 };
 
-// A work unit: one output tile (token tile fastest) and a slice [sb0, sb1) of its
-// super-blocks; units that share a tile add their partial sums into the output,
-// which the host zeroed beforehand.
+// A work unit: one output tile (token tile fastest) and a slice sp, [sb0, sb1), of its
+// super-blocks. A launch covers tiles tile0 .. tile0 + ntiles - 1, each as `splits` units;
+// r is the tile's index within the launch. Units that share a tile add their partial sums
+// into the output: in any order for split-K (the host zeroed the output beforehand), in slice
+// order for an ordered launch (see Order).
 struct Work {
-    int m0, n0, sb0, sb1;
+    int m0, n0, sb0, sb1, sp, r;
 };
 // nfast: weight-row tiles fastest (when the activation operand is the larger one, so
 // that each token tile's activations are read from memory once).
-__device__ __forceinline__ Work work_of(int u, int splits, int num_mt, int num_nt, bool nfast, int S, int bt) {
-    const int t = u / splits, sp = u - t * splits;
+__device__ __forceinline__ Work work_of(int u, int splits, int num_mt, int num_nt, bool nfast, int S, int bt,
+                                        int tile0) {
+    const int r = u / splits, sp = u - r * splits, t = tile0 + r;
     const int mt = nfast ? t / num_nt : t % num_mt, nt = nfast ? t % num_nt : t / num_mt;
-    return Work{mt * bt, nt * BW, (sp * S) / splits, ((sp + 1) * S) / splits};
+    return Work{mt * bt, nt * BW, (sp * S) / splits, ((sp + 1) * S) / splits, sp, r};
+}
+
+// Ordered split. A persistent grid of G CTAs takes the output tiles G at a time; when their
+// count T is not a multiple of G, the last round would leave SMs idle for a whole tile's
+// time. The host then launches the first T - T mod G tiles whole, and the last T mod G tiles
+// in a second launch, cut along K into `splits` slices each that run side by side (the second
+// launch may start as the first one's CTAs retire). Slice sp adds its partial sums into the
+// output only after slice sp - 1 has stored or added its own: one flag per tile, tagged with
+// the launch's epoch, which warp 3 of each CTA waits for and passes on (the epilogue warps
+// wait on shared-memory barriers only), so the order of the additions, and the result, do
+// not depend on timing. The last slice resets the flag to 0 for the next launch on the range.
+struct Order {
+    int on;           // 0: split-K units add in any order (or no split)
+    unsigned epoch;   // this launch's tag, in the high bits of each flag value
+    unsigned base;    // this launch's first flag in g_order_flags
+};
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait for an ordered-split flag to reach `want`.
+__device__ bool wait_flag(const unsigned* fl, unsigned want) {
+    const uint64_t t0 = tc::globaltimer();
+    for (unsigned spin = 0;; ++spin) {
+        if (ld_acquire_u32(fl) == want) return true;
+        if ((spin & 63u) == 63u && tc::globaltimer() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 // Non-suspending test of a phase (acquire semantics, like the waits).
@@ -294,21 +336,27 @@ __device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
     return (uint32_t)*reinterpret_cast<const uint16_t*>(p) | ((uint32_t)*reinterpret_cast<const uint16_t*>(p + 2) << 16);
 }
 
-template <int WT, bool SH>
+template <int WT, bool SH, bool ORD = false>
 __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmAct,
                                                            const __grid_constant__ CUtensorMap tmAx,
                                                            const __grid_constant__ CUtensorMap tmAf,
                                                            const __grid_constant__ CUtensorMap tmW,
                                                            float* __restrict__ out, int M, int N, int K, int splits,
-                                                           int nfast, int bt) {
+                                                           int nfast, int bt, int tile0, int ntiles, const Order ord) {
     using C = Cfg<WT, SH>;
     constexpr int kRB = C::kRB, kRF = C::kRF;
     extern __shared__ uint8_t smem_raw[];
     Smem<WT, SH>& sm = *reinterpret_cast<Smem<WT, SH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    mq_grid_release();   // a dependent launch (the second launch of an ordered split) may start
     const int S = K / mq::QK_K;
     const int num_mt = (M + bt - 1) / bt, num_nt = (N + BW - 1) / BW;
-    const int units = num_mt * num_nt * splits;
+    // the ordered split (Order) is compiled into its own instance, used only for the second
+    // launch of an ordered split: compiled into the instances every other launch uses, it made
+    // them up to 27 % slower
+    constexpr bool kOrd = ORD;
+    // q6_K launches may cover part of the tiles (the first launch of an ordered split)
+    const int units = WT == kQ6K ? ntiles * splits : num_mt * num_nt * splits;
 
     if (tid == 0) {
         tc::prefetch_tensormap(&tmW);
@@ -339,6 +387,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
             tc::mbar_init(&sm.t_empty[i], C::kEpiWarps);
         }
         tc::mbar_init(&sm.mma_done, 1);
+        tc::mbar_init(&sm.ord_go, 1);
         sm.abort = 0;
         tc::fence_mbar_init();
     }
@@ -358,7 +407,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
             uint32_t issA = 0, phA = 0, issX = 0, phX = 0, issB = 0, phB = 0;   // copies in flight (for an abort)
             int sbc = 0, ga = 0;
             for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt);
+                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
                 for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb, ++sbc) {
                     const int x = sbc % RX;
                     if (!wwait(sm, &sm.ax_empty[x], ((sbc / RX) & 1) ^ 1)) break;
@@ -413,7 +462,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
             const uint32_t idesc = tc::instr_desc(BW, (uint32_t)bt, 0);
             int total = 0;   // super-blocks this CTA accumulates (the issuer needs no tile positions)
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
-                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt);
+                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
                 total += wk.sb1 - wk.sb0;
             }
             // readiness of chunk j of super-block sbc, whose activation slot is ga
@@ -499,6 +548,25 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
                 tc::mbar_wait(&sm.mma_done, 0, kWaitLimitNs);
             }
             tc::tc_fence_before();
+        } else if (kOrd && warp == 3 && ord.on) {
+            // ---------------------------------------------------- ordered split: let the
+            // epilogue add once the tile's previous slice (another CTA) is in; the flag is passed
+            // on at the end of the kernel. An ordered launch gives each CTA at most one unit (the
+            // host keeps its units within the grid).
+            const int u = blockIdx.x;
+            if (u < units) {
+                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
+                if (wk.sp > 0) {
+                    const bool got =
+                        lane == 0 ? wait_flag(g_order_flags + ord.base + wk.r, (ord.epoch << 4) | (unsigned)wk.sp) : true;
+                    if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+                        if (lane == 0) tc::mbar_arrive(&sm.ord_go);
+                    } else {
+                        if (lane == 0) atomicOr(&g_gemm_error, 1u);
+                        *(volatile int*)&sm.abort = 1;
+                    }
+                }
+            }
         }
         __syncwarp();
     } else if (warp < 4 + C::kConvWarps) {
@@ -509,7 +577,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         int sbc = 0;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt);
+            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
             const int n = wk.n0 + r;
             for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb, ++sbc) {
                 const int b = sbc % kRB, x = sbc % RX;
@@ -751,7 +819,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         int sbc = 0;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt);
+            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
             float acc[C::kEpiCols];
 #pragma unroll
             for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0.0f;
@@ -794,6 +862,16 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
                 }
             }
             if (!ok) break;
+            // ordered split: slice sp > 0 adds once warp 3 has seen slice sp - 1 in (the same
+            // reduction as split-K, in a fixed order)
+            bool add;
+            if constexpr (kOrd) {
+                const int usp = u % splits;   // the unit's slice (recomputed: fewer live registers)
+                if (ord.on && usp > 0 && !wwait(sm, &sm.ord_go, 0)) break;   // (one unit per CTA)
+                add = splits > 1 && !(ord.on && usp == 0);
+            } else {
+                add = splits > 1;
+            }
             const int n = wk.n0 + r;
             if (n < N) {
                 const int t0 = wk.m0 + C::kEpiCols * ch;
@@ -801,7 +879,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
 #pragma unroll
                 for (int i = 0; i < C::kEpiCols; ++i) {
                     if (t0 + i < M) {
-                        if (splits > 1) atomicAdd(op + (size_t)i * N, acc[i]);
+                        if (add) atomicAdd(op + (size_t)i * N, acc[i]);
                         else op[(size_t)i * N] = acc[i];
                     }
                 }
@@ -814,6 +892,17 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
         tc::tc_fence_after();
         tc::tmem_dealloc(tbase, kTmemCols);
     }
+    if (kOrd && ord.on && warp == 3 && lane == 0 && blockIdx.x < units && !aborted(sm)) {
+        // every store and addition of this CTA came before the block barrier above; the release
+        // at GPU scope passes the tile to its next slice, or frees the flag after the last one
+        const int sp = blockIdx.x % splits, r0 = blockIdx.x / splits;
+        unsigned* fl = g_order_flags + ord.base + r0;
+        if (sp < splits - 1) st_release_u32(fl, (ord.epoch << 4) | (unsigned)(sp + 1));
+        else *fl = 0u;
+    }
+    // the second launch of an ordered split ends after the first one (a no-op otherwise), so
+    // that what follows on the stream sees both
+    mq_grid_wait();
 }
 
 // ------------------------------------------------------------------ host side
@@ -863,6 +952,45 @@ int choose_splits(long long tiles, int S, int sms) {
     return best;
 }
 
+// Slices per tile for the tiles of an incomplete last round (Order), or 1: at most as many
+// as fit the grid (and 15, the flag's slice field), chosen to minimise that round's length
+// in super-blocks: ceil(S / ts), plus kChainCost for each hand-over between slices (a flag and
+// the additions, ~2-3 us) and kLaunchCost for the second launch. No split if nothing is gained.
+constexpr int kChainCost = 2, kLaunchCost = 2;
+int order_slices(long long tiles, int S, int sms) {
+    if (tiles <= sms) return 1;   // fewer tiles than SMs: split-K instead
+    const long long rest = tiles % sms;
+    if (rest == 0) return 1;
+    const long long cap = sms / rest < 15 ? sms / rest : 15;
+    int best = 1, best_cost = S;
+    for (int ts = 2; ts <= cap; ++ts) {
+        const int cost = (S + ts - 1) / ts + kChainCost * (ts - 1) + kLaunchCost;
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = ts;
+        }
+    }
+    return best;
+}
+
+// The epoch and flag range of an ordered launch, per device. Launches take consecutive
+// ranges of the ring, so launches in flight together never share a flag.
+bool order_range(int need, unsigned* epoch, unsigned* base) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static unsigned ep[kMaxDevices], next[kMaxDevices];
+    int dev = 0;
+    if (need > kOrderRing || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(mu);
+    if (next[dev] + (unsigned)need > (unsigned)kOrderRing) next[dev] = 0;
+    *base = next[dev];
+    next[dev] += (unsigned)need;
+    ep[dev] = (ep[dev] + 1u) & 0x0fffffffu;   // 28 bits
+    if (ep[dev] == 0u) ep[dev] = 1u;
+    *epoch = ep[dev];
+    return true;
+}
+
 int check_gemm(const mq_q8_plane* a, const void* w, int N, const float* out) {
     if (!a) return MQ_ERR_NULL;
     if (N < 0 || a->M < 0 || !mq::valid_k(a->K)) return MQ_ERR_SHAPE;
@@ -876,7 +1004,7 @@ int check_gemm(const mq_q8_plane* a, const void* w, int N, const float* out) {
 // Once per device: the register split between warpgroups assumes the launch register
 // count, and the kernel's shared-memory size is set. Later calls make no attribute
 // calls, so a sequence of entry points can be captured in a graph.
-template <int WT, bool SH>
+template <int WT, bool SH, bool ORD = false>
 bool gemm_ready(size_t smem) {
     constexpr int kMaxDevices = 64;
     static int state[kMaxDevices];   // 0 unknown, 1 ready, 2 failed
@@ -889,8 +1017,9 @@ bool gemm_ready(size_t smem) {
         v = state[dev];
         if (v == 0) {
             cudaFuncAttributes fa;
-            v = (cudaFuncGetAttributes(&fa, gemm_kernel<WT, SH>) == cudaSuccess && fa.numRegs == Cfg<WT, SH>::kLaunchRegs &&
-                 cudaFuncSetAttribute(gemm_kernel<WT, SH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+            v = (cudaFuncGetAttributes(&fa, gemm_kernel<WT, SH, ORD>) == cudaSuccess &&
+                 fa.numRegs == Cfg<WT, SH>::kLaunchRegs &&
+                 cudaFuncSetAttribute(gemm_kernel<WT, SH, ORD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
                      cudaSuccess)
                     ? 1
                     : 2;
@@ -933,15 +1062,34 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
     const int splits = choose_splits(tiles, S, sms);
     if (splits > 1 && cudaMemsetAsync(out, 0, (size_t)M * N * sizeof(float), stream) != cudaSuccess)
         return MQ_ERR_LAUNCH;
-    const long long units = tiles * splits;
-    const int grid = (int)(units < sms ? units : sms);
     // weight-row tiles fastest when the activations outweigh the weights
     const int nfast = (double)M * K * 2 > (double)N * row ? 1 : 0;
-    if (sh)
-        gemm_kernel<WT, kS><<<grid, Cfg<WT, kS>::kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits, nfast, bt);
-    else
-        gemm_kernel<WT, false><<<grid, Cfg<WT, false>::kThreads, smem, stream>>>(tmAct, tmAx, tmAf, tmW, out, M, N, K, splits, nfast, bt);
-    return mq::launch_status();
+    // one launch of tiles [tile0, tile0 + ntiles), each as `sp` units
+    const Order none{0, 0u, 0u};
+    auto plain = [&](int tile0, int ntiles, int sp) -> int {
+        const long long units = (long long)ntiles * sp;
+        const int grid = (int)(units < sms ? units : sms);
+        if (sh)
+            return mq::launch_plain(gemm_kernel<WT, kS>, dim3(grid), dim3(Cfg<WT, kS>::kThreads), smem, stream, tmAct,
+                                    tmAx, tmAf, tmW, out, M, N, K, sp, nfast, bt, tile0, ntiles, none);
+        return mq::launch_plain(gemm_kernel<WT, false>, dim3(grid), dim3(Cfg<WT, false>::kThreads), smem, stream, tmAct,
+                                tmAx, tmAf, tmW, out, M, N, K, sp, nfast, bt, tile0, ntiles, none);
+    };
+    const int ts = WT == kQ6K && !sh && splits == 1 ? order_slices(tiles, S, sms) : 1;
+    if (ts == 1) return plain(0, (int)tiles, splits);
+    if constexpr (WT == kQ6K) {
+        // ordered split: whole tiles for the complete rounds, then the rest in ts slices each, in
+        // a dependent launch of the ordered instance (at most one unit per CTA: rest * ts <= sms)
+        if (!gemm_ready<WT, false, true>(smem)) return MQ_ERR_LAUNCH;
+        const int full = (int)(tiles - tiles % sms), rest = (int)(tiles - full);
+        Order ord{1, 0u, 0u};
+        if (!order_range(rest, &ord.epoch, &ord.base)) return MQ_ERR_LAUNCH;
+        rc = plain(0, full, 1);
+        if (rc != MQ_OK) return rc;
+        return mq::launch_pdl(gemm_kernel<WT, false, true>, dim3(rest * ts), dim3(Cfg<WT, false>::kThreads), smem, stream,
+                              tmAct, tmAx, tmAf, tmW, out, M, N, K, ts, nfast, bt, full, rest, ord);
+    }
+    return MQ_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -954,6 +1102,11 @@ int take_gemm_device_error(cudaStream_t stream, unsigned* code) {
     if (v) {
         const unsigned zero = 0;
         if (cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(zero)) != cudaSuccess) return MQ_ERR_LAUNCH;
+        // a launch that gave up may have left ordered-split flags set
+        void* flags = nullptr;
+        if (cudaGetSymbolAddress(&flags, g_order_flags) != cudaSuccess ||
+            cudaMemset(flags, 0, sizeof(unsigned) * kOrderRing) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+            return MQ_ERR_LAUNCH;
     }
     *code = v;
     return MQ_OK;
