@@ -49,7 +49,8 @@ enum {
     MQ_ERR_ALIGN = 3,   /* a pointer is not 16-byte aligned */
     MQ_ERR_ARCH = 4,    /* the current device is not a compute capability 10.3 (GB300) GPU */
     MQ_ERR_LAUNCH = 5,  /* the CUDA launch (or tensor-map encoding) failed */
-    MQ_ERR_DEVICE = 6   /* a kernel gave up on a bounded wait (reported by mq_device_status) */
+    MQ_ERR_DEVICE = 6,  /* a kernel gave up on a bounded wait (reported by mq_device_status) */
+    MQ_ERR_SCRATCH = 7  /* mq_gemm_q6k_static: the call needs more than its fixed scratch array holds */
 };
 
 /* Most activation rows one mq_gemv_q4k / mq_gemv_q6k call takes. */
@@ -203,6 +204,23 @@ int mq_swiglu_quant(const float* g, const float* u, int M, int K,
  */
 int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
+
+/*
+ * mq_gemm_q6k_static — mq_gemm_q6k for callers that cannot have device memory allocated on
+ * their behalf: a server that hands all device memory to its own pool at start-up, or code
+ * that must not call cudaMalloc because it can synchronize the device and stall other work.
+ * The pages have no counterpart; this is a property of this library's interface only.
+ * Same arguments, result, accuracy and errors as mq_gemm_q6k. Where mq_gemm_q6k's ordered
+ * split takes its flags from a ring shared by all its launches, this variant uses a fixed
+ * array of its own of 1024 flags (4 KB of device memory, held by every GPU that loads the
+ * library until the process exits; one flag per tile the split cuts). It clears the flags it
+ * uses on `stream` at every call. A call that would need more than 1024 of them returns
+ * MQ_ERR_SCRATCH before anything is enqueued. Calls share the array, so two calls that run
+ * on the GPU at the same time (on different streams) race and may give wrong results. The
+ * first call on a device looks the array's device address up (once per device); make that
+ * first call before any stream capture. It calls no cudaMalloc or cudaFree.
+ */
+int mq_gemm_q6k_static(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 
 /*
  * mq_gemm_q4_0 / mq_gemm_q4_1 — the same prefill matmul for the Q4_0 / Q4_1 types

@@ -90,6 +90,7 @@ extern "C" const char* mq_status_str(int status) {
         case MQ_ERR_ARCH: return "MQ_ERR_ARCH: the current device is not a compute capability 10.3 GPU";
         case MQ_ERR_LAUNCH: return "MQ_ERR_LAUNCH: the CUDA launch failed";
         case MQ_ERR_DEVICE: return "MQ_ERR_DEVICE: a kernel gave up on a bounded wait";
+        case MQ_ERR_SCRATCH: return "MQ_ERR_SCRATCH: the call needs more than the entry point's fixed scratch array holds";
         default: return "MQ_ERR_UNKNOWN";
     }
 }

@@ -204,6 +204,7 @@ struct Order {
     int on;           // 0: split-K units add in any order (or no split)
     unsigned epoch;   // this launch's tag, in the high bits of each flag value
     unsigned base;    // this launch's first flag in g_order_flags
+    unsigned* flags;  // the flags in place of g_order_flags (instances with SF set: mq_gemm_q6k_static)
 };
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
@@ -336,7 +337,7 @@ __device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
     return (uint32_t)*reinterpret_cast<const uint16_t*>(p) | ((uint32_t)*reinterpret_cast<const uint16_t*>(p + 2) << 16);
 }
 
-template <int WT, bool SH, bool ORD = false>
+template <int WT, bool SH, bool ORD = false, bool SF = false>
 __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmAct,
                                                            const __grid_constant__ CUtensorMap tmAx,
                                                            const __grid_constant__ CUtensorMap tmAf,
@@ -558,7 +559,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
                 const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
                 if (wk.sp > 0) {
                     const bool got =
-                        lane == 0 ? wait_flag(g_order_flags + ord.base + wk.r, (ord.epoch << 4) | (unsigned)wk.sp) : true;
+                        lane == 0 ? wait_flag((SF ? ord.flags : g_order_flags) + ord.base + wk.r, (ord.epoch << 4) | (unsigned)wk.sp) : true;
                     if (__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
                         if (lane == 0) tc::mbar_arrive(&sm.ord_go);
                     } else {
@@ -896,7 +897,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
         // every store and addition of this CTA came before the block barrier above; the release
         // at GPU scope passes the tile to its next slice, or frees the flag after the last one
         const int sp = blockIdx.x % splits, r0 = blockIdx.x / splits;
-        unsigned* fl = g_order_flags + ord.base + r0;
+        unsigned* fl = (SF ? ord.flags : g_order_flags) + ord.base + r0;
         if (sp < splits - 1) st_release_u32(fl, (ord.epoch << 4) | (unsigned)(sp + 1));
         else *fl = 0u;
     }
@@ -1004,7 +1005,7 @@ int check_gemm(const mq_q8_plane* a, const void* w, int N, const float* out) {
 // Once per device: the register split between warpgroups assumes the launch register
 // count, and the kernel's shared-memory size is set. Later calls make no attribute
 // calls, so a sequence of entry points can be captured in a graph.
-template <int WT, bool SH, bool ORD = false>
+template <int WT, bool SH, bool ORD = false, bool SF = false>
 bool gemm_ready(size_t smem) {
     constexpr int kMaxDevices = 64;
     static int state[kMaxDevices];   // 0 unknown, 1 ready, 2 failed
@@ -1017,9 +1018,9 @@ bool gemm_ready(size_t smem) {
         v = state[dev];
         if (v == 0) {
             cudaFuncAttributes fa;
-            v = (cudaFuncGetAttributes(&fa, gemm_kernel<WT, SH, ORD>) == cudaSuccess &&
+            v = (cudaFuncGetAttributes(&fa, gemm_kernel<WT, SH, ORD, SF>) == cudaSuccess &&
                  fa.numRegs == Cfg<WT, SH>::kLaunchRegs &&
-                 cudaFuncSetAttribute(gemm_kernel<WT, SH, ORD>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+                 cudaFuncSetAttribute(gemm_kernel<WT, SH, ORD, SF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
                      cudaSuccess)
                     ? 1
                     : 2;
@@ -1036,8 +1037,12 @@ bool gemm_ready(size_t smem) {
 // weight stream and its conversion rather than by work on empty columns.
 int token_tile(int M) { return M >= BT ? BT : ((M + 15) / 16) * 16; }
 
+// static_flags: mq_gemm_q6k_static's fixed flag array (device address), else nullptr
+constexpr int kStaticFlags = 1024;   // tiles an ordered split of mq_gemm_q6k_static may cut, at most
+
 template <int WT>
-int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
+int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream,
+                unsigned* static_flags = nullptr) {
     int rc = check_gemm(a, w, N, out);
     if (rc != MQ_OK || N == 0 || a->M == 0) return rc;
     const int M = a->M, K = a->K, S = K / mq::QK_K;
@@ -1080,8 +1085,20 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
     if constexpr (WT == kQ6K) {
         // ordered split: whole tiles for the complete rounds, then the rest in ts slices each, in
         // a dependent launch of the ordered instance (at most one unit per CTA: rest * ts <= sms)
-        if (!gemm_ready<WT, false, true>(smem)) return MQ_ERR_LAUNCH;
         const int full = (int)(tiles - tiles % sms), rest = (int)(tiles - full);
+        if (static_flags) {
+            // mq_gemm_q6k_static: its own flags, cleared on the stream, used from 0 with one epoch
+            if (rest > kStaticFlags) return MQ_ERR_SCRATCH;
+            if (!gemm_ready<WT, false, true, true>(smem)) return MQ_ERR_LAUNCH;
+            if (cudaMemsetAsync(static_flags, 0, (size_t)rest * sizeof(unsigned), stream) != cudaSuccess)
+                return MQ_ERR_LAUNCH;
+            rc = plain(0, full, 1);
+            if (rc != MQ_OK) return rc;
+            return mq::launch_pdl(gemm_kernel<WT, false, true, true>, dim3(rest * ts), dim3(Cfg<WT, false>::kThreads), smem,
+                                  stream, tmAct, tmAx, tmAf, tmW, out, M, N, K, ts, nfast, bt, full, rest,
+                                  Order{1, 1u, 0u, static_flags});
+        }
+        if (!gemm_ready<WT, false, true>(smem)) return MQ_ERR_LAUNCH;
         Order ord{1, 0u, 0u};
         if (!order_range(rest, &ord.epoch, &ord.base)) return MQ_ERR_LAUNCH;
         rc = plain(0, full, 1);
@@ -1126,6 +1143,37 @@ extern "C" int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* ou
 
 extern "C" int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     return launch_gemm<kQ6K>(a, w, N, out, stream);
+}
+
+// The scratch of mq_gemm_q6k_static: one flag per tile of an ordered split's second launch
+// (4 KB, held by every GPU that loads the library until the process exits). Host code must
+// not pass the name itself to a kernel: on the host it stands for a host-side shadow, not the
+// device memory. static_flags_ptr looks the device address up, once per device.
+static __device__ __align__(256) unsigned int g_static_flags[kStaticFlags];
+
+namespace {
+unsigned* static_flags_ptr() {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static unsigned* ptr[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_flags) != cudaSuccess || !p) return nullptr;
+        ptr[dev] = static_cast<unsigned*>(p);
+    }
+    return ptr[dev];
+}
+}  // namespace
+
+extern "C" int mq_gemm_q6k_static(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
+    const int rc = check_gemm(a, w, N, out);
+    if (rc != MQ_OK || N == 0 || a->M == 0) return rc;
+    unsigned* flags = static_flags_ptr();
+    if (!flags) return MQ_ERR_LAUNCH;
+    return launch_gemm<kQ6K>(a, w, N, out, stream, flags);
 }
 
 extern "C" int mq_gemm_q4_0(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {

@@ -16,15 +16,15 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libmq.so")
 
-MQ_OK, MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_ARCH, MQ_ERR_LAUNCH, MQ_ERR_DEVICE = range(7)
+MQ_OK, MQ_ERR_NULL, MQ_ERR_SHAPE, MQ_ERR_ALIGN, MQ_ERR_ARCH, MQ_ERR_LAUNCH, MQ_ERR_DEVICE, MQ_ERR_SCRATCH = range(8)
 MQ_GEMV_MAX_ROWS = 8   # include/mq.h
 
 EXPORTED = ["mq_plane_bytes", "mq_q4k_row_bytes", "mq_q6k_row_bytes", "mq_q6k_packed_row_bytes", "mq_prepack_q6k",
             "mq_quantize_q8", "mq_rms_quant",
             "mq_swiglu_quant", "mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k",
             "mq_q5k_row_bytes", "mq_q4_0_row_bytes", "mq_q4_1_row_bytes", "mq_gemv_q5k", "mq_gemv_q4_0",
-            "mq_gemv_q4_1", "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemv_q6k_packed", "mq_device_status",
-            "mq_status_str"]
+            "mq_gemv_q4_1", "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemv_q6k_packed", "mq_gemm_q6k_static",
+            "mq_device_status", "mq_status_str"]
 
 
 class MQError(RuntimeError):
@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
             "mq_gemv_q4k": (i, [pp, vp, i, vp, vp]),
             "mq_gemv_q6k": (i, [pp, vp, i, vp, vp]),
             "mq_gemv_q6k_packed": (i, [pp, vp, i, vp, vp]),
+            "mq_gemm_q6k_static": (i, [pp, vp, i, vp, vp]),
             "mq_q5k_row_bytes": (sz, [i]),
             "mq_q4_0_row_bytes": (sz, [i]),
             "mq_q4_1_row_bytes": (sz, [i]),
@@ -248,6 +249,12 @@ def mq_gemv_q6k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=Non
 def mq_gemv_q6k_packed(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
     """q6_K GEMV on prepacked rows (mq_prepack_q6k), the form the GEMM reads too."""
     return _matmul("mq_gemv_q6k_packed", a, w, N, out, stream)
+
+
+def mq_gemm_q6k_static(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """mq_gemm_q6k for callers that cannot have device memory allocated for them: its scratch is
+    a fixed array inside the library (see include/mq.h)."""
+    return _matmul("mq_gemm_q6k_static", a, w, N, out, stream)
 
 
 def mq_gemm_q4_0(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
