@@ -96,7 +96,7 @@ def gemm_launches(kind, M, N, K, sms):
     rest = tiles % sms
     best_cost = S
     for ts in range(2, min(sms // rest, 15) + 1):
-        best_cost = min(best_cost, -(-S // ts) + 2 * (ts - 1) + 2)
+        best_cost = min(best_cost, -(-S // ts) + 2 * (ts - 1) + 10)
     return 2 if best_cost < S else 1
 
 

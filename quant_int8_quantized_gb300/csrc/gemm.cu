@@ -956,8 +956,10 @@ int choose_splits(long long tiles, int S, int sms) {
 // Slices per tile for the tiles of an incomplete last round (Order), or 1: at most as many
 // as fit the grid (and 15, the flag's slice field), chosen to minimise that round's length
 // in super-blocks: ceil(S / ts), plus kChainCost for each hand-over between slices (a flag and
-// the additions, ~2-3 us) and kLaunchCost for the second launch. No split if nothing is gained.
-constexpr int kChainCost = 2, kLaunchCost = 2;
+// the additions, ~2-3 us) and kLaunchCost for the second launch (its pipeline fills and drains
+// again: ~20 us, measured on the q6_K kernel at ~2.2 us a super-block). No split if nothing is
+// gained.
+constexpr int kChainCost = 2, kLaunchCost = 10;
 int order_slices(long long tiles, int S, int sms) {
     if (tiles <= sms) return 1;   // fewer tiles than SMs: split-K instead
     const long long rest = tiles % sms;

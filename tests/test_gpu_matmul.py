@@ -138,13 +138,14 @@ def test_gemm_full_size_sampled_rows(kind, N, K):
     assert mq.mq_device_status() == mq.MQ_OK
 
 
-@pytest.mark.parametrize("kind,M,N,K", [("q6k", 3314, 3584, 3584), ("q6k", 3314, 3584, 18944),
-                                         ("q6k", 1000, 3456, 3584), ("q6k", 2000, 2560, 4096),
+@pytest.mark.parametrize("kind,M,N,K", [("q6k", 3314, 3584, 18944), ("q6k", 1000, 3456, 8192),
+                                         ("q6k", 2000, 2560, 16384), ("q6k", 3314, 3584, 3584),
                                          ("q4k", 3314, 3584, 3584)])
 def test_gemm_ordered_split_of_the_last_round(kind, M, N, K):
     """q6_K tile counts that leave the persistent grid's last round partly idle (504, 162 and
-    220 tiles on 152 SMs): those tiles run in a second launch as 2 or 3 K slices that add into
-    the output in a fixed order (q4_K, which does not split, as a control). Sampled rows
+    220 tiles on 152 SMs) with enough super-blocks a row for a split to pay (74, 32, 64): those
+    tiles run in a second launch as 2 to 4 K slices that add into the output in a fixed order
+    (q6_K with 14 super-blocks a row, which does not split, and q4_K as controls). Sampled rows
     against the oracle, half of them in the last 400 tokens (where those tiles lie), every
     element written, the same bits on a second call and on three replays of a captured graph,
     and no bounded wait given up."""

@@ -36,7 +36,7 @@ def _call(name, plane, w, N, out):
                                    ctypes.c_void_p(out.data_ptr()), stream)
 
 
-@pytest.mark.parametrize("M,N,K", [(3314, 3584, 3584), (1000, 3456, 3584), (2000, 2560, 4096), (200, 768, 1024)])
+@pytest.mark.parametrize("M,N,K", [(3314, 3584, 18944), (1000, 3456, 8192), (2000, 2560, 16384), (200, 768, 1024)])
 def test_static_variant_matches_gemm_q6k(M, N, K):
     x = synth.normal((M, K), 0, f"na.x{M}x{K}", device="cuda")
     w_raw = synth.weights("q6k", N, K, 0, f"na.w{N}x{K}")
