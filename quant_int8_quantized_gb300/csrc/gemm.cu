@@ -349,7 +349,6 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
     extern __shared__ uint8_t smem_raw[];
     Smem<WT, SH>& sm = *reinterpret_cast<Smem<WT, SH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    mq_grid_release();   // a dependent launch (the second launch of an ordered split) may start
     const int S = K / mq::QK_K;
     const int num_mt = (M + bt - 1) / bt, num_nt = (N + BW - 1) / BW;
     // the ordered split (Order) is compiled into its own instance, used only for the second
@@ -396,6 +395,13 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tbase = sm.tmem;
+    // Launched as a programmatic dependent launch, the set-up above overlaps the previous
+    // kernel's tail; nothing in global memory is read or written before this wait. The next
+    // launch may start only once every CTA has passed it, so the second launch of an ordered
+    // split (which reads nothing the first one writes) needs no wait of its own here: by then
+    // the kernels before the first launch have completed.
+    if constexpr (!ORD) mq_grid_wait();
+    mq_grid_release();
 
     if (warp < 4) {
         // ============================================================ warpgroup 0
@@ -901,8 +907,8 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
         if (sp < splits - 1) st_release_u32(fl, (ord.epoch << 4) | (unsigned)(sp + 1));
         else *fl = 0u;
     }
-    // the second launch of an ordered split ends after the first one (a no-op otherwise), so
-    // that what follows on the stream sees both
+    // the second launch of an ordered split ends after the first one (otherwise the wait has
+    // returned already), so that what follows on the stream sees both
     mq_grid_wait();
 }
 
@@ -1077,10 +1083,10 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
         const long long units = (long long)ntiles * sp;
         const int grid = (int)(units < sms ? units : sms);
         if (sh)
-            return mq::launch_plain(gemm_kernel<WT, kS>, dim3(grid), dim3(Cfg<WT, kS>::kThreads), smem, stream, tmAct,
-                                    tmAx, tmAf, tmW, out, M, N, K, sp, nfast, bt, tile0, ntiles, none);
-        return mq::launch_plain(gemm_kernel<WT, false>, dim3(grid), dim3(Cfg<WT, false>::kThreads), smem, stream, tmAct,
-                                tmAx, tmAf, tmW, out, M, N, K, sp, nfast, bt, tile0, ntiles, none);
+            return mq::launch_pdl(gemm_kernel<WT, kS>, dim3(grid), dim3(Cfg<WT, kS>::kThreads), smem, stream, tmAct,
+                                  tmAx, tmAf, tmW, out, M, N, K, sp, nfast, bt, tile0, ntiles, none);
+        return mq::launch_pdl(gemm_kernel<WT, false>, dim3(grid), dim3(Cfg<WT, false>::kThreads), smem, stream, tmAct,
+                              tmAx, tmAf, tmW, out, M, N, K, sp, nfast, bt, tile0, ntiles, none);
     };
     const int ts = WT == kQ6K && !sh && splits == 1 ? order_slices(tiles, S, sms) : 1;
     if (ts == 1) return plain(0, (int)tiles, splits);
