@@ -43,6 +43,7 @@
 //   warp 1      MMA issuer (warps 0 and 1 run their loops as whole warps, one
 //               elected lane issuing each copy, MMA and commit);
 //   warp 2      TMEM allocator;
+//   warp 3      (ordered split only) waits for the tile's previous K slice, see Order;
 //   warps 4-11  weight converters, thread = weight row, two warps per TMEM lane
 //               quarter, each half of a super-block's K;
 //   warps 12-19 epilogue, thread = weight row, two warps per lane quarter, 96
@@ -50,6 +51,9 @@
 //               super-blocks of a work unit.
 // Every mbarrier wait is bounded; on timeout the kernel records an error, stops,
 // drains its own copies and MMAs, frees TMEM and returns.
+// Launches are programmatic dependent launches (set-up overlaps the previous kernel). A q6_K
+// call whose tiles leave the grid's last round partly idle makes a second, dependent launch
+// that runs those tiles as K slices added into the output in a fixed order (Order).
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
