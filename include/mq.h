@@ -22,6 +22,11 @@
  *    `stream` (0 = legacy default stream).
  *  - Inputs are read only. Outputs (planes, out) are overwritten, never
  *    accumulated into.
+ *  - Stream order holds as for any CUDA work: a call's memory accesses come after
+ *    the work enqueued before it on `stream` and before the work enqueued after
+ *    it. The producers and the prefill GEMMs are programmatic dependent launches:
+ *    their set-up may overlap the end of the previous kernel on the stream, but
+ *    they touch no global memory before that kernel has completed.
  *  - K must be a positive multiple of 256 (one weight super-block; it also
  *    gives the producers whole 8-lane groups, [r52] §3.2). M == 0 or N == 0 is
  *    a no-op returning MQ_OK.
