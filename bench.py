@@ -62,7 +62,7 @@ BYTES_PER_SB = {"q4k": 144, "q6k": 210, "q5k": 176, "q4_0": 8 * 18, "q4_1": 8 * 
 # with these SHA-256 digests (gemm.cu up to its host-side section, and tc.cuh) and is reported as
 # null once either changes.
 GEMM_Q4K_TRAFFIC = {"bytes": 66515712 + 205114880,
-                    "sha256": {"gemm.cu": "076951c220e4fce411b6c2a37a82db40bc877fb40222879e43d347607cc50321",
+                    "sha256": {"gemm.cu": "4a5543e9a53af1aa5d28206697ae252feef59f31b63aa95691427d74b0cfb215",
                                "tc.cuh": "77627d374b6dc4619249b40701e93050c782a7d46494b273d5b7a343462067e1"}}
 HOST_SECTION = b"// ------------------------------------------------------------------ host side"
 

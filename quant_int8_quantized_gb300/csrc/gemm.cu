@@ -86,6 +86,9 @@ constexpr uint64_t kWaitLimitNs = MQ_WAIT_LIMIT_NS;
 // Test builds only: when set, CTA 0's TMA producer skips its first activation copy, so that
 // chunk's barrier never completes and the kernel's bounded waits run out (abort path).
 __device__ int g_test_skip_first_act;
+// Test builds only: when set, the first K slice of each tile of an ordered split never passes
+// its flag on, so the later slices' bounded waits for it run out (abort path).
+__device__ int g_test_skip_release;
 #endif
 constexpr uint32_t kTmemCols = 512;
 constexpr int kShortTok = 64;           // token tiles up to this take the short-tile form (q4_K)
@@ -908,8 +911,11 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
         // at GPU scope passes the tile to its next slice, or frees the flag after the last one
         const int sp = blockIdx.x % splits, r0 = blockIdx.x / splits;
         unsigned* fl = (SF ? ord.flags : g_order_flags) + ord.base + r0;
-        if (sp < splits - 1) st_release_u32(fl, (ord.epoch << 4) | (unsigned)(sp + 1));
-        else *fl = 0u;
+#ifdef MQ_TEST_INJECT
+        if (g_test_skip_release && sp == 0) fl = nullptr;
+#endif
+        if (fl && sp < splits - 1) st_release_u32(fl, (ord.epoch << 4) | (unsigned)(sp + 1));
+        else if (fl) *fl = 0u;
     }
     // the second launch of an ordered split ends after the first one (otherwise the wait has
     // returned already), so that what follows on the stream sees both
@@ -1143,9 +1149,14 @@ int take_gemm_device_error(cudaStream_t stream, unsigned* code) {
 }  // namespace mq
 
 #ifdef MQ_TEST_INJECT
-// Test builds only: switch the injected missing copy on or off.
+// Test builds only: switch the injected failures on or off (bit 0: the missing copy, bit 1:
+// the missing flag release of an ordered split).
 extern "C" int mq_test_inject(int on) {
-    return cudaMemcpyToSymbol(g_test_skip_first_act, &on, sizeof(on)) == cudaSuccess ? MQ_OK : MQ_ERR_LAUNCH;
+    const int act = on & 1, rel = (on >> 1) & 1;
+    return cudaMemcpyToSymbol(g_test_skip_first_act, &act, sizeof(act)) == cudaSuccess &&
+                   cudaMemcpyToSymbol(g_test_skip_release, &rel, sizeof(rel)) == cudaSuccess
+               ? MQ_OK
+               : MQ_ERR_LAUNCH;
 }
 #endif
 
