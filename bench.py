@@ -61,8 +61,8 @@ BYTES_PER_SB = {"q4k": 144, "q6k": 210, "q5k": 176, "q4_0": 8 * 18, "q4_1": 8 * 
 # 3314 x 18944 x 3584, from one ncu capture (summary under profiles/). It describes the device code
 # with these SHA-256 digests (gemm.cu up to its host-side section, and tc.cuh) and is reported as
 # null once either changes.
-GEMM_Q4K_TRAFFIC = {"bytes": 66515712 + 205114880,
-                    "sha256": {"gemm.cu": "4a5543e9a53af1aa5d28206697ae252feef59f31b63aa95691427d74b0cfb215",
+GEMM_Q4K_TRAFFIC = {"bytes": 67058432 + 204712960,
+                    "sha256": {"gemm.cu": "c5a12fc9c911e518b926dfbcfb3fc2ecbb646a65af2637e6ff5c2390560f8581",
                                "tc.cuh": "77627d374b6dc4619249b40701e93050c782a7d46494b273d5b7a343462067e1"}}
 HOST_SECTION = b"// ------------------------------------------------------------------ host side"
 
@@ -232,10 +232,15 @@ class Stack:
             self.ev_h = torch.cuda.Event()
             self.ev_kv = torch.cuda.Event()
 
-    # launches per prefill step: 28 * (2 rms + 1 quantize + 1 swiglu + the GEMMs' launches) + rms + gemv
+    # launches per prefill step: 28 * (2 rms + 1 quantize + 1 swiglu + the GEMMs' launches) + rms + gemv;
+    # attn_q and attn_k are one paired call (one launch when their tiles fill a round, as here)
     @staticmethod
     def launches_per_step(sms):
-        gemms = sum(gemm_launches(kind, M_TOK, N, K, sms) for _, kind, N, K, _ in PREFILL_MATS)
+        mats = {name: (kind, N, K) for name, kind, N, K, _ in PREFILL_MATS}
+        tiles = lambda N: -(-M_TOK // 192) * -(-N // 128)
+        qk = 1 if tiles(mats["q"][1]) + tiles(mats["k"][1]) >= sms else 2
+        gemms = qk + sum(gemm_launches(kind, M_TOK, N, K, sms) for name, (kind, N, K) in mats.items()
+                         if name not in ("q", "k"))
         return LAYERS * (4 + gemms) + 2
     LAUNCHES_PER_DECODE = D_LAYERS * 8   # rms, q, k|v, quantize, o, gate|up, swiglu, down
 
@@ -248,6 +253,11 @@ class Stack:
             mq.mq_quantize_q8(self.attn, self.p_attn)
             mq.mq_rms_quant(self.x, self.rms2_w[l], EPS, self.p_rms2)
             for name, kind, N, K, src in PREFILL_MATS:
+                if name == "k":
+                    continue   # with q, below
+                if name == "q":   # attn_q and attn_k read the same plane: one paired call
+                    mq.mq_gemm_q4k_pair(planes[src], W["q"], N, self.out["q"], W["k"], KVD, self.out["k"])
+                    continue
                 if name == "down":
                     mq.mq_swiglu_quant(self.out["gate"], self.out["up"], self.p_ffn)
                 if time_q4 and name in ("gate", "up"):

@@ -211,6 +211,20 @@ int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
 int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream);
 
 /*
+ * mq_gemm_q4k_pair — two q4_K GEMMs that read the same activation plane (the same M and K,
+ * e.g. attn_q and attn_k, or ffn_gate and ffn_up: [r52] §2.2's one plane feeding several
+ * projections), out0 = a x w0 (N0 rows) and out1 = a x w1 (N1 rows), each exactly as
+ * mq_gemm_q4k computes it (the same bits, for tiles that mq_gemm_q4k would not split along
+ * K). When both have whole 192-token tiles (M >= 192) and together fill at least one round of
+ * the GPU's SMs, they run in one launch, the second problem's tiles filling what the first
+ * leaves idle and the pair paying one launch's fixed cost; otherwise the call makes two
+ * mq_gemm_q4k calls. Arguments, accuracy and errors as for mq_gemm_q4k, for each problem;
+ * MQ_ERR_SHAPE also if out0 and out1 overlap.
+ */
+int mq_gemm_q4k_pair(const mq_q8_plane* a, const void* w0, int N0, float* out0, const void* w1, int N1,
+                     float* out1, cudaStream_t stream);
+
+/*
  * mq_gemm_q6k_static — mq_gemm_q6k for callers that cannot have device memory allocated on
  * their behalf: a server that hands all device memory to its own pool at start-up, or code
  * that must not call cudaMalloc because it can synchronize the device and stall other work.

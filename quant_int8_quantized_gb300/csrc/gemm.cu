@@ -188,6 +188,7 @@ struct Smem {
 // order for an ordered launch (see Order).
 struct Work {
     int m0, n0, sb0, sb1, sp, r;
+    int pb;   // paired launch: which of the two problems (0: out / N / tmW, 1: Pair)
 };
 // nfast: weight-row tiles fastest (when the activation operand is the larger one, so
 // that each token tile's activations are read from memory once).
@@ -195,8 +196,19 @@ __device__ __forceinline__ Work work_of(int u, int splits, int num_mt, int num_n
                                         int tile0) {
     const int r = u / splits, sp = u - r * splits, t = tile0 + r;
     const int mt = nfast ? t / num_nt : t % num_mt, nt = nfast ? t % num_nt : t / num_mt;
-    return Work{mt * bt, nt * BW, (sp * S) / splits, ((sp + 1) * S) / splits, sp, r};
+    return Work{mt * bt, nt * BW, (sp * S) / splits, ((sp + 1) * S) / splits, sp, r, 0};
 }
+
+// Paired launch (mq_gemm_q4k_pair): two q4_K problems that read the same activation plane (the
+// same M and K, e.g. attn_q and attn_k, or ffn_gate and ffn_up) in one persistent launch, whole
+// tiles only. Units 0 .. tiles0 - 1 are the first problem's tiles (out, N, tmW), the rest the
+// second's (Pair::out, Pair::N, tmW2): the second problem's tiles fill the rounds the first
+// leaves idle, and the pair pays one launch's fixed cost instead of two.
+struct Pair {
+    float* out;   // the second problem's output
+    int N;        // its weight rows
+    int tiles0;   // the first problem's tiles
+};
 
 // Ordered split. A persistent grid of G CTAs takes the output tiles G at a time; when their
 // count T is not a multiple of G, the last round would leave SMs idle for a whole tile's
@@ -344,13 +356,15 @@ __device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
     return (uint32_t)*reinterpret_cast<const uint16_t*>(p) | ((uint32_t)*reinterpret_cast<const uint16_t*>(p + 2) << 16);
 }
 
-template <int WT, bool SH, bool ORD = false, bool SF = false>
+template <int WT, bool SH, bool ORD = false, bool SF = false, bool PAIR = false>
 __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __grid_constant__ CUtensorMap tmAct,
                                                            const __grid_constant__ CUtensorMap tmAx,
                                                            const __grid_constant__ CUtensorMap tmAf,
                                                            const __grid_constant__ CUtensorMap tmW,
+                                                           const __grid_constant__ CUtensorMap tmW2,
                                                            float* __restrict__ out, int M, int N, int K, int splits,
-                                                           int nfast, int bt, int tile0, int ntiles, const Order ord) {
+                                                           int nfast, int bt, int tile0, int ntiles, const Order ord,
+                                                           const Pair pair) {
     using C = Cfg<WT, SH>;
     constexpr int kRB = C::kRB, kRF = C::kRF;
     extern __shared__ uint8_t smem_raw[];
@@ -363,10 +377,25 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
     // them up to 27 % slower
     constexpr bool kOrd = ORD;
     // q6_K launches may cover part of the tiles (the first launch of an ordered split)
-    const int units = WT == kQ6K ? ntiles * splits : num_mt * num_nt * splits;
+    int units = WT == kQ6K ? ntiles * splits : num_mt * num_nt * splits;
+    if constexpr (PAIR) units = pair.tiles0 + num_mt * ((pair.N + BW - 1) / BW);   // whole tiles (splits = 1)
+    // the work unit u: its tile and super-block range, and for a paired launch its problem
+    auto unit = [&](int u) -> Work {
+        if constexpr (PAIR) {
+            if (u >= pair.tiles0) {
+                Work w = work_of(u - pair.tiles0, 1, num_mt, (pair.N + BW - 1) / BW, nfast, S, bt, 0);
+                w.pb = 1;
+                return w;
+            }
+            return work_of(u, 1, num_mt, num_nt, nfast, S, bt, 0);
+        } else {
+            return work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
+        }
+    };
 
     if (tid == 0) {
         tc::prefetch_tensormap(&tmW);
+        if constexpr (PAIR) tc::prefetch_tensormap(&tmW2);
         tc::prefetch_tensormap(&tmAct);
         tc::prefetch_tensormap(&tmAx);
         tc::prefetch_tensormap(&tmAf);
@@ -421,7 +450,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
             uint32_t issA = 0, phA = 0, issX = 0, phX = 0, issB = 0, phB = 0;   // copies in flight (for an abort)
             int sbc = 0, ga = 0;
             for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
+                const Work wk = unit(u);
                 for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb, ++sbc) {
                     const int x = sbc % RX;
                     if (!wwait(sm, &sm.ax_empty[x], ((sbc / RX) & 1) ^ 1)) break;
@@ -434,7 +463,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
                         const int b = sbc % kRB;
                         if (!wwait(sm, &sm.b_empty[b], ((sbc / kRB) & 1) ^ 1)) break;
                         if (leader) tc::mbar_arrive_expect_tx(&sm.b_full[b], C::kStage);
-                        if (leader) tc::tma_load_2d(sm.braw[b], &tmW, sb * C::kSB, wk.n0, &sm.b_full[b]);
+                        if (leader) tc::tma_load_2d(sm.braw[b], PAIR && wk.pb ? &tmW2 : &tmW, sb * C::kSB, wk.n0, &sm.b_full[b]);
                         issB |= 1u << b;
                         phB = (phB & ~(1u << b)) | (((sbc / kRB) & 1) << b);
                     }
@@ -476,7 +505,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
             const uint32_t idesc = tc::instr_desc(BW, (uint32_t)bt, 0);
             int total = 0;   // super-blocks this CTA accumulates (the issuer needs no tile positions)
             for (int u = blockIdx.x; u < units; u += gridDim.x) {
-                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
+                const Work wk = unit(u);
                 total += wk.sb1 - wk.sb0;
             }
             // readiness of chunk j of super-block sbc, whose activation slot is ga
@@ -569,7 +598,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
             // host keeps its units within the grid).
             const int u = blockIdx.x;
             if (u < units) {
-                const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
+                const Work wk = unit(u);
                 if (wk.sp > 0) {
                     const bool got =
                         lane == 0 ? wait_flag((SF ? ord.flags : g_order_flags) + ord.base + wk.r, (ord.epoch << 4) | (unsigned)wk.sp) : true;
@@ -591,7 +620,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         int sbc = 0;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
+            const Work wk = unit(u);
             const int n = wk.n0 + r;
             for (int sb = wk.sb0; sb < wk.sb1 && !waborted(sm); ++sb, ++sbc) {
                 const int b = sbc % kRB, x = sbc % RX;
@@ -672,7 +701,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&sm.ax_full[x]);
                         if (!wwait(sm, &sm.c_empty[x], ((sbc / RX) & 1) ^ 1)) break;
-                        sm.cvec[x][r] = n < N ? hd.c : 0.0f;
+                        sm.cvec[x][r] = n < (PAIR && wk.pb ? pair.N : N) ? hd.c : 0.0f;
                         __syncwarp();
                         if (lane == 0) tc::mbar_arrive(&sm.c_full[x]);
                     }
@@ -833,7 +862,7 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
         const uint32_t lane_bits = (uint32_t)(32 * q) << 16;
         int sbc = 0;
         for (int u = blockIdx.x; u < units && !waborted(sm); u += gridDim.x) {
-            const Work wk = work_of(u, splits, num_mt, num_nt, nfast, S, bt, kOrd ? tile0 : 0);
+            const Work wk = unit(u);
             float acc[C::kEpiCols];
 #pragma unroll
             for (int i = 0; i < C::kEpiCols; ++i) acc[i] = 0.0f;
@@ -887,14 +916,15 @@ __global__ void __launch_bounds__(Cfg<WT, SH>::kThreads, 1) gemm_kernel(const __
                 add = splits > 1;
             }
             const int n = wk.n0 + r;
-            if (n < N) {
+            const int NN = PAIR && wk.pb ? pair.N : N;
+            if (n < NN) {
                 const int t0 = wk.m0 + C::kEpiCols * ch;
-                float* op = out + (size_t)t0 * N + n;
+                float* op = (PAIR && wk.pb ? pair.out : out) + (size_t)t0 * NN + n;
 #pragma unroll
                 for (int i = 0; i < C::kEpiCols; ++i) {
                     if (t0 + i < M) {
-                        if (add) atomicAdd(op + (size_t)i * N, acc[i]);
-                        else op[(size_t)i * N] = acc[i];
+                        if (add) atomicAdd(op + (size_t)i * NN, acc[i]);
+                        else op[(size_t)i * NN] = acc[i];
                     }
                 }
             }
@@ -1023,7 +1053,7 @@ int check_gemm(const mq_q8_plane* a, const void* w, int N, const float* out) {
 // Once per device: the register split between warpgroups assumes the launch register
 // count, and the kernel's shared-memory size is set. Later calls make no attribute
 // calls, so a sequence of entry points can be captured in a graph.
-template <int WT, bool SH, bool ORD = false, bool SF = false>
+template <int WT, bool SH, bool ORD = false, bool SF = false, bool PAIR = false>
 bool gemm_ready(size_t smem) {
     constexpr int kMaxDevices = 64;
     static int state[kMaxDevices];   // 0 unknown, 1 ready, 2 failed
@@ -1036,9 +1066,10 @@ bool gemm_ready(size_t smem) {
         v = state[dev];
         if (v == 0) {
             cudaFuncAttributes fa;
-            v = (cudaFuncGetAttributes(&fa, gemm_kernel<WT, SH, ORD, SF>) == cudaSuccess &&
+            v = (cudaFuncGetAttributes(&fa, gemm_kernel<WT, SH, ORD, SF, PAIR>) == cudaSuccess &&
                  fa.numRegs == Cfg<WT, SH>::kLaunchRegs &&
-                 cudaFuncSetAttribute(gemm_kernel<WT, SH, ORD, SF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+                 cudaFuncSetAttribute(gemm_kernel<WT, SH, ORD, SF, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem) ==
                      cudaSuccess)
                     ? 1
                     : 2;
@@ -1058,6 +1089,16 @@ int token_tile(int M) { return M >= BT ? BT : ((M + 15) / 16) * 16; }
 // static_flags: mq_gemm_q6k_static's fixed flag array (device address), else nullptr
 constexpr int kStaticFlags = 1024;   // tiles an ordered split of mq_gemm_q6k_static may cut, at most
 
+// Tensor maps of the plane's operand arrays for token tiles of bt.
+bool act_maps(const mq_q8_plane* a, int bt, CUtensorMap* tmAct, CUtensorMap* tmAx, CUtensorMap* tmAf) {
+    const int M = a->M, K = a->K, S = K / mq::QK_K, mp = mq::af_stride(M);
+    return make_map(tmAct, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ah, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, KS, bt,
+                    CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map(tmAx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ax, (uint64_t)S * 16, (uint64_t)M, (uint64_t)S * 32, 16, bt,
+                    CU_TENSOR_MAP_SWIZZLE_32B) &&
+           make_map(tmAf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->af, (uint64_t)mp, (uint64_t)S, (uint64_t)mp * 4, bt, 1);
+}
+
 template <int WT>
 int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream,
                 unsigned* static_flags = nullptr) {
@@ -1073,13 +1114,7 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
     CUtensorMap tmAct, tmAx, tmAf, tmW;
     if (!make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, row, (uint64_t)N, row, Cfg<WT>::kRowBytes, BW))
         return MQ_ERR_LAUNCH;
-    const int mp = mq::af_stride(M);
-    if (!make_map(&tmAct, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ah, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, KS, bt,
-                  CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tmAx, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a->ax, (uint64_t)S * 16, (uint64_t)M, (uint64_t)S * 32, 16,
-                  bt, CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !make_map(&tmAf, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a->af, (uint64_t)mp, (uint64_t)S, (uint64_t)mp * 4, bt, 1))
-        return MQ_ERR_LAUNCH;
+    if (!act_maps(a, bt, &tmAct, &tmAx, &tmAf)) return MQ_ERR_LAUNCH;
     const long long tiles = (long long)((M + bt - 1) / bt) * ((N + BW - 1) / BW);
     const int sms = mq::num_sms();
     const int splits = choose_splits(tiles, S, sms);
@@ -1094,9 +1129,9 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
         const int grid = (int)(units < sms ? units : sms);
         if (sh)
             return mq::launch_pdl(gemm_kernel<WT, kS>, dim3(grid), dim3(Cfg<WT, kS>::kThreads), smem, stream, tmAct,
-                                  tmAx, tmAf, tmW, out, M, N, K, sp, nfast, bt, tile0, ntiles, none);
+                                  tmAx, tmAf, tmW, tmW, out, M, N, K, sp, nfast, bt, tile0, ntiles, none, Pair{});
         return mq::launch_pdl(gemm_kernel<WT, false>, dim3(grid), dim3(Cfg<WT, false>::kThreads), smem, stream, tmAct,
-                              tmAx, tmAf, tmW, out, M, N, K, sp, nfast, bt, tile0, ntiles, none);
+                              tmAx, tmAf, tmW, tmW, out, M, N, K, sp, nfast, bt, tile0, ntiles, none, Pair{});
     };
     const int ts = WT == kQ6K && !sh && splits == 1 ? order_slices(tiles, S, sms) : 1;
     if (ts == 1) return plain(0, (int)tiles, splits);
@@ -1113,8 +1148,8 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
             rc = plain(0, full, 1);
             if (rc != MQ_OK) return rc;
             return mq::launch_pdl(gemm_kernel<WT, false, true, true>, dim3(rest * ts), dim3(Cfg<WT, false>::kThreads), smem,
-                                  stream, tmAct, tmAx, tmAf, tmW, out, M, N, K, ts, nfast, bt, full, rest,
-                                  Order{1, 1u, 0u, static_flags});
+                                  stream, tmAct, tmAx, tmAf, tmW, tmW, out, M, N, K, ts, nfast, bt, full, rest,
+                                  Order{1, 1u, 0u, static_flags}, Pair{});
         }
         if (!gemm_ready<WT, false, true>(smem)) return MQ_ERR_LAUNCH;
         Order ord{1, 0u, 0u};
@@ -1122,9 +1157,48 @@ int launch_gemm(const mq_q8_plane* a, const void* w, int N, float* out, cudaStre
         rc = plain(0, full, 1);
         if (rc != MQ_OK) return rc;
         return mq::launch_pdl(gemm_kernel<WT, false, true>, dim3(rest * ts), dim3(Cfg<WT, false>::kThreads), smem, stream,
-                              tmAct, tmAx, tmAf, tmW, out, M, N, K, ts, nfast, bt, full, rest, ord);
+                              tmAct, tmAx, tmAf, tmW, tmW, out, M, N, K, ts, nfast, bt, full, rest, ord, Pair{});
     }
     return MQ_ERR_LAUNCH;
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na && nb && x < y + nb && y < x + na;
+}
+
+// Two q4_K problems on one plane (Pair): one launch when both have whole 192-token tiles and
+// together fill at least one round of the grid, else two ordinary calls.
+int launch_gemm_q4k_pair(const mq_q8_plane* a, const void* w0, int N0, float* out0, const void* w1, int N1,
+                         float* out1, cudaStream_t stream) {
+    int rc = check_gemm(a, w0, N0, out0);
+    if (rc == MQ_OK) rc = check_gemm(a, w1, N1, out1);
+    if (rc != MQ_OK) return rc;
+    if (a->M == 0) return MQ_OK;
+    const int M = a->M, K = a->K, S = K / mq::QK_K;
+    if (ranges_overlap(out0, (size_t)M * N0 * sizeof(float), out1, (size_t)M * N1 * sizeof(float))) return MQ_ERR_SHAPE;
+    const int bt = token_tile(M), sms = mq::num_sms();
+    const long long num_mt = (M + bt - 1) / bt;
+    const long long tiles0 = num_mt * ((N0 + BW - 1) / BW), tiles1 = num_mt * ((N1 + BW - 1) / BW);
+    if (N0 == 0 || N1 == 0 || bt != BT || tiles0 + tiles1 < sms) {
+        rc = launch_gemm<kQ4K>(a, w0, N0, out0, stream);
+        return rc != MQ_OK ? rc : launch_gemm<kQ4K>(a, w1, N1, out1, stream);
+    }
+    using C = Cfg<kQ4K, false>;
+    const size_t smem = sizeof(Smem<kQ4K, false>) + 1024;
+    if (!gemm_ready<kQ4K, false, false, false, true>(smem)) return MQ_ERR_LAUNCH;
+    const unsigned long long row = (unsigned long long)S * C::kSB;
+    CUtensorMap tmAct, tmAx, tmAf, tmW0, tmW1;
+    if (!make_map(&tmW0, CU_TENSOR_MAP_DATA_TYPE_UINT8, w0, row, (uint64_t)N0, row, C::kRowBytes, BW) ||
+        !make_map(&tmW1, CU_TENSOR_MAP_DATA_TYPE_UINT8, w1, row, (uint64_t)N1, row, C::kRowBytes, BW) ||
+        !act_maps(a, bt, &tmAct, &tmAx, &tmAf))
+        return MQ_ERR_LAUNCH;
+    const int nfast = (double)M * K * 2 > (double)(N0 + N1) * row ? 1 : 0;
+    const long long units = tiles0 + tiles1;
+    const int grid = (int)(units < sms ? units : sms);
+    return mq::launch_pdl(gemm_kernel<kQ4K, false, false, false, true>, dim3(grid), dim3(C::kThreads), smem, stream,
+                          tmAct, tmAx, tmAf, tmW0, tmW1, out0, M, N0, K, 1, nfast, bt, 0, (int)tiles0, Order{},
+                          Pair{out1, N1, (int)tiles0});
 }
 
 }  // namespace
@@ -1166,6 +1240,11 @@ extern "C" int mq_gemm_q4k(const mq_q8_plane* a, const void* w, int N, float* ou
 
 extern "C" int mq_gemm_q6k(const mq_q8_plane* a, const void* w, int N, float* out, cudaStream_t stream) {
     return launch_gemm<kQ6K>(a, w, N, out, stream);
+}
+
+extern "C" int mq_gemm_q4k_pair(const mq_q8_plane* a, const void* w0, int N0, float* out0, const void* w1, int N1,
+                                float* out1, cudaStream_t stream) {
+    return launch_gemm_q4k_pair(a, w0, N0, out0, w1, N1, out1, stream);
 }
 
 // The scratch of mq_gemm_q6k_static: one flag per tile of an ordered split's second launch

@@ -23,7 +23,7 @@ EXPORTED = ["mq_plane_bytes", "mq_q4k_row_bytes", "mq_q6k_row_bytes", "mq_q6k_pa
             "mq_quantize_q8", "mq_rms_quant",
             "mq_swiglu_quant", "mq_gemm_q4k", "mq_gemm_q6k", "mq_gemv_q4k", "mq_gemv_q6k",
             "mq_q5k_row_bytes", "mq_q4_0_row_bytes", "mq_q4_1_row_bytes", "mq_gemv_q5k", "mq_gemv_q4_0",
-            "mq_gemv_q4_1", "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemv_q6k_packed", "mq_gemm_q6k_static",
+            "mq_gemv_q4_1", "mq_gemm_q4_0", "mq_gemm_q4_1", "mq_gemv_q6k_packed", "mq_gemm_q6k_static", "mq_gemm_q4k_pair",
             "mq_device_status", "mq_status_str"]
 
 
@@ -67,6 +67,7 @@ def lib() -> ctypes.CDLL:
             "mq_gemv_q6k": (i, [pp, vp, i, vp, vp]),
             "mq_gemv_q6k_packed": (i, [pp, vp, i, vp, vp]),
             "mq_gemm_q6k_static": (i, [pp, vp, i, vp, vp]),
+            "mq_gemm_q4k_pair": (i, [pp, vp, i, vp, vp, i, vp, vp]),
             "mq_q5k_row_bytes": (sz, [i]),
             "mq_q4_0_row_bytes": (sz, [i]),
             "mq_q4_1_row_bytes": (sz, [i]),
@@ -249,6 +250,22 @@ def mq_gemv_q6k(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=Non
 def mq_gemv_q6k_packed(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:
     """q6_K GEMV on prepacked rows (mq_prepack_q6k), the form the GEMM reads too."""
     return _matmul("mq_gemv_q6k_packed", a, w, N, out, stream)
+
+
+def mq_gemm_q4k_pair(a: Plane, w0: torch.Tensor, N0: int, out0: torch.Tensor, w1: torch.Tensor, N1: int,
+                     out1: torch.Tensor, stream=None):
+    """Two q4_K GEMMs on one plane (include/mq.h): out0 = a x w0, out1 = a x w1, in one launch
+    where that pays."""
+    for t, n in ((w0, "w0"), (w1, "w1")):
+        _dev_tensor(t, torch.uint8, n)
+    for t, n, N in ((out0, "out0", N0), (out1, "out1", N1)):
+        _dev_tensor(t, torch.float32, n)
+        if t.numel() < a.M * N:
+            raise ValueError(f"mq_gemm_q4k_pair: {n} holds {t.numel()} floats, needs M * N = {a.M * N}")
+    cp = a.c()
+    _check(lib().mq_gemm_q4k_pair(ctypes.byref(cp), _ptr(w0), int(N0), _ptr(out0), _ptr(w1), int(N1), _ptr(out1),
+                                  _stream(stream)), "mq_gemm_q4k_pair")
+    return out0, out1
 
 
 def mq_gemm_q6k_static(a: Plane, w: torch.Tensor, N: int, out: torch.Tensor, stream=None) -> torch.Tensor:

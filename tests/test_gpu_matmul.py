@@ -185,6 +185,43 @@ def test_gemm_ordered_split_of_the_last_round(kind, M, N, K):
     assert mq.mq_device_status() == mq.MQ_OK
 
 
+@pytest.mark.parametrize("M,N0,N1,K", [(3314, 3584, 512, 3584), (3314, 18944, 18944, 3584), (1000, 2560, 1280, 1024),
+                                        (400, 2560, 640, 1024)])
+def test_gemm_q4k_pair(M, N0, N1, K):
+    """Two q4_K GEMMs on one plane (attn_q | attn_k and ffn_gate | ffn_up at 3314 tokens, a small
+    pair, and one too small to share a launch): each output within the oracle bound on sampled
+    rows (half of them in the last 400 tokens) and bit-identical to mq_gemm_q4k's where that call
+    does not split along K, every element written, the same bits on a second call."""
+    x = synth.normal((M, K), 0, f"px{M}x{K}", device="cuda")
+    w0 = synth.weights("q4k", N0, K, 0, f"pw0{N0}x{K}", device="cuda")
+    w1 = synth.weights("q4k", N1, K, 0, f"pw1{N1}x{K}", device="cuda")
+    p = mq.Plane.empty(M, K)
+    mq.mq_quantize_q8(x, p)
+    g0, g1 = Guarded((M, N0), torch.float32), Guarded((M, N1), torch.float32)
+    mq.mq_gemm_q4k_pair(p, w0, N0, g0.t, w1, N1, g1.t)
+    torch.cuda.synchronize()
+    g0.check()
+    g1.check()
+    assert g0.untouched() == 0 and g1.untouched() == 0, "unwritten outputs"
+    rng = np.random.default_rng(M + N0 + N1)
+    tail = np.arange(max(0, M - 400), M)
+    rows = np.unique(np.r_[rng.choice(M, 10, replace=False), rng.choice(tail, 10, replace=False), M - 1])
+    for g, w, N in ((g0, w0, N0), (g1, w1, N1)):
+        _check(g.t, p, w, "q4k", N, K, rows=rows)
+        single = torch.empty((M, N), device="cuda")
+        mq.mq_gemm_q4k(p, w, N, single)
+        torch.cuda.synchronize()
+        bt = 192 if M >= 192 else (M + 15) // 16 * 16
+        tiles = -(-M // bt) * -(-N // 128)
+        if tiles >= torch.cuda.get_device_properties(0).multi_processor_count:   # mq_gemm_q4k does not split
+            assert torch.equal(single, g.t), f"N = {N}: other bits than mq_gemm_q4k"
+    o0, o1 = torch.empty((M, N0), device="cuda"), torch.empty((M, N1), device="cuda")
+    mq.mq_gemm_q4k_pair(p, w0, N0, o0, w1, N1, o1)
+    torch.cuda.synchronize()
+    assert torch.equal(o0, g0.t) and torch.equal(o1, g1.t), "a second call gave other bits"
+    assert mq.mq_device_status() == mq.MQ_OK
+
+
 # ----------------------------------------------------------------- GEMV
 
 GEMV_SHAPES = [(256, 512), (1024, 5120), (100, 768), (5120, 13824), (1, 256), (7001, 3584), (3, 1280)]
