@@ -1040,13 +1040,20 @@ bool order_range(int need, unsigned* epoch, unsigned* base) {
     return true;
 }
 
-int check_gemm(const mq_q8_plane* a, const void* w, int N, const float* out) {
+// The host-side checks of one GEMM call's arguments (check_gemm adds the architecture).
+int check_gemm_args(const mq_q8_plane* a, const void* w, int N, const float* out) {
     if (!a) return MQ_ERR_NULL;
     if (N < 0 || a->M < 0 || !mq::valid_k(a->K)) return MQ_ERR_SHAPE;
     int rc = mq::check_plane(a, a->M, a->K);
     if (rc != MQ_OK || N == 0 || a->M == 0) return rc;
     if (!mq::has_op(a) || !w || !out) return MQ_ERR_NULL;
     if (!mq::aligned16(w) || !mq::aligned16(out)) return MQ_ERR_ALIGN;
+    return MQ_OK;
+}
+
+int check_gemm(const mq_q8_plane* a, const void* w, int N, const float* out) {
+    const int rc = check_gemm_args(a, w, N, out);
+    if (rc != MQ_OK || N == 0 || a->M == 0) return rc;
     return mq::check_arch();
 }
 
@@ -1171,10 +1178,12 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
 // together fill at least one round of the grid, else two ordinary calls.
 int launch_gemm_q4k_pair(const mq_q8_plane* a, const void* w0, int N0, float* out0, const void* w1, int N1,
                          float* out1, cudaStream_t stream) {
-    int rc = check_gemm(a, w0, N0, out0);
-    if (rc == MQ_OK) rc = check_gemm(a, w1, N1, out1);
+    int rc = check_gemm_args(a, w0, N0, out0);
+    if (rc == MQ_OK) rc = check_gemm_args(a, w1, N1, out1);
     if (rc != MQ_OK) return rc;
-    if (a->M == 0) return MQ_OK;
+    if (a->M == 0 || (N0 == 0 && N1 == 0)) return MQ_OK;
+    rc = mq::check_arch();
+    if (rc != MQ_OK) return rc;
     const int M = a->M, K = a->K, S = K / mq::QK_K;
     if (ranges_overlap(out0, (size_t)M * N0 * sizeof(float), out1, (size_t)M * N1 * sizeof(float))) return MQ_ERR_SHAPE;
     const int bt = token_tile(M), sms = mq::num_sms();

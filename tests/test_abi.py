@@ -125,3 +125,28 @@ def test_matmul_validation_before_any_cuda_call(L):
     assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 256, ctypes.byref(p9), null) == mq.MQ_ERR_NULL
     p10 = _plane(4, 256, 16, None, 16)
     assert L.mq_quantize_q8(ctypes.c_void_p(16), 4, 256, ctypes.byref(p10), null) == mq.MQ_ERR_NULL
+
+
+def test_pair_and_static_gemm_validation_before_any_cuda_call(L):
+    """mq_gemm_q4k_pair checks both problems (either one's bad argument is reported before
+    anything runs); mq_gemm_q6k_static checks as mq_gemm_q6k does."""
+    null = None
+    p1 = _plane(1, 512, 16, 16, 16, 16, 16, 16)
+    fn = L.mq_gemm_q4k_pair
+    fn.restype = ctypes.c_int
+    v = ctypes.c_void_p
+    assert fn(None, v(16), 8, v(16), v(16), 8, v(16), null) == mq.MQ_ERR_NULL
+    assert fn(ctypes.byref(p1), None, 8, v(16), v(16), 8, v(16), null) == mq.MQ_ERR_NULL
+    assert fn(ctypes.byref(p1), v(16), 8, v(16), None, 8, v(16), null) == mq.MQ_ERR_NULL
+    assert fn(ctypes.byref(p1), v(16), 8, v(16), v(16), 8, None, null) == mq.MQ_ERR_NULL
+    assert fn(ctypes.byref(p1), v(16), 8, v(16), v(24), 8, v(16), null) == mq.MQ_ERR_ALIGN
+    assert fn(ctypes.byref(p1), v(16), -1, v(16), v(16), 8, v(16), null) == mq.MQ_ERR_SHAPE
+    assert fn(ctypes.byref(p1), v(16), 8, v(16), v(16), -1, v(16), null) == mq.MQ_ERR_SHAPE
+    assert fn(ctypes.byref(_plane(1, 300, 16, 16, 16, 16, 16, 16)), v(16), 8, v(16), v(16), 8, v(16), null) == mq.MQ_ERR_SHAPE
+    s = L.mq_gemm_q6k_static
+    s.restype = ctypes.c_int
+    assert s(None, v(16), 8, v(16), null) == mq.MQ_ERR_NULL
+    assert s(ctypes.byref(p1), v(24), 8, v(16), null) == mq.MQ_ERR_ALIGN
+    assert s(ctypes.byref(p1), v(16), -1, v(16), null) == mq.MQ_ERR_SHAPE
+    assert s(ctypes.byref(p1), v(16), 0, None, null) == mq.MQ_OK      # N == 0: no-op
+    assert mq.status_str(mq.MQ_ERR_SCRATCH).startswith("MQ_ERR_SCRATCH")
