@@ -207,8 +207,6 @@ class Stack:
         self.p_last = mq.Plane.empty(1, HID, dev, op=False)
         self.logits = torch.empty((VOCAB,), **f32)
         self.q4_events = []
-        self.pside = torch.cuda.Stream(device=dev)   # attn_v of each prefill layer
-        self.pev_rms, self.pev_v = torch.cuda.Event(), torch.cuda.Event()
         if decode:
             self.dx = S.normal((1, D_HID), seed, "d.x", device=dev)
             self.dattn = S.normal((1, D_HID), seed, "d.attn", device=dev)
@@ -249,23 +247,14 @@ class Stack:
     def step(self, time_q4=False):
         mq = self.mq
         planes = {"rms": self.p_rms, "rms2": self.p_rms2, "attn": self.p_attn, "swiglu": self.p_ffn}
-        main = torch.cuda.current_stream()
         for l in range(LAYERS):
             W = self.W[l]
-            if l > 0:
-                main.wait_event(self.pev_v)   # the previous layer's V has read p_rms
             mq.mq_rms_quant(self.x, self.rms_w[l], EPS, self.p_rms)
-            # attn_v reads the same plane and nothing in the layer reads its output: it runs on a
-            # second stream, its tiles filling the SMs the other GEMMs' last rounds leave idle
-            self.pev_rms.record(main)
-            self.pside.wait_event(self.pev_rms)
-            mq.gemm("q6k", self.p_rms, W["v"], KVD, self.out["v"], stream=self.pside)
-            self.pev_v.record(self.pside)
             mq.mq_quantize_q8(self.attn, self.p_attn)
             mq.mq_rms_quant(self.x, self.rms2_w[l], EPS, self.p_rms2)
             for name, kind, N, K, src in PREFILL_MATS:
-                if name in ("k", "v"):
-                    continue   # k with q below, v on the second stream above
+                if name == "k":
+                    continue   # with q, below
                 if name == "q":   # attn_q and attn_k read the same plane: one paired call
                     mq.mq_gemm_q4k_pair(planes[src], W["q"], N, self.out["q"], W["k"], KVD, self.out["k"])
                     continue
@@ -281,7 +270,6 @@ class Stack:
                     mq.gemm(kind, planes[src], W[name], N, self.out[name])
         mq.mq_rms_quant(self.out["down"][-1:], self.final_w, EPS, self.p_last)
         mq.mq_gemv_q6k_packed(self.p_last, self.lm_head, VOCAB, self.logits)
-        main.wait_event(self.pev_v)   # the step ends when the last V does
 
     def decode_step(self):
         mq = self.mq
